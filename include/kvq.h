@@ -1,0 +1,202 @@
+/*
+ * kvq.h -- C ABI of the paged quantized KV-cache library (GB300, sm_103a).
+ *
+ * One decode step of an LLM over a block-paged KV cache held in INT8 / FP8
+ * codes with fp32 scales (or plain FP16 for selected layers):
+ *
+ *   kvq_alloc_pool   one pool of fixed-size physical blocks per layer
+ *   kvq_append       quantize the new tokens' K/V and scatter them into slots
+ *   kvq_paged_decode attention of each new Q over its sequence's cached K/V,
+ *                    reached through a block table, dequantized on the fly
+ *
+ * Sources (the pages this method is described on):
+ *   [KVC]  "KV Cache优化实战：大模型推理显存占用与加速方案详解",
+ *          0539edu.com/news/5800990
+ *   [P402] xpshop.cn/articles/article-402.html (INT8 KV + paged cache)
+ *   [P312] xpshop.cn/articles/article-312.html (PagedAttention + FP8/INT8 KV)
+ *
+ * Conventions shared by every call:
+ *   - Pointers are DEVICE pointers unless a comment says "host".
+ *   - fp16 data is IEEE binary16, passed as kvq_half (its 16 bits).
+ *   - Every call that takes a stream is asynchronous on that stream; its
+ *     return value reports only the host-side argument checks (and launch
+ *     errors).  Errors found on the device -- a slot or block id outside the
+ *     pool, a context longer than the caller promised, a pipeline wait that
+ *     ran out -- set an error word inside the pool; the offending token or
+ *     block is skipped and nothing faults.  kvq_get_error() reads and clears it.
+ *   - The library allocates device memory only in kvq_alloc_pool (and only when
+ *     the caller passes no buffer).  Decode scratch ("workspace") comes from
+ *     the caller.
+ *   - Thread safety: calls on different pools may run concurrently; calls on
+ *     one pool must be ordered by the caller (one stream, or events).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvq_half; /* IEEE binary16 bits */
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent shape      */
+    KVQ_ERR_UNSUPPORTED = 2,  /* valid but not built (head_dim, group, block)    */
+    KVQ_ERR_CUDA = 3,         /* a CUDA runtime call failed                      */
+    KVQ_ERR_OUT_OF_RANGE = 4, /* device: slot / block id / length out of range   */
+    KVQ_ERR_WORKSPACE = 5,    /* decode workspace smaller than required          */
+    KVQ_ERR_TIMEOUT = 6       /* device: a bounded pipeline wait gave up         */
+} kvq_status;
+
+/* Cache formats ([KVC] §2.3: INT8 absmax-symmetric with per-token, per-channel
+ * or per-group scales; FP8; [KVC] §3.3 / [P312] §三: selected layers stay FP16). */
+typedef enum {
+    KVQ_FP16 = 0,              /* fp16 values, no scale                              */
+    KVQ_INT8_PER_TOKEN = 1,    /* one fp32 scale per (token, K|V) over all kv heads  */
+    KVQ_INT8_PER_CHANNEL = 2,  /* static fp32 scale per (K|V, kv head, channel)      */
+    KVQ_INT8_PER_GROUP = 3,    /* one fp32 scale per `group` contiguous channels of
+                                  one (token, kv head, K|V) vector                   */
+    KVQ_FP8_E4M3_PER_TOKEN = 4 /* e4m3 codes, one fp32 scale per (token, K|V)        */
+} kvq_dtype;
+
+typedef struct kvq_pool kvq_pool; /* opaque; one per layer */
+
+/* Byte accounting of a pool ([KVC] §1.2: KV bytes = 2 x tokens x kv_heads x
+ * head_dim x bytes per layer).  code_bytes is exactly that formula for
+ * num_blocks*block_size tokens; scales and the small header are separate. */
+typedef struct {
+    size_t total_bytes;  /* everything kvq_alloc_pool needs (header + regions)  */
+    size_t code_bytes;   /* 2 * num_blocks * block_size * kv_heads * head_dim * elem */
+    size_t scale_bytes;  /* fp32 scales of every format that has them           */
+    size_t header_bytes; /* device error word and padding                       */
+    size_t page_bytes;   /* bytes of one (block, kv head) page: K+V codes (+ group scales) */
+} kvq_pool_layout;
+
+/* Byte accounting for the given geometry, without allocating.  Returns
+ * KVQ_ERR_INVALID_ARG / KVQ_ERR_UNSUPPORTED for a geometry kvq_alloc_pool would
+ * refuse.  `out` is a host pointer.  Host only; needs no GPU. */
+kvq_status kvq_pool_layout_query(int64_t num_blocks, int block_size, int kv_heads,
+                                 int head_dim, kvq_dtype dtype, int group,
+                                 kvq_pool_layout* out);
+
+/* Total bytes of kvq_pool_layout_query (0 for a refused geometry). */
+size_t kvq_pool_bytes(int64_t num_blocks, int block_size, int kv_heads, int head_dim,
+                      kvq_dtype dtype, int group);
+
+/* Create a pool ([KVC] §2.2 PagedAttention: fixed-size physical blocks, e.g.
+ * 16 tokens, reached through a per-request block table; [P312] §三: blocks of
+ * 16 or 32 tokens).
+ *   num_blocks : physical blocks (>= 1)
+ *   block_size : tokens per block; a multiple of 16, at most 256
+ *   kv_heads   : KV heads (>= 1); head_dim: 64 or 128
+ *   group      : channels per scale for KVQ_INT8_PER_GROUP (a multiple of 16
+ *                that divides head_dim); ignored for other formats
+ *   device_buf : caller-owned device memory of buf_bytes >= kvq_pool_bytes(..),
+ *                256-byte aligned; NULL makes the library cudaMalloc (and later
+ *                cudaFree) the pool on the current device.
+ *   out        : host pointer that receives the handle.
+ * The pool's contents are unspecified until written by kvq_append, except
+ * that the error word is cleared and per-channel scales are set to zero.
+ * Synchronous.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+kvq_status kvq_alloc_pool(int64_t num_blocks, int block_size, int kv_heads, int head_dim,
+                          kvq_dtype dtype, int group, void* device_buf, size_t buf_bytes,
+                          kvq_pool** out);
+
+/* Release the handle; frees device memory only if the library allocated it.
+ * Synchronises the device first when it frees.  NULL is accepted. */
+kvq_status kvq_free_pool(kvq_pool* pool);
+
+/* KVQ_INT8_PER_CHANNEL only: set the static scales ([KVC] §2.3 "per-channel:
+ * a scale per channel").  k_scale, v_scale: fp32 [kv_heads][head_dim] device
+ * arrays, copied into the pool on `stream`.  A zero scale quantizes its
+ * channel to code 0. */
+kvq_status kvq_set_channel_scales(kvq_pool* pool, const float* k_scale, const float* v_scale,
+                                  cudaStream_t stream);
+
+/* KVQ_INT8_PER_CHANNEL only: calibrate the static scales from T tokens:
+ * scale[kv][h][d] = max_t |x[t][h][d]| / 127 (fp32).  k, v: [T][kv_heads][head_dim]
+ * fp16.  T >= 1. */
+kvq_status kvq_calibrate_channel_scales(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
+                                        int64_t T, cudaStream_t stream);
+
+/* Quantize and scatter T new tokens ([KVC] §1.1: the decode step appends the
+ * new token's K/V to the cache; §2.3: absmax symmetric quantization).
+ *   k, v         : fp16 [T][kv_heads][head_dim]
+ *   slot_mapping : int64 [T]; token i goes to block slot/block_size, offset
+ *                  slot%block_size.  A negative slot skips the token.
+ * Per format: scale s = absmax/127 (INT8 dynamic) or absmax/448 (FP8), fp32
+ * IEEE division; code = clamp(round_half_even(x/s), -127, 127) for INT8,
+ * e4m3 round-to-nearest-even saturating for FP8; an all-zero group stores s=0
+ * and zero codes.  Per-channel uses the pool's static scales.  FP16 stores x.
+ * Two tokens with the same slot in one call race (result unspecified).
+ * Device errors: a slot >= num_blocks*block_size sets OUT_OF_RANGE and the
+ * token is skipped. */
+kvq_status kvq_append(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
+                      const int64_t* slot_mapping, int64_t T, cudaStream_t stream);
+
+/* Scratch bytes kvq_paged_decode needs for these sizes (split-K partials).
+ * May be 0.  Host only. */
+size_t kvq_decode_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,
+                                  int max_context_len);
+
+/* Decode attention over the paged cache ([KVC] §1.1 decode step, §2.1 GQA,
+ * §2.2 block table, §2.3 quantized KV; §4.3: dequantization fused into the
+ * attention kernel rather than a separate pass).
+ *   q             : fp16 [num_seqs][num_q_heads][head_dim]; num_q_heads is a
+ *                   multiple of kv_heads; Q head hq reads kv head hq / (num_q_heads/kv_heads)
+ *   block_table   : int32 [num_seqs][max_blocks_per_seq] physical block ids
+ *   context_lens  : int32 [num_seqs] tokens to attend (after this step's append)
+ *   max_context_len : host-side upper bound of context_lens, <= max_blocks_per_seq*block_size
+ *   sm_scale      : softmax scale (usually 1/sqrt(head_dim))
+ *   out           : fp32 [num_seqs][num_q_heads][head_dim]
+ *   workspace     : >= kvq_decode_workspace_bytes(..) bytes, 256-byte aligned
+ *                   (may be NULL when that is 0)
+ * out = softmax(q . k^T * sm_scale) v over tokens 0..L-1, with k^, v^ = code * scale.
+ * A sequence with L == 0 gets zeros.  Device errors: a block id outside the
+ * pool sets OUT_OF_RANGE and that block is skipped; L > max_context_len sets
+ * OUT_OF_RANGE and L is clamped. */
+kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                            int num_q_heads, const int32_t* block_table,
+                            int max_blocks_per_seq, const int32_t* context_lens,
+                            int max_context_len, float sm_scale, float* out,
+                            void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* As kvq_paged_decode, with an explicit split of each sequence's blocks across
+ * thread blocks: split_blocks > 0 forces that many blocks per split (split-K
+ * over the context, merged by log-sum-exp); 0 picks automatically. */
+size_t kvq_decode_workspace_bytes_ex(const kvq_pool* pool, int num_seqs, int num_q_heads,
+                                     int max_context_len, int split_blocks);
+kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                               int num_q_heads, const int32_t* block_table,
+                               int max_blocks_per_seq, const int32_t* context_lens,
+                               int max_context_len, float sm_scale, float* out,
+                               void* workspace, size_t ws_bytes, int split_blocks,
+                               cudaStream_t stream);
+
+/* Read back n slots in a canonical layout (for tests and debugging).
+ *   codes_out  : [n][2][kv_heads][head_dim] elements of the pool's code type
+ *                (int8, e4m3 byte, or fp16)
+ *   scales_out : per-group [n][2][kv_heads][head_dim/group] fp32;
+ *                per-token [n][2] fp32; may be NULL (and is ignored) for
+ *                FP16 and per-channel pools
+ * A slot outside the pool sets OUT_OF_RANGE and its output is left untouched. */
+kvq_status kvq_read_slots(const kvq_pool* pool, const int64_t* slots, int64_t n,
+                          void* codes_out, float* scales_out, cudaStream_t stream);
+
+/* Synchronise `stream`, read and clear the pool's device error word.
+ * Returns KVQ_OK, KVQ_ERR_OUT_OF_RANGE or KVQ_ERR_TIMEOUT (the first that is set). */
+kvq_status kvq_get_error(kvq_pool* pool, cudaStream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

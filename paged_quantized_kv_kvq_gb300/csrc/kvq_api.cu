@@ -1,0 +1,311 @@
+// kvq_api.cu -- the C ABI (include/kvq.h): pool creation and byte accounting,
+// host-side argument checks, and dispatch to the kernels.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "kvq.h"
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+using kvq::PoolView;
+
+struct kvq_pool {
+  PoolView view;
+  void* base = nullptr;
+  size_t total_bytes = 0;
+  bool owned = false;
+  int device = 0;
+  kvq_pool_layout layout{};
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool valid_dtype(int d) { return d >= KVQ_FP16 && d <= KVQ_FP8_E4M3_PER_TOKEN; }
+
+// Geometry check + byte accounting.  Fills `view` offsets relative to base 0.
+kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int group,
+                      kvq_pool_layout* lay, PoolView* view, size_t* off_pages, size_t* off_tok,
+                      size_t* off_chan) {
+  if (num_blocks < 1 || bs < 1 || Hkv < 1 || D < 1 || !valid_dtype(dtype) || lay == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (D % 16 != 0) return KVQ_ERR_INVALID_ARG;
+  if (bs % 16 != 0 || bs > 256) return KVQ_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  int ng = 1;
+  if (dtype == KVQ_INT8_PER_GROUP) {
+    if (group <= 0 || D % group != 0) return KVQ_ERR_INVALID_ARG;
+    if (group % 16 != 0) return KVQ_ERR_UNSUPPORTED;
+    ng = D / group;
+  } else {
+    group = 0;
+  }
+  const int esize = dtype == KVQ_FP16 ? 2 : 1;
+  const size_t code_bytes = (size_t)bs * D * esize;  // K (or V) codes of one page
+  const size_t page_scale = dtype == KVQ_INT8_PER_GROUP ? 2 * (size_t)bs * ng * 4 : 0;
+  const size_t page_bytes = 2 * code_bytes + page_scale;
+  const size_t n_pages = (size_t)num_blocks * Hkv;
+  size_t off = kvq::kHeaderBytes;
+  const size_t op = off;
+  off = align_up(off + n_pages * page_bytes, 256);
+  const size_t ot = off;
+  const bool tok = dtype == KVQ_INT8_PER_TOKEN || dtype == KVQ_FP8_E4M3_PER_TOKEN;
+  const size_t tok_bytes = tok ? (size_t)num_blocks * 2 * bs * 4 : 0;
+  off = align_up(off + tok_bytes, 256);
+  const size_t oc = off;
+  const size_t chan_bytes = dtype == KVQ_INT8_PER_CHANNEL ? 2 * (size_t)Hkv * D * 4 : 0;
+  off = align_up(off + chan_bytes, 256);
+
+  lay->total_bytes = off;
+  lay->code_bytes = 2 * (size_t)num_blocks * bs * Hkv * D * esize;
+  lay->scale_bytes = n_pages * page_scale + tok_bytes + chan_bytes;
+  lay->header_bytes = off - lay->code_bytes - lay->scale_bytes;
+  lay->page_bytes = page_bytes;
+  if (view) {
+    view->num_blocks = num_blocks;
+    view->bs = bs;
+    view->Hkv = Hkv;
+    view->D = D;
+    view->fmt = dtype;
+    view->group = group;
+    view->ng = ng;
+    view->esize = esize;
+    view->sub_bytes = 16 * D * esize;
+    view->code_bytes = static_cast<int>(code_bytes);
+    view->page_bytes = static_cast<int>(page_bytes);
+  }
+  if (off_pages) *off_pages = op;
+  if (off_tok) *off_tok = ot;
+  if (off_chan) *off_chan = oc;
+  return KVQ_OK;
+}
+
+int device_sms() {
+  static int cached[kvq::kMaxDevicesApi] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < kvq::kMaxDevicesApi && cached[dev] > 0) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 152;
+  if (dev >= 0 && dev < kvq::kMaxDevicesApi) cached[dev] = sms;
+  return sms;
+}
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_pool_layout_query(int64_t num_blocks, int block_size, int kv_heads, int head_dim,
+                                 kvq_dtype dtype, int group, kvq_pool_layout* out) {
+  return layout_for(num_blocks, block_size, kv_heads, head_dim, dtype, group, out, nullptr,
+                    nullptr, nullptr, nullptr);
+}
+
+size_t kvq_pool_bytes(int64_t num_blocks, int block_size, int kv_heads, int head_dim,
+                      kvq_dtype dtype, int group) {
+  kvq_pool_layout lay{};
+  if (layout_for(num_blocks, block_size, kv_heads, head_dim, dtype, group, &lay, nullptr, nullptr,
+                 nullptr, nullptr) != KVQ_OK)
+    return 0;
+  return lay.total_bytes;
+}
+
+kvq_status kvq_alloc_pool(int64_t num_blocks, int block_size, int kv_heads, int head_dim,
+                          kvq_dtype dtype, int group, void* device_buf, size_t buf_bytes,
+                          kvq_pool** out) {
+  if (out == nullptr) return KVQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  kvq_pool_layout lay{};
+  PoolView view{};
+  size_t op = 0, ot = 0, oc = 0;
+  kvq_status st = layout_for(num_blocks, block_size, kv_heads, head_dim, dtype, group, &lay, &view,
+                             &op, &ot, &oc);
+  if (st != KVQ_OK) return st;
+  if (view.page_bytes <= 0 || (size_t)view.page_bytes != lay.page_bytes) return KVQ_ERR_UNSUPPORTED;
+  void* base = device_buf;
+  bool owned = false;
+  if (base == nullptr) {
+    if (cudaMalloc(&base, lay.total_bytes) != cudaSuccess) return KVQ_ERR_CUDA;
+    owned = true;
+  } else {
+    if (buf_bytes < lay.total_bytes || (reinterpret_cast<uintptr_t>(base) & 255) != 0)
+      return KVQ_ERR_INVALID_ARG;
+  }
+  // Clear the header (error word) and the per-channel scales.
+  cudaError_t e = cudaMemset(base, 0, kvq::kHeaderBytes);
+  if (e == cudaSuccess && dtype == KVQ_INT8_PER_CHANNEL)
+    e = cudaMemset(static_cast<char*>(base) + oc, 0, 2 * (size_t)kv_heads * head_dim * 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    if (owned) cudaFree(base);
+    return KVQ_ERR_CUDA;
+  }
+  kvq_pool* p = new (std::nothrow) kvq_pool;
+  if (p == nullptr) {
+    if (owned) cudaFree(base);
+    return KVQ_ERR_INVALID_ARG;
+  }
+  char* b = static_cast<char*>(base);
+  view.err = reinterpret_cast<int*>(b);
+  view.pages = b + op;
+  view.tok_scales = reinterpret_cast<float*>(b + ot);
+  view.chan_scales = reinterpret_cast<float*>(b + oc);
+  p->view = view;
+  p->base = base;
+  p->total_bytes = lay.total_bytes;
+  p->owned = owned;
+  p->layout = lay;
+  cudaGetDevice(&p->device);
+  *out = p;
+  return KVQ_OK;
+}
+
+kvq_status kvq_free_pool(kvq_pool* pool) {
+  if (pool == nullptr) return KVQ_OK;
+  kvq_status st = KVQ_OK;
+  if (pool->owned) {
+    if (cudaDeviceSynchronize() != cudaSuccess) st = KVQ_ERR_CUDA;
+    if (cudaFree(pool->base) != cudaSuccess) st = KVQ_ERR_CUDA;
+  }
+  delete pool;
+  return st;
+}
+
+kvq_status kvq_set_channel_scales(kvq_pool* pool, const float* k_scale, const float* v_scale,
+                                  cudaStream_t stream) {
+  if (pool == nullptr || k_scale == nullptr || v_scale == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (pool->view.fmt != KVQ_INT8_PER_CHANNEL) return KVQ_ERR_INVALID_ARG;
+  const size_t n = (size_t)pool->view.Hkv * pool->view.D * sizeof(float);
+  cudaError_t e = cudaMemcpyAsync(pool->view.chan_scales, k_scale, n, cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(reinterpret_cast<char*>(pool->view.chan_scales) + n, v_scale, n,
+                        cudaMemcpyDeviceToDevice, stream);
+  return from_cuda(e);
+}
+
+kvq_status kvq_calibrate_channel_scales(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
+                                        int64_t T, cudaStream_t stream) {
+  if (pool == nullptr || k == nullptr || v == nullptr || T < 1) return KVQ_ERR_INVALID_ARG;
+  if (pool->view.fmt != KVQ_INT8_PER_CHANNEL) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(kvq::launch_calibrate(pool->view, reinterpret_cast<const __half*>(k),
+                                         reinterpret_cast<const __half*>(v), T, stream));
+}
+
+kvq_status kvq_append(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
+                      const int64_t* slot_mapping, int64_t T, cudaStream_t stream) {
+  if (pool == nullptr || T < 0) return KVQ_ERR_INVALID_ARG;
+  if (T == 0) return KVQ_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (T > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(kvq::launch_append(pool->view, reinterpret_cast<const __half*>(k),
+                                      reinterpret_cast<const __half*>(v), slot_mapping, T, stream));
+}
+
+size_t kvq_decode_workspace_bytes_ex(const kvq_pool* pool, int num_seqs, int num_q_heads,
+                                     int max_context_len, int split_blocks) {
+  if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || num_q_heads % pool->view.Hkv != 0)
+    return 0;
+  kvq::DecodePlan plan;
+  if (!kvq::plan_decode(pool->view, num_seqs, num_q_heads, max_context_len, split_blocks,
+                        device_sms(), &plan))
+    return 0;
+  return plan.ws_bytes;
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,
+                                  int max_context_len) {
+  return kvq_decode_workspace_bytes_ex(pool, num_seqs, num_q_heads, max_context_len, 0);
+}
+
+kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                               int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, float sm_scale,
+                               float* out, void* workspace, size_t ws_bytes, int split_blocks,
+                               cudaStream_t stream) {
+  if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 ||
+      max_context_len < 0 || split_blocks < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KVQ_OK;
+  if (q == nullptr || block_table == nullptr || context_lens == nullptr || out == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % pool->view.Hkv != 0) return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * pool->view.bs) return KVQ_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) & 15) return KVQ_ERR_INVALID_ARG;
+  kvq::DecodePlan plan;
+  if (!kvq::plan_decode(pool->view, num_seqs, num_q_heads, max_context_len, split_blocks,
+                        device_sms(), &plan))
+    return KVQ_ERR_UNSUPPORTED;
+  if (plan.ws_bytes > 0) {
+    if (workspace == nullptr || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return KVQ_ERR_INVALID_ARG;
+  }
+  kvq::DecodeArgs a;
+  a.pool = pool->view;
+  a.q = reinterpret_cast<const __half*>(q);
+  a.table = block_table;
+  a.lens = context_lens;
+  a.out = out;
+  a.workspace = workspace;
+  a.S = num_seqs;
+  a.Hq = num_q_heads;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_ctx = max_context_len;
+  a.sm_scale = sm_scale;
+  return from_cuda(kvq::launch_decode(a, plan, stream));
+}
+
+kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
+                            const int32_t* block_table, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context_len, float sm_scale,
+                            float* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return kvq_paged_decode_ex(pool, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq,
+                             context_lens, max_context_len, sm_scale, out, workspace, ws_bytes, 0,
+                             stream);
+}
+
+kvq_status kvq_read_slots(const kvq_pool* pool, const int64_t* slots, int64_t n, void* codes_out,
+                          float* scales_out, cudaStream_t stream) {
+  if (pool == nullptr || n < 0) return KVQ_ERR_INVALID_ARG;
+  if (n == 0) return KVQ_OK;
+  if (slots == nullptr || codes_out == nullptr || n > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
+  const int f = pool->view.fmt;
+  const bool has_scales = f == KVQ_INT8_PER_GROUP || f == KVQ_INT8_PER_TOKEN || f == KVQ_FP8_E4M3_PER_TOKEN;
+  return from_cuda(kvq::launch_read_slots(pool->view, slots, n, codes_out,
+                                          has_scales ? scales_out : nullptr, stream));
+}
+
+kvq_status kvq_get_error(kvq_pool* pool, cudaStream_t stream) {
+  if (pool == nullptr) return KVQ_ERR_INVALID_ARG;
+  int host = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpy(&host, pool->view.err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(pool->view.err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  if (host & kvq::ERR_RANGE) return KVQ_ERR_OUT_OF_RANGE;
+  if (host & kvq::ERR_TIMEOUT) return KVQ_ERR_TIMEOUT;
+  return KVQ_OK;
+}
+
+const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported geometry";
+    case KVQ_ERR_CUDA: return "CUDA runtime error";
+    case KVQ_ERR_OUT_OF_RANGE: return "slot, block id or context length out of range";
+    case KVQ_ERR_WORKSPACE: return "decode workspace too small";
+    case KVQ_ERR_TIMEOUT: return "a bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

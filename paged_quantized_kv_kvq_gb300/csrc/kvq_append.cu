@@ -1,0 +1,262 @@
+// kvq_append.cu -- quantize-and-scatter of new tokens, per-channel
+// calibration, and a canonical read-back of slots (sm_103a).
+//
+// Method ("KV Cache优化实战：大模型推理显存占用与加速方案详解",
+// 0539edu.com/news/5800990): each decode step appends the new token's K/V to
+// the cache (§1.1) into fixed-size physical blocks (§2.2); K/V are stored with
+// absmax-symmetric INT8 (per-token, per-channel or per-group-of-128/64 scales)
+// or FP8 (§2.3, §3.3).  Scale = absmax/127 (INT8) or absmax/448 (e4m3) in
+// fp32 with an IEEE division; code = clamp(round_half_even(x / scale), +-127),
+// or e4m3 round-to-nearest-even with saturation; an all-zero group stores
+// scale 0 and zero codes.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kAppendThreads = 128;
+
+struct AppendParams {
+  PoolView pool;
+  const __half* k;
+  const __half* v;
+  const int64_t* slots;
+  int64_t T;
+};
+
+__device__ __forceinline__ float absmax8(const __half2 (&x)[4]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a = fmaxf(a, fabsf(__low2float(x[i])));
+    a = fmaxf(a, fabsf(__high2float(x[i])));
+  }
+  return a;
+}
+
+__device__ __forceinline__ int8_t quant_i8(float x, float s) {
+  if (s == 0.f) return 0;
+  float q = rintf(__fdiv_rn(x, s));
+  q = fminf(fmaxf(q, -127.f), 127.f);
+  return static_cast<int8_t>(q);
+}
+
+__device__ __forceinline__ uint8_t quant_e4m3(float x, float s) {
+  if (s == 0.f) return 0;
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
+}
+
+// One CTA per (token, K|V).  Each thread owns 8 consecutive channels of one
+// kv head per iteration (a 16-byte load).
+template <int FMT>
+__global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const AppendParams p) {
+  const PoolView& pool = p.pool;
+  const int64_t t = blockIdx.x;
+  const int kv = blockIdx.y;
+  const int64_t slot = p.slots[t];
+  if (slot < 0) return;
+  if (slot >= pool.num_blocks * pool.bs) {
+    if (threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
+    return;
+  }
+  const int64_t blk = slot / pool.bs;
+  const int off = static_cast<int>(slot % pool.bs);
+  const int sub = off >> 4, tt = off & 15;
+  const int D = pool.D, Hkv = pool.Hkv;
+  const int per = Hkv * D;
+  const __half* x = (kv == 0 ? p.k : p.v) + t * per;
+
+  __shared__ float red[kAppendThreads / 32];
+  float tok_scale = 0.f;
+  if constexpr (FMT == FMT_INT8_TOKEN || FMT == FMT_FP8_TOKEN) {
+    float a = 0.f;
+    for (int c = threadIdx.x * 8; c < per; c += kAppendThreads * 8) {
+      uint4 raw = *reinterpret_cast<const uint4*>(x + c);
+      a = fmaxf(a, absmax8(*reinterpret_cast<__half2(*)[4]>(&raw)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+    __syncthreads();
+    a = red[0];
+#pragma unroll
+    for (int w = 1; w < kAppendThreads / 32; ++w) a = fmaxf(a, red[w]);
+    tok_scale = a == 0.f ? 0.f : __fdiv_rn(a, FMT == FMT_FP8_TOKEN ? 448.f : 127.f);
+    if (threadIdx.x == 0) pool.tok_scales[(blk * 2 + kv) * pool.bs + off] = tok_scale;
+  }
+
+  // Whole warps iterate together (the per-group reduction shuffles across
+  // lanes); lanes past the end carry zeros and store nothing.
+  for (int base = 0; base < per; base += kAppendThreads * 8) {
+    const int c = base + threadIdx.x * 8;
+    const bool act = c < per;
+    const int h = act ? c / D : 0, d0 = act ? c - h * D : 0;
+    char* page = pool.pages + (blk * Hkv + h) * pool.page_bytes;
+    char* tile = page + (kv == 0 ? 0 : pool.code_bytes) + sub * pool.sub_bytes;
+    uint4 raw = act ? *reinterpret_cast<const uint4*>(x + c) : make_uint4(0, 0, 0, 0);
+    const __half2(&xv)[4] = *reinterpret_cast<const __half2(*)[4]>(&raw);
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __low2float(xv[i]);
+      f[2 * i + 1] = __high2float(xv[i]);
+    }
+
+    if constexpr (FMT == FMT_FP16) {
+      if (!act) continue;
+      const uint16_t* hb = reinterpret_cast<const uint16_t*>(&raw);
+      if (kv == 0) {
+        // channels d0..d0+3 and d0+4..d0+7 are two 4-element words
+        *reinterpret_cast<uint2*>(tile + k_tile_offset(tt, d0, D, 2)) = make_uint2(raw.x, raw.y);
+        *reinterpret_cast<uint2*>(tile + k_tile_offset(tt, d0 + 4, D, 2)) = make_uint2(raw.z, raw.w);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<uint16_t*>(tile + v_tile_offset(tt, d0 + i, D, 2)) = hb[i];
+      }
+    } else {
+      uint8_t code[8];
+      if constexpr (FMT == FMT_INT8_GROUP) {
+        // group = g contiguous channels of this head: g/8 consecutive lanes
+        const int lanes = pool.group >> 3;
+        float a = absmax8(xv);
+        for (int o = lanes >> 1; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        const float s = a == 0.f ? 0.f : __fdiv_rn(a, 127.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(quant_i8(f[i], s));
+        if (act && (d0 % pool.group) == 0) {
+          float* sc = reinterpret_cast<float*>(page + 2 * pool.code_bytes) +
+                      (kv * pool.bs + off) * pool.ng + d0 / pool.group;
+          *sc = s;
+        }
+      } else if constexpr (FMT == FMT_INT8_TOKEN) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(quant_i8(f[i], tok_scale));
+      } else if constexpr (FMT == FMT_FP8_TOKEN) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) code[i] = quant_e4m3(f[i], tok_scale);
+      } else {  // FMT_INT8_CHANNEL
+        const float* cs = pool.chan_scales + ((int64_t)kv * Hkv + h) * D + d0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(quant_i8(f[i], cs[i]));
+      }
+      if (!act) continue;
+      if (kv == 0) {
+        const uint32_t w0 = code[0] | (code[1] << 8) | (code[2] << 16) | ((uint32_t)code[3] << 24);
+        const uint32_t w1 = code[4] | (code[5] << 8) | (code[6] << 16) | ((uint32_t)code[7] << 24);
+        *reinterpret_cast<uint32_t*>(tile + k_tile_offset(tt, d0, D, 1)) = w0;
+        *reinterpret_cast<uint32_t*>(tile + k_tile_offset(tt, d0 + 4, D, 1)) = w1;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tile[v_tile_offset(tt, d0 + i, D, 1)] = static_cast<char>(code[i]);
+      }
+    }
+  }
+}
+
+// Per-channel calibration, pass 1: absmax of |x| per (K|V, channel) over a
+// chunk of tokens, merged with an integer max on the (non-negative) float bits.
+__global__ void kvq_calib_absmax_kernel(PoolView pool, const __half* k, const __half* v,
+                                        int64_t T, int64_t chunk) {
+  const int C = pool.Hkv * pool.D;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int kv = blockIdx.y;
+  if (c >= C) return;
+  const __half* x = kv == 0 ? k : v;
+  const int64_t t0 = blockIdx.z * chunk, t1 = min(T, t0 + chunk);
+  float a = 0.f;
+  for (int64_t t = t0; t < t1; ++t) a = fmaxf(a, fabsf(__half2float(x[t * C + c])));
+  atomicMax(reinterpret_cast<unsigned int*>(pool.chan_scales) + kv * C + c, __float_as_uint(a));
+}
+
+// Pass 2: scale = absmax / 127 (fp32 IEEE division), in place.
+__global__ void kvq_calib_finish_kernel(PoolView pool) {
+  const int n = 2 * pool.Hkv * pool.D;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  pool.chan_scales[i] = __fdiv_rn(pool.chan_scales[i], 127.f);
+}
+
+// Canonical read-back: codes [n][2][Hkv][D], scales per format.
+__global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64_t n,
+                                      void* codes_out, float* scales_out) {
+  const int64_t i = blockIdx.x;
+  const int kv = blockIdx.y;
+  const int64_t slot = slots[i];
+  if (slot < 0 || slot >= pool.num_blocks * pool.bs) {
+    if (threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
+    return;
+  }
+  const int64_t blk = slot / pool.bs;
+  const int off = static_cast<int>(slot % pool.bs);
+  const int sub = off >> 4, tt = off & 15;
+  const int D = pool.D, per = pool.Hkv * D, es = pool.esize;
+  for (int c = threadIdx.x; c < per; c += blockDim.x) {
+    const int h = c / D, d = c - h * D;
+    const char* page = pool.pages + (blk * pool.Hkv + h) * pool.page_bytes;
+    const char* tile = page + (kv == 0 ? 0 : pool.code_bytes) + sub * pool.sub_bytes;
+    const int o = kv == 0 ? k_tile_offset(tt, d, D, es) : v_tile_offset(tt, d, D, es);
+    const int64_t dst = (i * 2 + kv) * per + c;
+    if (es == 2)
+      reinterpret_cast<uint16_t*>(codes_out)[dst] = *reinterpret_cast<const uint16_t*>(tile + o);
+    else
+      reinterpret_cast<uint8_t*>(codes_out)[dst] = *reinterpret_cast<const uint8_t*>(tile + o);
+  }
+  if (scales_out == nullptr) return;
+  if (pool.fmt == FMT_INT8_GROUP) {
+    const int ns = pool.Hkv * pool.ng;
+    for (int c = threadIdx.x; c < ns; c += blockDim.x) {
+      const int h = c / pool.ng, gi = c - h * pool.ng;
+      const char* page = pool.pages + (blk * pool.Hkv + h) * pool.page_bytes;
+      const float* sc = reinterpret_cast<const float*>(page + 2 * pool.code_bytes);
+      scales_out[(i * 2 + kv) * ns + c] = sc[(kv * pool.bs + off) * pool.ng + gi];
+    }
+  } else if (pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN) {
+    if (threadIdx.x == 0) scales_out[i * 2 + kv] = pool.tok_scales[(blk * 2 + kv) * pool.bs + off];
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
+                          const int64_t* slots, int64_t T, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  AppendParams p{pool, k, v, slots, T};
+  dim3 grid(static_cast<unsigned>(T), 2);
+  switch (pool.fmt) {
+    case FMT_FP16: kvq_append_kernel<FMT_FP16><<<grid, kAppendThreads, 0, st>>>(p); break;
+    case FMT_INT8_TOKEN: kvq_append_kernel<FMT_INT8_TOKEN><<<grid, kAppendThreads, 0, st>>>(p); break;
+    case FMT_INT8_CHANNEL: kvq_append_kernel<FMT_INT8_CHANNEL><<<grid, kAppendThreads, 0, st>>>(p); break;
+    case FMT_INT8_GROUP: kvq_append_kernel<FMT_INT8_GROUP><<<grid, kAppendThreads, 0, st>>>(p); break;
+    case FMT_FP8_TOKEN: kvq_append_kernel<FMT_FP8_TOKEN><<<grid, kAppendThreads, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,
+                             cudaStream_t st) {
+  const int C = pool.Hkv * pool.D;
+  cudaError_t e = cudaMemsetAsync(pool.chan_scales, 0, sizeof(float) * 2 * C, st);
+  if (e != cudaSuccess) return e;
+  const int64_t chunk = 256;
+  const int64_t nz = (T + chunk - 1) / chunk;
+  dim3 grid((C + 255) / 256, 2, static_cast<unsigned>(nz < 65535 ? nz : 65535));
+  const int64_t ch = (T + grid.z - 1) / grid.z;
+  kvq_calib_absmax_kernel<<<grid, 256, 0, st>>>(pool, k, v, T, ch);
+  kvq_calib_finish_kernel<<<(2 * C + 255) / 256, 256, 0, st>>>(pool);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_t n,
+                              void* codes_out, float* scales_out, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(n), 2);
+  kvq_read_slots_kernel<<<grid, 256, 0, st>>>(pool, slots, n, codes_out, scales_out);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,56 @@
+// kvq_internal.h -- host-side declarations shared by the C ABI and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime_api.h>
+
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
+                          const int64_t* slots, int64_t T, cudaStream_t st);
+cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,
+                             cudaStream_t st);
+cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_t n,
+                              void* codes_out, float* scales_out, cudaStream_t st);
+
+// Launch geometry of one decode call.
+struct DecodePlan {
+  int pps = 0;          // blocks per split
+  int nsplit = 0;       // splits (grid.x)
+  int n_ht = 0;         // head tiles of 8 Q heads per kv head
+  int nstage_log2 = 0;  // pipeline stages per warp = 1 << nstage_log2
+  int stage_bytes = 0;  // bytes of one stage
+  int smem_bytes = 0;   // dynamic shared memory per CTA
+  size_t ws_bytes = 0;  // workspace (split partials); 0 when nsplit == 1
+};
+
+// Plan a decode call; `sms` is the device's SM count.  Returns false for an
+// unsupported geometry.
+bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blocks, int sms,
+                 DecodePlan* plan);
+
+struct DecodeArgs {
+  PoolView pool;
+  const __half* q;
+  const int* table;
+  const int* lens;
+  float* out;
+  void* workspace;
+  int S, Hq, max_blocks, max_ctx;
+  float sm_scale;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st);
+
+// Per-format kernel launchers (one translation unit each, compiled in parallel).
+struct DecodeLaunch;
+cudaError_t launch_decode_int8_group(const DecodeLaunch& l);
+cudaError_t launch_decode_fp16(const DecodeLaunch& l);
+cudaError_t launch_decode_token(const DecodeLaunch& l);
+cudaError_t launch_decode_channel(const DecodeLaunch& l);
+
+}  // namespace kvq
