@@ -1,0 +1,507 @@
+"""Benchmark of one decode step over a paged, quantized KV cache.
+
+A step is the whole hot path for every layer of a 32-layer model: quantize and
+append one new K/V token per sequence into the layer's pool, then run paged
+decode attention of the step's Q over each sequence's cached K/V.  The default
+workload is 64 sequences x 2048 tokens, 32 Q / 8 KV heads, head_dim 128, block
+16, INT8 per-group-128 KV; every layer has its own pool (32 pools, 9.8 GB), so
+no layer's reads can be served from L2.
+
+Prints one JSON line.  `value` is the effective HBM bandwidth of the step:
+algorithmic bytes (KV codes + scales + Q + block tables + context lengths read
+by decode, plus the append's fp16 input and code/scale output) over the
+device-timed step.  Also reported: decode tokens/s, the decode launch's
+roofline fraction, an end-to-end number through the Python API with host
+buffers, and the CPU oracle timed on a bounded sample on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Paged quantized-KV decode: effective HBM GB/s (% of peak) and decode tok/s"
+FORMAT_NAME = {0: "fp16", 1: "int8 per-token", 2: "int8 per-channel", 3: "int8 per-group",
+               4: "fp8 e4m3 per-token"}
+ESIZE = {0: 2, 1: 1, 2: 1, 3: 1, 4: 1}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_traffic.json")
+KERNEL_SOURCES = ["paged_quantized_kv_kvq_gb300/csrc/kvq_decode_impl.cuh",
+                  "paged_quantized_kv_kvq_gb300/csrc/kvq_common.cuh",
+                  "paged_quantized_kv_kvq_gb300/csrc/kvq_decode.cu"]
+
+
+# ----------------------------------------------------------------- byte model
+def layer_bytes(w, fmt, group, seqs=None):
+    """Algorithmic bytes of one layer's append + decode for the given sequences."""
+    seqs = np.arange(w.S) if seqs is None else np.asarray(seqs)
+    L = w.context_lens[seqs].astype(np.int64)
+    n = len(seqs)
+    es = ESIZE[fmt]
+    tok = int(L.sum())
+    codes = tok * w.Hkv * w.D * 2 * es
+    if fmt == 3:
+        scales = tok * w.Hkv * 2 * (w.D // group) * 4
+    elif fmt in (1, 4):
+        scales = tok * 2 * 4
+    elif fmt == 2:
+        scales = 2 * w.Hkv * w.D * 4
+    else:
+        scales = 0
+    q = n * w.Hq * w.D * 2
+    tables = int(((L + w.bs - 1) // w.bs).sum()) * 4 + n * 4
+    decode = codes + scales + q + tables
+    app_scales = {3: n * w.Hkv * 2 * (w.D // max(group, 1)) * 4, 1: n * 2 * 4, 4: n * 2 * 4}.get(fmt, 0)
+    append = n * w.Hkv * w.D * 2 * 2 + n * 8 + n * w.Hkv * w.D * 2 * es + app_scales
+    unique_codes = codes
+    if w.shared_prefix_tokens:
+        unique_codes -= (n - 1) * w.shared_prefix_tokens * w.Hkv * w.D * 2 * es
+    return {"decode": decode, "append": append, "codes": codes, "scales": scales,
+            "unique_codes": unique_codes, "output": n * w.Hq * w.D * 4}
+
+
+def step_bytes(w):
+    tot = {"decode": 0, "append": 0, "codes": 0, "scales": 0, "unique_codes": 0, "output": 0}
+    for fmt, group in w.layer_formats:
+        for k, v in layer_bytes(w, fmt, group).items():
+            tot[k] += v
+    return tot
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()
+
+
+def read_traffic(workload):
+    try:
+        rec = json.load(open(PROFILE_TRAFFIC))
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_sha256") != kernel_sha() or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        busy = [x for x in sm if mx and x > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [p for p in vis.split(",") if p.strip()]
+        if local_rank < len(parts) and parts[local_rank].strip().isdigit():
+            return int(parts[local_rank])
+    return local_rank
+
+
+# ----------------------------------------------------------------- oracle leg
+def oracle_sample(w, fmt, group, seqs, oracle_mod, synth, kv_heads=None):
+    """Set up the oracle's cache for `seqs` of layer 0 (untimed); returns a
+    callable that runs the step (append the new tokens, decode) on it.  With
+    kv_heads = n, only the first n KV heads (and their Q heads) take part."""
+    hk = w.Hkv if kv_heads is None else kv_heads
+    hq = hk * w.G
+    table = w.block_table[seqs]
+    nblk = [(int(w.context_lens[s]) + w.bs - 1) // w.bs for s in seqs]
+    used = np.unique(np.concatenate([table[i, :nblk[i]] for i in range(len(seqs))]))
+    remap = np.full(w.num_blocks, -1, np.int64)
+    remap[used] = np.arange(len(used))
+    ctable = np.where(table >= 0, remap[np.clip(table, 0, None)], 0).astype(np.int32)
+    cache = oracle_mod.OracleCache(fmt, len(used), w.bs, hk, w.D, group)
+    idx = w.fill_token_index()
+    keep = np.isin(idx[:, 0], seqs)
+    if w.shared_prefix_tokens and 0 not in seqs:
+        keep |= (idx[:, 0] == 0) & (idx[:, 1] < w.shared_prefix_tokens)
+    slots = w.fill_slots()[keep]
+    k, v = synth.kv_tokens(w, 0, idx[keep])
+    k, v = np.ascontiguousarray(k[:, :hk]), np.ascontiguousarray(v[:, :hk])
+    cs = remap[slots // w.bs] * w.bs + slots % w.bs
+    if fmt == 2:
+        cache.calibrate(k, v)
+    cache.append(k, v, cs)
+    ks, vs = synth.step_kv(w, 0)
+    st = w.step_slots()[seqs]
+    st = remap[st // w.bs] * w.bs + st % w.bs
+    q = np.ascontiguousarray(synth.queries(w, 0)[seqs][:, :hq])
+    lens = w.context_lens[seqs]
+    ks, vs = np.ascontiguousarray(ks[seqs][:, :hk]), np.ascontiguousarray(vs[seqs][:, :hk])
+
+    def run():
+        cache.append(ks, vs, st)
+        return cache.decode(q, ctable, lens)
+
+    return run
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """Time the oracle (as it stands) on host cores on a bounded sample of the
+    workload: layer 0, the first n sequences, n sized to ~budget_s of work."""
+    import oracle
+    from paged_quantized_kv_kvq_gb300 import synth
+
+    oracle.build()
+    fmt, group = w.layer_formats[0]
+    run1 = oracle_sample(w, fmt, group, [0], oracle, synth)
+    t0 = time.perf_counter()
+    run1()
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(w.S, round(budget_s / max(t1, 1e-3)))))
+    seqs = list(range(n))
+    run = oracle_sample(w, fmt, group, seqs, oracle, synth)
+    t0 = time.perf_counter()
+    run()
+    once = time.perf_counter() - t0
+    # repeat the same step (append rewrites the same slots) to ~budget_s of work
+    reps = int(max(1, min(50, round(budget_s / max(once, 1e-3)))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run()
+    dt = (time.perf_counter() - t0) / reps
+    b = layer_bytes(w, fmt, group, seqs)
+    nbytes = b["decode"] + b["append"]
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s",
+            "cores": min(oracle.num_threads(), n * w.Hq),
+            "kind": "oracle",
+            "sample": "layer 0 of %d, sequences 0..%d of %d (append of the step token + float64 "
+                      "paged decode) run %d times, %.2f s of CPU work, %d algorithmic bytes per run"
+                      % (w.layers, n - 1, w.S, reps, dt * reps, nbytes),
+            "seconds": dt, "bytes": nbytes}
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import paged_quantized_kv_kvq_gb300 as kvq
+    from paged_quantized_kv_kvq_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    kvq.lib()
+    w = synth.workload(args.workload, layers=args.layers)
+    stream = torch.cuda.current_stream()
+
+    # -- per-layer pools, filled with the cached tokens (untimed set-up)
+    pools = []
+    fill_slots = torch.from_numpy(w.fill_slots()).to(dev)
+    fill_idx = w.fill_token_index()
+    for layer, (fmt, group) in enumerate(w.layer_formats):
+        pool = kvq.KVPool(w.num_blocks, w.bs, w.Hkv, w.D, fmt, group, device=dev)
+        if w.drift_sigma > 0 or fmt == kvq.KVQ_INT8_PER_CHANNEL:
+            ks_, vs_ = [], []
+            for s in range(w.S):
+                t0 = w.shared_prefix_tokens if (s > 0 and w.shared_prefix_tokens) else 0
+                k, v = synth.device_kv(w, layer, s, 0, int(w.context_lens[s]) - 1, dev)
+                ks_.append(k[t0:]); vs_.append(v[t0:])
+            k_all, v_all = torch.cat(ks_), torch.cat(vs_)
+            if fmt == kvq.KVQ_INT8_PER_CHANNEL:
+                kvq.kvq_calibrate_channel_scales(pool.handle, k_all, v_all)
+            for a in range(0, k_all.shape[0], 1 << 16):
+                b = min(k_all.shape[0], a + (1 << 16))
+                pool.append(k_all[a:b], v_all[a:b], fill_slots[a:b])
+            del k_all, v_all, ks_, vs_
+        else:
+            n = fill_slots.numel()
+            for a in range(0, n, 1 << 16):
+                b = min(n, a + (1 << 16))
+                k, v = synth.device_kv(w, layer, -1, a, b, dev)
+                pool.append(k, v, fill_slots[a:b])
+        pools.append(pool)
+    torch.cuda.synchronize()
+    for p in pools:
+        assert p.error() == kvq.KVQ_OK
+
+    # -- step inputs, resident in HBM
+    L = w.layers
+    q = torch.stack([synth.device_queries(w, l, dev) for l in range(L)])
+    kn = torch.empty((L, w.S, w.Hkv, w.D), dtype=torch.float16, device=dev)
+    vn = torch.empty_like(kn)
+    for l in range(L):
+        for s in range(w.S):
+            pos = int(w.context_lens[s]) - 1
+            if w.drift_sigma > 0:
+                k, v = synth.device_kv(w, l, s, 0, pos + 1, dev)
+                kn[l, s], vn[l, s] = k[pos], v[pos]
+            else:
+                k, v = synth.device_kv(w, l, 10 ** 6 + s, pos, pos + 1, dev)
+                kn[l, s], vn[l, s] = k[0], v[0]
+    slots = torch.from_numpy(w.step_slots()).to(dev)
+    table = torch.from_numpy(w.block_table).to(dev)
+    lens = torch.from_numpy(w.context_lens).to(dev)
+    max_ctx = int(w.context_lens.max())
+    out = torch.empty((L, w.S, w.Hq, w.D), dtype=torch.float32, device=dev)
+    ws_need = max(kvq.kvq_decode_workspace_bytes(p.handle, w.S, w.Hq, max_ctx) for p in pools)
+    ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=dev)
+    sm_scale = w.D ** -0.5
+
+    def step(qq, kk, vv, sl, ln, oo, ev=None):
+        for l in range(L):
+            pools[l].append(kk[l], vv[l], sl, stream)
+            if ev is not None:
+                ev[l][0].record(stream)
+            kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l], ws,
+                                 0, stream)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step(q, kn, vn, slots, lens, out)
+    torch.cuda.synchronize()
+    for p in pools:
+        assert p.error() == kvq.KVQ_OK
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # -- device-timed region
+    K = args.steps
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(L)] for _ in range(K)]
+    sampler = ClockSampler(gpu_index(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        step(q, kn, vn, slots, lens, out, evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / K
+    dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(K) for l in range(L)]
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # -- end to end through the Python API with host buffers
+    pin = lambda x: x.cpu().pin_memory()
+    q_h, kn_h, vn_h, sl_h, ln_h = pin(q), pin(kn), pin(vn), pin(slots), pin(lens)
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    q_d, kn_d, vn_d = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    sl_d, ln_d = torch.empty_like(slots), torch.empty_like(lens)
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, kn_h, vn_h, sl_h, ln_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h, non_blocking=True)
+        vn_d.copy_(vn_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        ln_d.copy_(ln_h, non_blocking=True)
+        step(q_d, kn_d, vn_d, sl_d, ln_d, out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    K2 = max(1, min(K, 50))
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / K2
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    for p in pools:
+        assert p.error() == kvq.KVQ_OK
+
+    b = step_bytes(w)
+    step_total = b["decode"] + b["append"]
+    value = world * step_total / (ms * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    dec_avg_ms = float(np.mean(dec_ms))
+    fmt0, g0 = w.layer_formats[0]
+    per_launch = layer_bytes(w, fmt0, g0)["decode"]
+    achieved = per_launch / (dec_avg_ms * 1e-3) / 1e9
+    # launches: per layer one append + one decode (+ one merge when the context is split)
+    pl = kvq.kvq_decode_workspace_bytes(pools[0].handle, w.S, w.Hq, max_ctx)
+    launches_per_layer = 2 + (1 if pl > 0 else 0)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i8/e4m3 codes x f16 mma -> f32 acc",
+        "data": "synthetic (seeded on-device normal draws with the workload's outlier/drift structure)",
+        "config": {
+            "workload": w.name, "layers": L, "seqs": w.S,
+            "context_lens": "%d..%d (mean %.0f)" % (w.context_lens.min(), w.context_lens.max(),
+                                                   w.context_lens.mean()),
+            "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
+            "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f == 3 else "")
+                                 for f, g in w.layer_formats}),
+            "pool_blocks_per_layer": w.num_blocks,
+            "l2": "inputs larger than L2: %d per-layer pools, %.1f GB"
+                  % (L, sum(p.buffer.numel() for p in pools) / 1e9),
+            "step": "per layer: kvq_append (1 token/seq) then kvq_paged_decode",
+        },
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "decode_tok_per_s": round(world * w.S / (ms * 1e-3), 1),
+        "bytes_per_step": b,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": read_traffic(w.name),
+                     "kernel": "kvq_paged_decode call (decode kernel + split merge)",
+                     "bytes_per_launch": per_launch, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "peak_source": "%s hbm_gbs" % peak_kind},
+        "e2e": {"value": round(world * step_total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K2},
+        "gpu_launches": K * L * launches_per_layer,
+        "clocks": clocks,
+    }
+    del pools
+    return res
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample of
+    the workload (layer 0, one sequence), timed on the host cores."""
+    from paged_quantized_kv_kvq_gb300 import synth
+    import oracle
+
+    import dataclasses
+
+    w = synth.workload(args.workload)
+    fmt, group = w.layer_formats[0]
+    oracle.build()
+    # one step = sequence 0, KV head 0 and its Q heads, of layer 0
+    run = oracle_sample(w, fmt, group, [0], oracle, synth, kv_heads=1)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    ws = dataclasses.replace(w, Hkv=1, Hq=w.G)
+    b = layer_bytes(ws, fmt, group, [0])
+    nbytes = b["decode"] + b["append"]
+    v = nbytes / dt / 1e9
+    sample = ("layer 0 of %d, sequence 0 of %d, KV head 0 of %d with its %d Q heads (append of "
+              "the step token + float64 paged decode over %d tokens) per step"
+              % (w.layers, w.S, w.Hkv, w.G, int(w.context_lens[0])))
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (numpy seeded)",
+            "config": {"workload": w.name},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s",
+                             "cores": min(oracle.num_threads(), w.G),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gqa_64x2048")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers (profiling runs only; the bench line uses all)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            from paged_quantized_kv_kvq_gb300 import synth
+
+            res["cpu_baseline"] = cpu_baseline(synth.workload(args.workload))
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -265,3 +265,51 @@ def step_kv(w: Workload, layer: int) -> tuple[np.ndarray, np.ndarray]:
     """fp16 K/V [S, Hkv, D] of this step's new token (position L-1) per sequence."""
     idx = np.stack([np.arange(w.S), w.context_lens.astype(np.int64) - 1], 1)
     return kv_tokens(w, layer, idx)
+
+
+# ---------------------------------------------------------------- on-device draws
+# The benchmark fills 32 layers of multi-GB pools; drawing those values on the
+# host would take minutes, so it draws them with torch's device generator
+# (same distributions and structure as above, different random streams).
+def _device_gen(device, *key):
+    import torch
+
+    g = torch.Generator(device=device)
+    h = 0
+    for k in key:
+        h = (h * 1000003 + int(k)) & 0x7FFFFFFFFFFFFFFF
+    g.manual_seed(h)
+    return g
+
+
+def device_kv(w: Workload, layer: int, seq: int, t0: int, t1: int, device):
+    """fp16 K, V [t1-t0, Hkv, D] for positions t0..t1-1 of one sequence,
+    drawn on the device (positions are independent unless the workload has
+    drift, in which case t0 must be 0)."""
+    import torch
+
+    n = max(t1 - t0, 0)
+    k = torch.randn((n, w.Hkv, w.D), generator=_device_gen(device, w.seed, layer, seq, t0, 1),
+                    device=device, dtype=torch.float32)
+    v = torch.randn((n, w.Hkv, w.D), generator=_device_gen(device, w.seed, layer, seq, t0, 2),
+                    device=device, dtype=torch.float32)
+    if w.drift_sigma > 0 and n:
+        assert t0 == 0
+        gk = _device_gen(device, w.seed, layer, seq, t0, 3)
+        gv = _device_gen(device, w.seed, layer, seq, t0, 4)
+        k += torch.cumsum(w.drift_sigma * torch.randn(k.shape, generator=gk, device=device), 0)
+        v += torch.cumsum(w.drift_sigma * torch.randn(v.shape, generator=gv, device=device), 0)
+    for h, d in w.outlier_channels:
+        k[:, h, d] *= w.outlier_gain
+        v[:, h, d] *= w.outlier_gain
+    return k.half(), v.half()
+
+
+def device_queries(w: Workload, layer: int, device):
+    import torch
+
+    q = torch.randn((w.S, w.Hq, w.D), generator=_device_gen(device, w.seed, layer, 104729),
+                    device=device, dtype=torch.float32)
+    for h, d in w.outlier_channels:
+        q[:, h * w.G:(h + 1) * w.G, d] *= w.outlier_gain
+    return q.half()
