@@ -178,6 +178,36 @@ kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_
                                void* workspace, size_t ws_bytes, int split_blocks,
                                cudaStream_t stream);
 
+/* Maximum split-K scratch of kvq_paged_decode_noalloc, in bytes (16 MiB). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* kvq_paged_decode_ex for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for library users.
+ * Some callers must not allocate: a serving loop whose memory is all reserved
+ * up front, code running under a custom or capped allocator that refuses new
+ * requests, or host code in a context where a cudaMalloc would stall or is
+ * not permitted.  This call takes no workspace: the split-K scratch lives in
+ * a fixed array of KVQ_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library keeps until the process exits.  Arguments and
+ * results are those of kvq_paged_decode_ex; the caller still provides q,
+ * the table, the lengths and `out`.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress), so make that first call before any stream
+ *     capture; later calls on the device reuse the address.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose execution
+ *     overlaps on the GPU -- on two streams, or from two threads -- race on
+ *     it; order them.
+ *   - Returns KVQ_ERR_WORKSPACE, launching nothing, when the scratch the call
+ *     needs (kvq_decode_workspace_bytes_ex for the same sizes) exceeds
+ *     KVQ_NOALLOC_SCRATCH_BYTES; KVQ_ERR_CUDA if the array cannot be located. */
+kvq_status kvq_paged_decode_noalloc(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                                    int num_q_heads, const int32_t* block_table,
+                                    int max_blocks_per_seq, const int32_t* context_lens,
+                                    int max_context_len, float sm_scale, float* out,
+                                    int split_blocks, cudaStream_t stream);
+
 /* Read back n slots in a canonical layout (for tests and debugging).
  *   codes_out  : [n][2][kv_heads][head_dim] elements of the pool's code type
  *                (int8, e4m3 byte, or fp16)

@@ -90,6 +90,7 @@ def _declare(L):
         "kvq_decode_workspace_bytes_ex": (sz, [P, i32, i32, i32, i32]),
         "kvq_paged_decode": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
         "kvq_paged_decode_ex": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, i32, P]),
+        "kvq_paged_decode_noalloc": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, i32, P]),
         "kvq_read_slots": (i32, [P, P, i64, P, P, P]),
         "kvq_get_error": (i32, [P, P]),
         "kvq_status_string": (ctypes.c_char_p, [i32]),
@@ -199,6 +200,24 @@ def kvq_paged_decode(pool, q, block_table, context_lens, max_context_len, sm_sca
         float(sm_scale), _ptr(out, torch.float32, "out"),
         _ptr(workspace, None, "workspace") if workspace is not None else None, ws_bytes,
         int(split_blocks), _stream(stream)), "kvq_paged_decode")
+
+
+KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def kvq_paged_decode_noalloc(pool, q, block_table, context_lens, max_context_len, sm_scale, out,
+                             split_blocks=0, stream=None) -> None:
+    """kvq_paged_decode without a workspace argument, for callers that cannot
+    allocate device memory: the split scratch is a fixed 16 MiB array inside
+    the library (see kvq_paged_decode_noalloc in include/kvq.h)."""
+    import torch
+
+    S, Hq, _ = q.shape
+    _check(lib().kvq_paged_decode_noalloc(
+        pool, _ptr(q, torch.float16, "q"), S, Hq, _ptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len),
+        float(sm_scale), _ptr(out, torch.float32, "out"), int(split_blocks), _stream(stream)),
+        "kvq_paged_decode_noalloc")
 
 
 def kvq_read_slots(pool, slots, codes_out, scales_out=None, stream=None) -> None:
