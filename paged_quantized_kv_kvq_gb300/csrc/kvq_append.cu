@@ -38,11 +38,12 @@ __device__ __forceinline__ float absmax8(const __half2 (&x)[4]) {
   return a;
 }
 
-__device__ __forceinline__ int8_t quant_i8(float x, float s) {
-  if (s == 0.f) return 0;
+// INT8 code, returned biased (c + 128) as stored in the pool.
+__device__ __forceinline__ uint8_t quant_i8(float x, float s) {
+  if (s == 0.f) return static_cast<uint8_t>(kInt8Bias);
   float q = rintf(__fdiv_rn(x, s));
   q = fminf(fmaxf(q, -127.f), 127.f);
-  return static_cast<int8_t>(q);
+  return static_cast<uint8_t>(static_cast<int>(q) + 128);
 }
 
 __device__ __forceinline__ uint8_t quant_e4m3(float x, float s) {
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
         for (int o = lanes >> 1; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         const float s = a == 0.f ? 0.f : __fdiv_rn(a, 127.f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(quant_i8(f[i], s));
+        for (int i = 0; i < 8; ++i) code[i] = quant_i8(f[i], s);
         if (act && (d0 % pool.group) == 0) {
           float* sc = reinterpret_cast<float*>(page + 2 * pool.code_bytes) +
                       (kv * pool.bs + off) * pool.ng + d0 / pool.group;
@@ -135,14 +136,14 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
         }
       } else if constexpr (FMT == FMT_INT8_TOKEN) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(quant_i8(f[i], tok_scale));
+        for (int i = 0; i < 8; ++i) code[i] = quant_i8(f[i], tok_scale);
       } else if constexpr (FMT == FMT_FP8_TOKEN) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) code[i] = quant_e4m3(f[i], tok_scale);
       } else {  // FMT_INT8_CHANNEL
         const float* cs = pool.chan_scales + ((int64_t)kv * Hkv + h) * D + d0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) code[i] = static_cast<uint8_t>(quant_i8(f[i], cs[i]));
+        for (int i = 0; i < 8; ++i) code[i] = quant_i8(f[i], cs[i]);
       }
       if (!act) continue;
       if (kv == 0) {
@@ -203,8 +204,9 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
     const int64_t dst = (i * 2 + kv) * per + c;
     if (es == 2)
       reinterpret_cast<uint16_t*>(codes_out)[dst] = *reinterpret_cast<const uint16_t*>(tile + o);
-    else
-      reinterpret_cast<uint8_t*>(codes_out)[dst] = *reinterpret_cast<const uint8_t*>(tile + o);
+    else  // INT8 codes are stored biased; hand back the signed code
+      reinterpret_cast<uint8_t*>(codes_out)[dst] =
+          *reinterpret_cast<const uint8_t*>(tile + o) ^ (pool.fmt == FMT_FP8_TOKEN ? 0u : kInt8Bias);
   }
   if (scales_out == nullptr) return;
   if (pool.fmt == FMT_INT8_GROUP) {

@@ -8,6 +8,7 @@
 // exactly the bytes its tensor-core fragments need with 16-byte loads.
 //
 //   header      : 256 B, int32 error word at offset 0
+//   (INT8 codes are stored biased by +128, see kInt8Bias)
 //   pages       : [num_blocks][kv_heads] pages of page_bytes each:
 //                   K codes : block_size/16 sub-tiles of 16 tokens x D
 //                   V codes : block_size/16 sub-tiles
@@ -161,11 +162,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
-// Four int8 codes (bytes 0..3 of w) -> two fp16x2: lo = (b0, b1), hi = (b2, b3).
-// Exact: the biased byte u = b + 128 is placed in the low mantissa bits of
-// 1024.0 (0x6400 | u == 1024 + u), then 1152 = 1024 + 128 is subtracted.
-__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+// INT8 codes are stored biased, as the byte u = c + 128 (c ^ 0x80), so that
+// the conversion below needs no XOR.
+constexpr uint32_t kInt8Bias = 0x80u;
+
+// Four biased int8 codes (bytes 0..3 of w) -> two fp16x2: lo = (c0, c1),
+// hi = (c2, c3).  Exact: u is placed in the low mantissa bits of 1024.0
+// (0x6400 | u == 1024 + u), then 1152 = 1024 + 128 is subtracted.
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t u, uint32_t& lo, uint32_t& hi) {
   const uint32_t l = prmt(u, 0x64646464u, 0x4140u);
   const uint32_t h = prmt(u, 0x64646464u, 0x4342u);
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));

@@ -128,6 +128,221 @@ __device__ __forceinline__ void load_lane_words(const char* tile, int lane, uint
   }
 }
 
+// A 16-token sub-tile in shared memory: K and V codes in fragment order and the
+// per-row K / V scales (group or token formats); rows = valid tokens (0..16).
+struct TileRef {
+  const char* k;
+  const char* v;
+  const float* ks;
+  const float* vs;
+  int rows;
+};
+
+// One online-softmax update over two sub-tiles (32 tokens) for the up-to-8 Q
+// heads of a kv head.  Lane (g = lane/4, j = lane%4) holds scores of tokens
+// g and g+8 of each tile for heads 2j and 2j+1, and O^T rows 16mt+g, 16mt+g+8
+// for the same two heads.  B may be an empty tile (rows = 0; pointers valid).
+template <int FMT, int D, int NG>
+__device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B, int lane,
+                                             const uint32_t (&qb)[D / 16][2],
+                                             const uint32_t (&ql)[FmtTraits<FMT>::channel ? D / 16 : 1][2],
+                                             float csc, float (&m)[2], float (&l)[2], int& E,
+                                             float (&o)[D / 16][4]) {
+  using T = FmtTraits<FMT>;
+  constexpr int KS = D / 16;
+  constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;
+  constexpr int KPG = KS / NG;
+  constexpr int SUB = KPG >= 2 ? 2 : 1;  // independent accumulators per scale group
+  const float kNegInf = __int_as_float(0xff800000u);
+  const int g = lane >> 2, j = lane & 3;
+  const TileRef* tl[2] = {&A, &B};
+
+  // ---- scores: S[t][r] = sum_d code_K[t][d] q'[r][d], per scale group
+  float z[2][4];
+  {
+    uint32_t kw[2][NU32];
+    load_lane_words<FMT, D>(A.k, lane, kw[0]);
+    load_lane_words<FMT, D>(B.k, lane, kw[1]);
+    float acc[2][NG * SUB][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int a = 0; a < NG * SUB; ++a) acc[t][a][0] = acc[t][a][1] = acc[t][a][2] = acc[t][a][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int ai = (kk / KPG) * SUB + (SUB == 2 ? (kk & 1) : 0);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t a0, a1, a2, a3;
+        word_to_h2<FMT>(kw[t], kk, a0, a2);       // row g   : channels e=0,1 | e=2,3
+        word_to_h2<FMT>(kw[t], KS + kk, a1, a3);  // row g+8
+        mma_16816(acc[t][ai], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        if constexpr (T::channel) mma_16816(acc[t][ai], a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const TileRef& tr = *tl[t];
+      float zz[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        float s4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s4[e] = SUB == 2 ? acc[t][gi * SUB][e] + acc[t][gi * SUB + 1][e]
+                                                     : acc[t][gi * SUB][e];
+        float sA = csc, sB = csc;
+        if constexpr (T::group_scales) {
+          sA *= tr.ks[g * NG + gi];
+          sB *= tr.ks[(g + 8) * NG + gi];
+        } else if constexpr (T::token_scales) {
+          sA *= tr.ks[g];
+          sB *= tr.ks[g + 8];
+        }
+        zz[0] = fmaf(s4[0], sA, zz[0]);
+        zz[1] = fmaf(s4[1], sA, zz[1]);
+        zz[2] = fmaf(s4[2], sB, zz[2]);
+        zz[3] = fmaf(s4[3], sB, zz[3]);
+      }
+      const bool vA = g < tr.rows, vB = g + 8 < tr.rows;
+      z[t][0] = vA ? zz[0] : kNegInf;
+      z[t][1] = vA ? zz[1] : kNegInf;
+      z[t][2] = vB ? zz[2] : kNegInf;
+      z[t][3] = vB ? zz[3] : kNegInf;
+    }
+  }
+
+  // ---- online softmax (base 2) over the 32 tokens
+  float pr[2][4];
+  {
+    float t0 = fmaxf(fmaxf(z[0][0], z[0][2]), fmaxf(z[1][0], z[1][2]));
+    float t1 = fmaxf(fmaxf(z[0][1], z[0][3]), fmaxf(z[1][1], z[1][3]));
+    t0 = warp_max_over_rows(t0);
+    t1 = warp_max_over_rows(t1);
+    const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);
+    const float ms0 = mn0 == kNegInf ? 0.f : mn0;
+    const float ms1 = mn1 == kNegInf ? 0.f : mn1;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      pr[t][0] = fast_exp2(z[t][0] - ms0);
+      pr[t][1] = fast_exp2(z[t][1] - ms1);
+      pr[t][2] = fast_exp2(z[t][2] - ms0);
+      pr[t][3] = fast_exp2(z[t][3] - ms1);
+    }
+    int dE = 0;
+    if constexpr (T::row_scales) {
+      constexpr int NS = T::group_scales ? NG : 1;
+      float vmax = 0.f;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const TileRef& tr = *tl[t];
+#pragma unroll
+        for (int gi = 0; gi < NS; ++gi) {
+          if (g < tr.rows) vmax = fmaxf(vmax, tr.vs[g * NS + gi]);
+          if (g + 8 < tr.rows) vmax = fmaxf(vmax, tr.vs[(g + 8) * NS + gi]);
+        }
+      }
+      vmax = warp_max_over_rows(vmax);
+      if (vmax > 0.f) {
+        const int En = min(E, 13 - exponent_of(vmax));
+        dE = En - E;
+        E = En;
+      }
+    }
+    const float al0 = fast_exp2(m[0] - ms0), al1 = fast_exp2(m[1] - ms1);
+    l[0] = fmaf(l[0], al0, (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
+    l[1] = fmaf(l[1], al1, (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+    m[0] = mn0;
+    m[1] = mn1;
+    const float f2 = pow2f(dE);
+    const float ao0 = al0 * f2, ao1 = al1 * f2;
+    if (__any_sync(0xffffffffu, ao0 != 1.f || ao1 != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= ao0;
+        o[mt][1] *= ao1;
+        o[mt][2] *= ao0;
+        o[mt][3] *= ao1;
+      }
+    }
+  }
+
+  // ---- P.V: B operand = p * s_V * 2^E split into fp16 hi + lo, transposed so
+  // that k runs over the tile's tokens
+  constexpr int NB = T::group_scales ? NG : 1;
+  uint32_t bh0[2][NB], bh1[2][NB], bl0[2][NB], bl1[2][NB];
+  {
+    const float sc = pow2f(E);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const TileRef& tr = *tl[t];
+      const bool vA = g < tr.rows, vB = g + 8 < tr.rows;
+#pragma unroll
+      for (int gi = 0; gi < NB; ++gi) {
+        float fA = sc, fB = sc;
+        if constexpr (T::group_scales) {
+          fA *= tr.vs[g * NG + gi];
+          fB *= tr.vs[(g + 8) * NG + gi];
+        } else if constexpr (T::token_scales) {
+          fA *= tr.vs[g];
+          fB *= tr.vs[g + 8];
+        }
+        const float p0 = vA ? pr[t][0] * fA : 0.f, p1 = vA ? pr[t][1] * fA : 0.f;
+        const float p2 = vB ? pr[t][2] * fB : 0.f, p3 = vB ? pr[t][3] * fB : 0.f;
+        uint32_t hA, lA, hB, lB;
+        split_h2(p0, p1, hA, lA);
+        split_h2(p2, p3, hB, lB);
+        bh0[t][gi] = movmatrix_t(hA);
+        bh1[t][gi] = movmatrix_t(hB);
+        bl0[t][gi] = movmatrix_t(lA);
+        bl1[t][gi] = movmatrix_t(lB);
+      }
+    }
+  }
+  {
+    uint32_t vw[2][NU32];
+    load_lane_words<FMT, D>(A.v, lane, vw[0]);
+    load_lane_words<FMT, D>(B.v, lane, vw[1]);
+    if constexpr (T::maybe_nan) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int rows = tl[t]->rows;
+        if (rows < 16) {
+          // tokens of this lane's V bytes: 2j, 2j+1, 2j+8, 2j+9; zero the ones
+          // past the context so that 0 * NaN cannot reach the sum
+          const int t0 = 2 * j;
+          if constexpr (FMT == FMT_FP16) {
+            const uint32_t mlo = (t0 < rows ? 0xFFFFu : 0u) | (t0 + 1 < rows ? 0xFFFF0000u : 0u);
+            const uint32_t mhi = (t0 + 8 < rows ? 0xFFFFu : 0u) | (t0 + 9 < rows ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int w = 0; w < NU32 / 2; ++w) {
+              vw[t][2 * w] &= mlo;
+              vw[t][2 * w + 1] &= mhi;
+            }
+          } else {
+            const uint32_t msk = (t0 < rows ? 0xFFu : 0u) | (t0 + 1 < rows ? 0xFF00u : 0u) |
+                                 (t0 + 8 < rows ? 0xFF0000u : 0u) |
+                                 (t0 + 9 < rows ? 0xFF000000u : 0u);
+#pragma unroll
+            for (int w = 0; w < NU32; ++w) vw[t][w] &= msk;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      const int gi = T::group_scales ? (mt / KPG) : 0;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t a0, a1, a2, a3;
+        word_to_h2<FMT>(vw[t], 2 * mt, a0, a2);      // channel 16mt+g   : tokens 2j,2j+1 | 2j+8,2j+9
+        word_to_h2<FMT>(vw[t], 2 * mt + 1, a1, a3);  // channel 16mt+g+8
+        mma_16816(o[mt], a0, a1, a2, a3, bh0[t][gi], bh1[t][gi]);
+        mma_16816(o[mt], a0, a1, a2, a3, bl0[t][gi], bl1[t][gi]);
+      }
+    }
+  }
+}
+
 template <int FMT, int D, int NG>
 __global__ void __launch_bounds__(kDecodeThreads)
     kvq_decode_kernel(const DecodeParams p) {
@@ -260,191 +475,68 @@ __global__ void __launch_bounds__(kDecodeThreads)
   float o[KS][4];
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  bool timed_out = false;
 
-  for (int i = 0; i < n_w; ++i) {
+  // Bounded wait for stage i; false (and the timeout bit set) if it gave up.
+  auto wait_stage = [&](int i) -> bool {
     const int st = i & (nstage - 1);
     const uint32_t parity = (i >> p.nstage_log2) & 1;
     bool ok = false;
     for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(&bars[st], parity);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0) set_error(pool.err, ERR_TIMEOUT);
-      timed_out = true;
-      break;
+      return false;
     }
-    const int phys = stage_phys[st];
+    return true;
+  };
+  // Sub-tile `sub` of the warp's i-th page as a tile reference (rows = 0 when
+  // the page is absent, out of range or the sub-tile lies past the context).
+  auto tile_of = [&](int i, int sub) -> TileRef {
+    TileRef t;
+    const int st = i & (nstage - 1);
     const char* stage = stages + st * p.stage_bytes;
+    t.k = stage + sub * pool.sub_bytes;
+    t.v = stage + pool.code_bytes + sub * pool.sub_bytes;
+    t.ks = nullptr;
+    t.vs = nullptr;
+    if constexpr (T::group_scales) {
+      t.ks = reinterpret_cast<const float*>(stage + 2 * pool.code_bytes) + sub * 16 * NG;
+      t.vs = t.ks + bs * NG;
+    } else if constexpr (T::token_scales) {
+      t.ks = reinterpret_cast<const float*>(stage + pool.page_bytes) + sub * 16;
+      t.vs = t.ks + bs;
+    }
     const int page = pg0 + warp + i * kDecodeWarps;
-    const int nvalid = min(bs, L - page * bs);
-    if (phys >= 0) {
-      const int nsub = (nvalid + 15) >> 4;
-      for (int sub = 0; sub < nsub; ++sub) {
-        const int rows = min(16, nvalid - sub * 16);
-        const char* ktile = stage + sub * pool.sub_bytes;
-        const char* vtile = stage + pool.code_bytes + sub * pool.sub_bytes;
-        const float* kscale = nullptr;
-        const float* vscale = nullptr;
-        if constexpr (T::group_scales) {
-          kscale = reinterpret_cast<const float*>(stage + 2 * pool.code_bytes) + sub * 16 * NG;
-          vscale = kscale + bs * NG;
-        } else if constexpr (T::token_scales) {
-          kscale = reinterpret_cast<const float*>(stage + pool.page_bytes) + sub * 16;
-          vscale = kscale + bs;
-        }
-        const bool vA = g < rows, vB = g + 8 < rows;
+    const int nvalid = min(bs, L - page * bs) - sub * 16;
+    t.rows = (i < n_w && stage_phys[st] >= 0) ? max(0, min(16, nvalid)) : 0;
+    return t;
+  };
 
-        // -- scores S[t][r] = sum_d code_K[t][d] q'[r][d] per scale group
-        float z[4];
-        {
-          uint32_t kw[NU32];
-          load_lane_words<FMT, D>(ktile, lane, kw);
-          float sacc[NG][4];
-#pragma unroll
-          for (int gi = 0; gi < NG; ++gi) sacc[gi][0] = sacc[gi][1] = sacc[gi][2] = sacc[gi][3] = 0.f;
-#pragma unroll
-          for (int kk = 0; kk < KS; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            word_to_h2<FMT>(kw, kk, a0, a2);       // row g   : channels e=0,1 | e=2,3
-            word_to_h2<FMT>(kw, KS + kk, a1, a3);  // row g+8
-            mma_16816(sacc[kk / KPG], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-            if constexpr (T::channel) mma_16816(sacc[0], a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
-          }
-          if constexpr (T::group_scales) {
-            float zA0 = 0.f, zA1 = 0.f, zB0 = 0.f, zB1 = 0.f;
-#pragma unroll
-            for (int gi = 0; gi < NG; ++gi) {
-              const float sA = kscale[g * NG + gi], sB = kscale[(g + 8) * NG + gi];
-              zA0 = fmaf(sacc[gi][0], sA, zA0);
-              zA1 = fmaf(sacc[gi][1], sA, zA1);
-              zB0 = fmaf(sacc[gi][2], sB, zB0);
-              zB1 = fmaf(sacc[gi][3], sB, zB1);
-            }
-            z[0] = zA0 * csc; z[1] = zA1 * csc; z[2] = zB0 * csc; z[3] = zB1 * csc;
-          } else if constexpr (T::token_scales) {
-            const float sA = kscale[g] * csc, sB = kscale[g + 8] * csc;
-            z[0] = sacc[0][0] * sA; z[1] = sacc[0][1] * sA;
-            z[2] = sacc[0][2] * sB; z[3] = sacc[0][3] * sB;
-          } else {
-            z[0] = sacc[0][0] * csc; z[1] = sacc[0][1] * csc;
-            z[2] = sacc[0][2] * csc; z[3] = sacc[0][3] * csc;
-          }
-          if (!vA) z[0] = z[1] = kNegInf;
-          if (!vB) z[2] = z[3] = kNegInf;
-        }
-
-        // -- online softmax (base 2)
-        float pr[4], alpha_o[2];
-        {
-          float t0 = warp_max_over_rows(fmaxf(z[0], z[2]));
-          float t1 = warp_max_over_rows(fmaxf(z[1], z[3]));
-          const float mn0 = fmaxf(m[0], t0), mn1 = fmaxf(m[1], t1);
-          const float ms0 = mn0 == kNegInf ? 0.f : mn0;
-          const float ms1 = mn1 == kNegInf ? 0.f : mn1;
-          pr[0] = fast_exp2(z[0] - ms0);
-          pr[1] = fast_exp2(z[1] - ms1);
-          pr[2] = fast_exp2(z[2] - ms0);
-          pr[3] = fast_exp2(z[3] - ms1);
-          int dE = 0;
-          if constexpr (T::row_scales) {
-            float vmax = 0.f;
-#pragma unroll
-            for (int gi = 0; gi < (T::group_scales ? NG : 1); ++gi) {
-              const int stride = T::group_scales ? NG : 1;
-              if (vA) vmax = fmaxf(vmax, vscale[g * stride + gi]);
-              if (vB) vmax = fmaxf(vmax, vscale[(g + 8) * stride + gi]);
-            }
-            vmax = warp_max_over_rows(vmax);
-            if (vmax > 0.f) {
-              const int En = min(E, 13 - exponent_of(vmax));
-              dE = En - E;
-              E = En;
-            }
-          }
-          alpha_o[0] = fast_exp2(m[0] - ms0 + (float)dE);
-          alpha_o[1] = fast_exp2(m[1] - ms1 + (float)dE);
-          const float al0 = fast_exp2(m[0] - ms0), al1 = fast_exp2(m[1] - ms1);
-          l[0] = fmaf(l[0], al0, pr[0] + pr[2]);
-          l[1] = fmaf(l[1], al1, pr[1] + pr[3]);
-          m[0] = mn0;
-          m[1] = mn1;
-        }
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          o[mt][0] *= alpha_o[0];
-          o[mt][1] *= alpha_o[1];
-          o[mt][2] *= alpha_o[0];
-          o[mt][3] *= alpha_o[1];
-        }
-
-        // -- P.V: B operand = (p * s_V * 2^E) split hi/lo, transposed to k = tokens
-        constexpr int NB = T::group_scales ? NG : 1;
-        uint32_t bh0[NB], bh1[NB], bl0[NB], bl1[NB];
-        {
-          const float sc = pow2f(E);
-#pragma unroll
-          for (int gi = 0; gi < NB; ++gi) {
-            float fA = sc, fB = sc;
-            if constexpr (T::group_scales) {
-              fA *= vscale[g * NG + gi];
-              fB *= vscale[(g + 8) * NG + gi];
-            } else if constexpr (T::token_scales) {
-              fA *= vscale[g];
-              fB *= vscale[g + 8];
-            }
-            const float p0 = vA ? pr[0] * fA : 0.f, p1 = vA ? pr[1] * fA : 0.f;
-            const float p2 = vB ? pr[2] * fB : 0.f, p3 = vB ? pr[3] * fB : 0.f;
-            uint32_t hA, lA, hB, lB;
-            split_h2(p0, p1, hA, lA);
-            split_h2(p2, p3, hB, lB);
-            bh0[gi] = movmatrix_t(hA);
-            bh1[gi] = movmatrix_t(hB);
-            bl0[gi] = movmatrix_t(lA);
-            bl1[gi] = movmatrix_t(lB);
-          }
-        }
-        {
-          uint32_t vw[NU32];
-          load_lane_words<FMT, D>(vtile, lane, vw);
-          if constexpr (T::maybe_nan) {
-            if (rows < 16) {
-              // tokens of this lane's V bytes: 2j, 2j+1, 2j+8, 2j+9; zero the
-              // ones past the context so that 0 * NaN cannot reach the sum.
-              const int t0 = 2 * j;
-              if constexpr (FMT == FMT_FP16) {
-                const uint32_t mlo = (t0 < rows ? 0xFFFFu : 0u) | (t0 + 1 < rows ? 0xFFFF0000u : 0u);
-                const uint32_t mhi = (t0 + 8 < rows ? 0xFFFFu : 0u) | (t0 + 9 < rows ? 0xFFFF0000u : 0u);
-#pragma unroll
-                for (int w = 0; w < NU32 / 2; ++w) {
-                  vw[2 * w] &= mlo;
-                  vw[2 * w + 1] &= mhi;
-                }
-              } else {
-                const uint32_t msk = (t0 < rows ? 0xFFu : 0u) | (t0 + 1 < rows ? 0xFF00u : 0u) |
-                                     (t0 + 8 < rows ? 0xFF0000u : 0u) |
-                                     (t0 + 9 < rows ? 0xFF000000u : 0u);
-#pragma unroll
-                for (int w = 0; w < NU32; ++w) vw[w] &= msk;
-              }
-            }
-          }
-#pragma unroll
-          for (int mt = 0; mt < KS; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            word_to_h2<FMT>(vw, 2 * mt, a0, a2);      // channel 16mt+g   : tokens 2j,2j+1 | 2j+8,2j+9
-            word_to_h2<FMT>(vw, 2 * mt + 1, a1, a3);  // channel 16mt+g+8
-            constexpr int dummy = 0;
-            (void)dummy;
-            const int gi = T::group_scales ? (mt / KPG) : 0;
-            mma_16816(o[mt], a0, a1, a2, a3, bh0[gi], bh1[gi]);
-            mma_16816(o[mt], a0, a1, a2, a3, bl0[gi], bl1[gi]);
-          }
-        }
+  const bool pair_pages = bs == 16;  // one 16-token sub-tile per page: pages go in pairs
+  for (int i = 0; i < n_w; i += pair_pages ? 2 : 1) {
+    const bool two = pair_pages && i + 1 < n_w;
+    if (!wait_stage(i) || (two && !wait_stage(i + 1))) break;
+    if (pair_pages) {
+      TileRef A = tile_of(i, 0);
+      TileRef B = two ? tile_of(i + 1, 0) : A;
+      if (!two) B.rows = 0;
+      if (A.rows == 0 && B.rows > 0) { TileRef t = A; A = B; B = t; }
+      if (B.rows == 0) { const int r = B.rows; B = A; B.rows = r; }
+      process_pair<FMT, D, NG>(A, B, lane, qb, ql, csc, m, l, E, o);
+    } else {
+      const int page = pg0 + warp + i * kDecodeWarps;
+      const int nsub = (min(bs, L - page * bs) + 15) >> 4;
+      for (int sp = 0; sp < nsub; sp += 2) {
+        TileRef A = tile_of(i, sp);
+        TileRef B = tile_of(i, sp + 1 < nsub ? sp + 1 : sp);
+        if (sp + 1 >= nsub) B.rows = 0;
+        if (A.rows == 0) break;  // page skipped (out-of-range block id)
+        process_pair<FMT, D, NG>(A, B, lane, qb, ql, csc, m, l, E, o);
       }
     }
     __syncwarp();
     if (i + nstage < n_w) issue(i + nstage);
+    if (two && i + 1 + nstage < n_w) issue(i + 1 + nstage);
   }
-  (void)timed_out;
 
   // ---- per-warp totals, then merge the warps through shared memory
   l[0] = warp_sum_over_rows(l[0]);

@@ -83,7 +83,10 @@ def test_append_bitexact_and_sentinels(fmt, group, D):
     # untouched slots still hold the sentinel bytes
     untouched = np.setdiff1d(np.arange(nb * bs), written)
     codes, scales = pool.read_slots(torch.from_numpy(untouched).to(DEV))
-    assert np.all(codes.cpu().numpy().view(np.uint8) == 0x5A)
+    # the read-back returns signed INT8 codes; the pool stores them biased by 128
+    sentinel = 0x5A ^ 0x80 if fmt in (kvq.KVQ_INT8_PER_TOKEN, kvq.KVQ_INT8_PER_CHANNEL,
+                                      kvq.KVQ_INT8_PER_GROUP) else 0x5A
+    assert np.all(codes.cpu().numpy().view(np.uint8) == sentinel)
     if scales is not None:
         assert np.all(scales.cpu().numpy().view(np.uint32) == 0x5A5A5A5A)
     pool.close()
