@@ -1,37 +1,42 @@
 // kvq_decode_impl.cuh -- paged decode attention over a quantized KV pool.
 //
 // Method ("KV Cache优化实战：大模型推理显存占用与加速方案详解",
-// 0539edu.com/news/5800990): decode step attends the new Q over all cached K/V
-// (§1.1); Q heads are grouped and each group shares one K/V head (§2.1);
-// the cache lives in fixed-size physical blocks reached through a block
-// table (§2.2); K/V are INT8/FP8 codes with per-token, per-channel or
-// per-group scales, or FP16 (§2.3, §3.3); dequantization is fused into the
-// attention kernel instead of running as a separate pass (§4.3).
+// 0539edu.com/news/5800990): the decode step attends the new Q over all cached
+// K/V (§1.1); Q heads are grouped and each group shares one K/V head (§2.1);
+// the cache lives in fixed-size physical blocks reached through a block table
+// (§2.2); K/V are INT8/FP8 codes with per-token, per-channel or per-group
+// scales, or FP16 (§2.3, §3.3); dequantization is fused into the attention
+// kernel instead of running as a separate pass (§4.3).
 //
 // GB300 design (sm_103a):
-//  * grid = (split, kv_head x head_tile, sequence); 4 warps per CTA.  A split
-//    is a contiguous run of a sequence's blocks (split-K over the context);
-//    warps take the split's blocks round-robin.
-//  * Each warp streams its blocks through NSTAGE shared-memory stages: lane 0
-//    looks the block up in the block table and issues one bulk (TMA) copy of
-//    the (block, kv head) page -- K codes, V codes and their group scales are
-//    contiguous -- completing on an mbarrier.  Waits are bounded; a wait that
-//    runs out sets an error bit instead of hanging.
-//  * The Q heads of the kv head (up to 8 per head tile) share every loaded
-//    page: Q.K^T and P.V run on the tensor cores as mma.m16n8k16 with the
-//    heads on the n dimension.  Codes are exact in fp16 (int8 in [-127,127],
-//    every e4m3 value), so dequantization is a scale applied outside the
-//    contraction: per-token / per-group K scales multiply the fp32 scores,
-//    per-token / per-group V scales are folded into the softmax weights, and
-//    per-channel scales fold into q (K) and the output columns (V).
-//  * fp32 operands that enter a tensor-core product (softmax weights times V
+//  * Persistent, balanced ("stream-K") grid: a unit is (sequence, kv head,
+//    head tile of up to 8 Q heads) and owns ceil(L/bs) pages.  All units'
+//    pages form one index space (computed in-kernel from context_lens); every
+//    warp of the grid streams one equal, contiguous range of it, so all SMs
+//    finish together whatever the length mix.  A unit wholly inside one warp's
+//    range is written straight to the output; a unit cut by range ends leaves
+//    a partial (running max, sum, unnormalised output) per piece, and a small
+//    merge kernel, launched as a programmatic dependent of the decode kernel
+//    (its launch overlaps the decode's tail), combines the pieces by
+//    log-sum-exp.  The decode kernel itself never waits on another warp.
+//  * Each warp keeps NSTAGE shared-memory stages in flight: lane 0 reads the
+//    block table and issues one bulk (TMA) copy of the (block, kv head) page --
+//    K codes, V codes and group scales are contiguous -- completing on an
+//    mbarrier.  One-byte formats move the page's fragments into registers and
+//    hand the stage back to the copy engine before computing.  Waits are
+//    bounded; a wait that runs out sets an error bit instead of hanging.
+//  * The Q heads of the unit share every loaded page: Q.K^T and P.V run on the
+//    tensor cores as mma.m16n8k16 with the heads on the n dimension, 32 tokens
+//    (two 16-token sub-tiles) per online-softmax update.  Codes are exact in
+//    fp16 (int8 in [-127,127], every e4m3 value), so dequantization is a scale
+//    applied outside the contraction: per-token / per-group K scales multiply
+//    the fp32 scores, per-token / per-group V scales are folded into the softmax
+//    weights, per-channel scales fold into q (K) and the output columns (V).
+//  * fp32 operands entering a tensor-core product (softmax weights times V
 //    scale; q times a per-channel K scale) are split into an fp16 high part and
 //    an fp16 low part (two MMAs), after scaling by a power of two that keeps
-//    them away from fp16 overflow and underflow; that power of two is undone
-//    exactly at the end.
-//  * Online softmax in base 2 (scores pre-multiplied by log2 e); the warps of a
-//    CTA merge through shared memory; splits merge by log-sum-exp in a second
-//    small kernel.
+//    them away from fp16 overflow and underflow; the power of two is undone
+//    exactly at the end.  Softmax runs in base 2 (scores times log2 e).
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -42,7 +47,9 @@ namespace kvq {
 
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kWaitTries = 4000;  // x 1 ms suspend hint per try: ~4 s upper bound
+constexpr int kWaitTries = 4000;   // x 1 ms suspend hint per try: ~4 s upper bound
+constexpr int kPartRows = 8;       // partial rows per (warp, slot): one per Q head of a tile
+constexpr int kMergeThreads = 128;
 
 struct DecodeParams {
   PoolView pool;
@@ -50,13 +57,13 @@ struct DecodeParams {
   const int* table;    // [S][max_blocks]
   const int* lens;     // [S]
   float* out;          // [S][Hq][D]
-  float* part_o;       // [S][Hq][nsplit][D]
-  float* part_ml;      // [S][Hq][nsplit][2]
+  int* ps;             // [S + 1] page prefix over sequences (written by CTA 0 for the merge)
+  float* part;         // [warps][2][kPartRows][D + 2]: m, l, O of cut units
   int S, Hq, G, n_ht, max_blocks, max_ctx;
-  int pps;             // blocks per split
-  int nsplit;
+  int ppw_fixed;       // pages per warp; 0 = balance the pages over all warps
   int nstage_log2;
   int stage_bytes;
+  int grid;            // decode CTAs (the merge kernel derives the warp ranges from it)
   float sm_scale_log2;  // sm_scale * log2(e)
 };
 
@@ -98,6 +105,8 @@ struct FmtTraits {
   static constexpr bool row_scales = group_scales || token_scales;  // per-(token[,group]) K/V scales
   static constexpr bool channel = FMT == FMT_INT8_CHANNEL;
   static constexpr bool maybe_nan = FMT == FMT_FP16 || FMT == FMT_FP8_TOKEN;
+  // One-byte pages move to registers before compute, freeing the stage early.
+  static constexpr bool early_release = one_byte;
 };
 
 // Word w (4 elements) of a lane's sub-tile -> (lo, hi) fp16x2 pairs.
@@ -128,41 +137,80 @@ __device__ __forceinline__ void load_lane_words(const char* tile, int lane, uint
   }
 }
 
-// A 16-token sub-tile in shared memory: K and V codes in fragment order and the
-// per-row K / V scales (group or token formats); rows = valid tokens (0..16).
-struct TileRef {
-  const char* k;
-  const char* v;
-  const float* ks;
-  const float* vs;
-  int rows;
+// Position of a warp in the unit-major page index space.
+struct Cursor {
+  int s, lu, pi, Ps;  // sequence, unit within the sequence, page within the unit, pages per unit
 };
 
-// One online-softmax update over two sub-tiles (32 tokens) for the up-to-8 Q
-// heads of a kv head.  Lane (g = lane/4, j = lane%4) holds scores of tokens
-// g and g+8 of each tile for heads 2j and 2j+1, and O^T rows 16mt+g, 16mt+g+8
-// for the same two heads.  B may be an empty tile (rows = 0; pointers valid).
+// Everything one online-softmax update needs from two 16-token sub-tiles,
+// held in registers: K (and, for one-byte formats, V) fragment words, the
+// scales of the two rows this lane owns (tokens g and g+8), the valid rows.
 template <int FMT, int D, int NG>
-__device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B, int lane,
+struct PairRegs {
+  using T = FmtTraits<FMT>;
+  static constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;
+  static constexpr int NS = T::group_scales ? NG : 1;
+  uint32_t kw[2][NU32];
+  uint32_t vw[2][T::early_release ? NU32 : 1];
+  float ks[2][2][NS];  // [tile][row g | g+8][group]
+  float vs[2][2][NS];
+  const char* vtile[2];  // V codes in shared memory (formats that keep the stage)
+  int rows[2];
+};
+
+// Fill tile t of `r` from sub-tile `sub` of a staged page.
+template <int FMT, int D, int NG>
+__device__ __forceinline__ void load_tile(PairRegs<FMT, D, NG>& r, int t, const char* stage,
+                                          int sub, int rows, const PoolView& pool, int lane) {
+  using T = FmtTraits<FMT>;
+  constexpr int NS = PairRegs<FMT, D, NG>::NS;
+  const int g = lane >> 2;
+  load_lane_words<FMT, D>(stage + sub * pool.sub_bytes, lane, r.kw[t]);
+  r.vtile[t] = stage + pool.code_bytes + sub * pool.sub_bytes;
+  if constexpr (T::early_release) load_lane_words<FMT, D>(r.vtile[t], lane, r.vw[t]);
+  if constexpr (T::row_scales) {
+    const float* ks;
+    const float* vs;
+    if constexpr (T::group_scales) {
+      ks = reinterpret_cast<const float*>(stage + 2 * pool.code_bytes) + sub * 16 * NG;
+      vs = ks + pool.bs * NG;
+    } else {
+      ks = reinterpret_cast<const float*>(stage + pool.page_bytes) + sub * 16;
+      vs = ks + pool.bs;
+    }
+#pragma unroll
+    for (int gi = 0; gi < NS; ++gi) {
+      r.ks[t][0][gi] = ks[g * NS + gi];
+      r.ks[t][1][gi] = ks[(g + 8) * NS + gi];
+      r.vs[t][0][gi] = vs[g * NS + gi];
+      r.vs[t][1][gi] = vs[(g + 8) * NS + gi];
+    }
+  }
+  r.rows[t] = rows;
+}
+
+// One online-softmax update over two sub-tiles (32 tokens) for the up-to-8 Q
+// heads of a unit.  Lane (g = lane/4, j = lane%4) holds the scores of tokens g
+// and g+8 of each tile for heads 2j and 2j+1, and O^T rows 16mt+g, 16mt+g+8
+// for the same two heads.  Tile 1 may be empty (rows = 0).
+template <int FMT, int D, int NG>
+__device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
                                              const uint32_t (&qb)[D / 16][2],
                                              const uint32_t (&ql)[FmtTraits<FMT>::channel ? D / 16 : 1][2],
                                              float csc, float (&m)[2], float (&l)[2], int& E,
                                              float (&o)[D / 16][4]) {
   using T = FmtTraits<FMT>;
   constexpr int KS = D / 16;
-  constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;
+  constexpr int NU32 = PairRegs<FMT, D, NG>::NU32;
+  constexpr int NS = PairRegs<FMT, D, NG>::NS;
   constexpr int KPG = KS / NG;
   constexpr int SUB = KPG >= 2 ? 2 : 1;  // independent accumulators per scale group
   const float kNegInf = __int_as_float(0xff800000u);
   const int g = lane >> 2, j = lane & 3;
-  const TileRef* tl[2] = {&A, &B};
 
   // ---- scores: S[t][r] = sum_d code_K[t][d] q'[r][d], per scale group
   float z[2][4];
   {
-    uint32_t kw[2][NU32];
-    load_lane_words<FMT, D>(A.k, lane, kw[0]);
-    load_lane_words<FMT, D>(B.k, lane, kw[1]);
     float acc[2][NG * SUB][4];
 #pragma unroll
     for (int t = 0; t < 2; ++t)
@@ -174,36 +222,32 @@ __device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B,
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         uint32_t a0, a1, a2, a3;
-        word_to_h2<FMT>(kw[t], kk, a0, a2);       // row g   : channels e=0,1 | e=2,3
-        word_to_h2<FMT>(kw[t], KS + kk, a1, a3);  // row g+8
+        word_to_h2<FMT>(r.kw[t], kk, a0, a2);       // row g   : channels e=0,1 | e=2,3
+        word_to_h2<FMT>(r.kw[t], KS + kk, a1, a3);  // row g+8
         mma_16816(acc[t][ai], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         if constexpr (T::channel) mma_16816(acc[t][ai], a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
       }
     }
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const TileRef& tr = *tl[t];
       float zz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
         float s4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s4[e] = SUB == 2 ? acc[t][gi * SUB][e] + acc[t][gi * SUB + 1][e]
-                                                     : acc[t][gi * SUB][e];
+        for (int e = 0; e < 4; ++e)
+          s4[e] = SUB == 2 ? acc[t][gi * SUB][e] + acc[t][gi * SUB + 1][e] : acc[t][gi * SUB][e];
         float sA = csc, sB = csc;
-        if constexpr (T::group_scales) {
-          sA *= tr.ks[g * NG + gi];
-          sB *= tr.ks[(g + 8) * NG + gi];
-        } else if constexpr (T::token_scales) {
-          sA *= tr.ks[g];
-          sB *= tr.ks[g + 8];
+        if constexpr (T::row_scales) {
+          sA *= r.ks[t][0][T::group_scales ? gi : 0];
+          sB *= r.ks[t][1][T::group_scales ? gi : 0];
         }
         zz[0] = fmaf(s4[0], sA, zz[0]);
         zz[1] = fmaf(s4[1], sA, zz[1]);
         zz[2] = fmaf(s4[2], sB, zz[2]);
         zz[3] = fmaf(s4[3], sB, zz[3]);
       }
-      const bool vA = g < tr.rows, vB = g + 8 < tr.rows;
+      const bool vA = g < r.rows[t], vB = g + 8 < r.rows[t];
       z[t][0] = vA ? zz[0] : kNegInf;
       z[t][1] = vA ? zz[1] : kNegInf;
       z[t][2] = vB ? zz[2] : kNegInf;
@@ -230,17 +274,14 @@ __device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B,
     }
     int dE = 0;
     if constexpr (T::row_scales) {
-      constexpr int NS = T::group_scales ? NG : 1;
       float vmax = 0.f;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const TileRef& tr = *tl[t];
+      for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int gi = 0; gi < NS; ++gi) {
-          if (g < tr.rows) vmax = fmaxf(vmax, tr.vs[g * NS + gi]);
-          if (g + 8 < tr.rows) vmax = fmaxf(vmax, tr.vs[(g + 8) * NS + gi]);
+          if (g < r.rows[t]) vmax = fmaxf(vmax, r.vs[t][0][gi]);
+          if (g + 8 < r.rows[t]) vmax = fmaxf(vmax, r.vs[t][1][gi]);
         }
-      }
       vmax = warp_max_over_rows(vmax);
       if (vmax > 0.f) {
         const int En = min(E, 13 - exponent_of(vmax));
@@ -274,17 +315,13 @@ __device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B,
     const float sc = pow2f(E);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const TileRef& tr = *tl[t];
-      const bool vA = g < tr.rows, vB = g + 8 < tr.rows;
+      const bool vA = g < r.rows[t], vB = g + 8 < r.rows[t];
 #pragma unroll
       for (int gi = 0; gi < NB; ++gi) {
         float fA = sc, fB = sc;
-        if constexpr (T::group_scales) {
-          fA *= tr.vs[g * NG + gi];
-          fB *= tr.vs[(g + 8) * NG + gi];
-        } else if constexpr (T::token_scales) {
-          fA *= tr.vs[g];
-          fB *= tr.vs[g + 8];
+        if constexpr (T::row_scales) {
+          fA *= r.vs[t][0][gi];
+          fB *= r.vs[t][1][gi];
         }
         const float p0 = vA ? pr[t][0] * fA : 0.f, p1 = vA ? pr[t][1] * fA : 0.f;
         const float p2 = vB ? pr[t][2] * fB : 0.f, p3 = vB ? pr[t][3] * fB : 0.f;
@@ -299,13 +336,21 @@ __device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B,
     }
   }
   {
-    uint32_t vw[2][NU32];
-    load_lane_words<FMT, D>(A.v, lane, vw[0]);
-    load_lane_words<FMT, D>(B.v, lane, vw[1]);
+    uint32_t vwl[2][T::early_release ? 1 : NU32];
+    uint32_t* vwp[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if constexpr (T::early_release) {
+        vwp[t] = r.vw[t];
+      } else {
+        load_lane_words<FMT, D>(r.vtile[t], lane, vwl[t]);
+        vwp[t] = vwl[t];
+      }
+    }
     if constexpr (T::maybe_nan) {
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        const int rows = tl[t]->rows;
+        const int rows = r.rows[t];
         if (rows < 16) {
           // tokens of this lane's V bytes: 2j, 2j+1, 2j+8, 2j+9; zero the ones
           // past the context so that 0 * NaN cannot reach the sum
@@ -315,15 +360,15 @@ __device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B,
             const uint32_t mhi = (t0 + 8 < rows ? 0xFFFFu : 0u) | (t0 + 9 < rows ? 0xFFFF0000u : 0u);
 #pragma unroll
             for (int w = 0; w < NU32 / 2; ++w) {
-              vw[t][2 * w] &= mlo;
-              vw[t][2 * w + 1] &= mhi;
+              vwp[t][2 * w] &= mlo;
+              vwp[t][2 * w + 1] &= mhi;
             }
           } else {
             const uint32_t msk = (t0 < rows ? 0xFFu : 0u) | (t0 + 1 < rows ? 0xFF00u : 0u) |
                                  (t0 + 8 < rows ? 0xFF0000u : 0u) |
                                  (t0 + 9 < rows ? 0xFF000000u : 0u);
 #pragma unroll
-            for (int w = 0; w < NU32; ++w) vw[t][w] &= msk;
+            for (int w = 0; w < NU32; ++w) vwp[t][w] &= msk;
           }
         }
       }
@@ -334,11 +379,63 @@ __device__ __forceinline__ void process_pair(const TileRef& A, const TileRef& B,
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         uint32_t a0, a1, a2, a3;
-        word_to_h2<FMT>(vw[t], 2 * mt, a0, a2);      // channel 16mt+g   : tokens 2j,2j+1 | 2j+8,2j+9
-        word_to_h2<FMT>(vw[t], 2 * mt + 1, a1, a3);  // channel 16mt+g+8
+        word_to_h2<FMT>(vwp[t], 2 * mt, a0, a2);      // channel 16mt+g   : tokens 2j,2j+1 | 2j+8,2j+9
+        word_to_h2<FMT>(vwp[t], 2 * mt + 1, a1, a3);  // channel 16mt+g+8
         mma_16816(o[mt], a0, a1, a2, a3, bh0[t][gi], bh1[t][gi]);
         mma_16816(o[mt], a0, a1, a2, a3, bl0[t][gi], bl1[t][gi]);
       }
+    }
+  }
+}
+
+// Q fragments of a unit: head n = g of the tile, channels 16kk + 4j .. +3.
+// Per-channel pools fold the K channel scale into q (fp32), scale the result by
+// 2^eq so that max|q'| lies in [2^13, 2^14), and split it into fp16 hi + lo;
+// csc then carries 2^-eq.
+template <int FMT, int D>
+__device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, int ht, int lane,
+                                       uint32_t (&qb)[D / 16][2],
+                                       uint32_t (&ql)[FmtTraits<FMT>::channel ? D / 16 : 1][2],
+                                       float& csc) {
+  constexpr int KS = D / 16;
+  const int g = lane >> 2, j = lane & 3;
+  const int Gt = min(8, p.G - 8 * ht);
+  const bool hv = g < Gt;
+  const int hq = h * p.G + 8 * ht + (hv ? g : 0);
+  const __half* qp = p.q + ((int64_t)s * p.Hq + hq) * D;
+  csc = p.sm_scale_log2;
+  if constexpr (!FmtTraits<FMT>::channel) {
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint2 v = hv ? *reinterpret_cast<const uint2*>(qp + 16 * kk + 4 * j) : make_uint2(0, 0);
+      qb[kk][0] = v.x;
+      qb[kk][1] = v.y;
+    }
+  } else {
+    const float* ksc = p.pool.chan_scales + (int64_t)h * D;
+    float qf[KS][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint2 v = hv ? *reinterpret_cast<const uint2*>(qp + 16 * kk + 4 * j) : make_uint2(0, 0);
+      __half2 a = *reinterpret_cast<__half2*>(&v.x), b = *reinterpret_cast<__half2*>(&v.y);
+      const int d0 = 16 * kk + 4 * j;
+      qf[kk][0] = __low2float(a) * ksc[d0 + 0];
+      qf[kk][1] = __high2float(a) * ksc[d0 + 1];
+      qf[kk][2] = __low2float(b) * ksc[d0 + 2];
+      qf[kk][3] = __high2float(b) * ksc[d0 + 3];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qf[kk][e]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
+    const float up = ldexpf(1.f, eq);
+    csc = ldexpf(csc, -eq);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      split_h2(qf[kk][0] * up, qf[kk][1] * up, qb[kk][0], ql[kk][0]);
+      split_h2(qf[kk][2] * up, qf[kk][3] * up, qb[kk][1], ql[kk][1]);
     }
   }
 }
@@ -347,89 +444,100 @@ template <int FMT, int D, int NG>
 __global__ void __launch_bounds__(kDecodeThreads)
     kvq_decode_kernel(const DecodeParams p) {
   using T = FmtTraits<FMT>;
-  constexpr int KS = D / 16;                  // k-steps of Q.K = m-tiles of P.V
-  constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;  // u32 per lane per sub-tile
-  constexpr int KPG = KS / NG;                // k-steps per scale group
+  constexpr int KS = D / 16;
   const float kNegInf = __int_as_float(0xff800000u);
 
   extern __shared__ __align__(128) char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, j = lane & 3;
-  const int split = blockIdx.x;
-  const int h = blockIdx.y / p.n_ht, ht = blockIdx.y % p.n_ht;
-  const int s = blockIdx.z;
   const PoolView& pool = p.pool;
   const int bs = pool.bs;
   const int nstage = 1 << p.nstage_log2;
-
-  int L = p.lens[s];
-  if (L > p.max_ctx) {
-    if (threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
-    L = p.max_ctx;
-  }
-  if (L < 0) L = 0;
-  const int npages = (L + bs - 1) / bs;
-  const int pg0 = split * p.pps;
-  const int Gt = min(8, p.G - 8 * ht);  // q heads handled by this CTA
-  if (pg0 >= npages && !(split == 0 && p.nsplit == 1)) return;  // empty split: merge skips it
-  const int pg1 = min(npages, pg0 + p.pps);
+  const int U = pool.Hkv * p.n_ht;  // units per sequence
 
   char* stages = smem + warp * nstage * p.stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecodeWarps * nstage * p.stage_bytes) +
-                   warp * nstage;
-  int* stage_phys = reinterpret_cast<int*>(
-                        reinterpret_cast<uint64_t*>(smem + kDecodeWarps * nstage * p.stage_bytes) +
-                        kDecodeWarps * nstage) +
-                    warp * nstage;
+  uint64_t* bars_base = reinterpret_cast<uint64_t*>(smem + kDecodeWarps * nstage * p.stage_bytes);
+  uint64_t* bars = bars_base + warp * nstage;
+  int* phys_base = reinterpret_cast<int*>(bars_base + kDecodeWarps * nstage);
+  int* stage_phys = phys_base + warp * nstage;
+  int* wtot = phys_base + kDecodeWarps * nstage;  // [kDecodeWarps]
+  int* PS = wtot + kDecodeWarps;                  // [S + 1] page prefix over sequences
 
-  const int span = pg1 - pg0;
-  const int n_w = span > warp ? (span - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
-
-  // ---- Q fragments: head n = g of this tile, channels 16kk + 4j .. +3.
-  uint32_t qb[KS][2];
-  uint32_t ql[T::channel ? KS : 1][2];
-  float csc = p.sm_scale_log2;
+  // ---- pages per sequence and their prefix (every CTA computes the same)
   {
-    const bool hv = g < Gt;
-    const int hq = h * p.G + 8 * ht + (hv ? g : 0);
-    const __half* qp = p.q + ((int64_t)s * p.Hq + hq) * D;
-    if constexpr (!T::channel) {
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        uint2 v = hv ? *reinterpret_cast<const uint2*>(qp + 16 * kk + 4 * j) : make_uint2(0, 0);
-        qb[kk][0] = v.x;
-        qb[kk][1] = v.y;
+    int carry = 0;
+    for (int base = 0; base < p.S; base += kDecodeThreads) {
+      const int s = base + threadIdx.x;
+      int v = 0;
+      if (s < p.S) {
+        int L = p.lens[s];
+        if (L > p.max_ctx) {
+          if (blockIdx.x == 0) set_error(pool.err, ERR_RANGE);
+          L = p.max_ctx;
+        }
+        v = L > 0 ? (L + bs - 1) / bs * U : 0;
       }
-    } else {
-      // q' = q * s_K[h][d] (fp32), scaled by 2^Eq so that max|q'| lies in
-      // [2^13, 2^14), then split into fp16 hi + lo.
-      const float* ksc = pool.chan_scales + (int64_t)h * D;
-      float qf[KS][4];
-      float amax = 0.f;
+      int x = v;
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        uint2 v = hv ? *reinterpret_cast<const uint2*>(qp + 16 * kk + 4 * j) : make_uint2(0, 0);
-        __half2 a = *reinterpret_cast<__half2*>(&v.x), b = *reinterpret_cast<__half2*>(&v.y);
-        const int d0 = 16 * kk + 4 * j;
-        qf[kk][0] = __low2float(a) * ksc[d0 + 0];
-        qf[kk][1] = __high2float(a) * ksc[d0 + 1];
-        qf[kk][2] = __low2float(b) * ksc[d0 + 2];
-        qf[kk][3] = __high2float(b) * ksc[d0 + 3];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qf[kk][e]));
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
       }
+      if (lane == 31) wtot[warp] = x;
+      __syncthreads();
+      int before = 0, all = 0;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
-      const float up = ldexpf(1.f, eq);
-      csc = ldexpf(csc, -eq);
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        split_h2(qf[kk][0] * up, qf[kk][1] * up, qb[kk][0], ql[kk][0]);
-        split_h2(qf[kk][2] * up, qf[kk][3] * up, qb[kk][1], ql[kk][1]);
+      for (int w = 0; w < kDecodeWarps; ++w) {
+        before += w < warp ? wtot[w] : 0;
+        all += wtot[w];
       }
+      if (s < p.S) PS[s + 1] = carry + before + x;
+      carry += all;
+      __syncthreads();
     }
+    if (threadIdx.x == 0) PS[0] = 0;
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int s = threadIdx.x; s <= p.S; s += kDecodeThreads) p.ps[s] = PS[s];
   }
+  // sequences with nothing to attend get zeros
+  for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
+    if (PS[s + 1] != PS[s]) continue;
+    float* o = p.out + (int64_t)s * p.Hq * D;
+    for (int i = threadIdx.x; i < p.Hq * D; i += kDecodeThreads) o[i] = 0.f;
+  }
+
+  const int Ttot = PS[p.S];
+  const int nwarps = gridDim.x * kDecodeWarps;
+  const int gw = blockIdx.x * kDecodeWarps + warp;
+  const int ppw = p.ppw_fixed > 0 ? p.ppw_fixed : (Ttot + nwarps - 1) / nwarps;
+  const int a0 = (int)min((int64_t)gw * ppw, (int64_t)Ttot);
+  const int b0 = (int)min((int64_t)a0 + ppw, (int64_t)Ttot);
+  const int n_w = b0 - a0;
+  if (n_w <= 0) return;
+
+  auto locate = [&](int x) -> Cursor {
+    int lo = 0, hi = p.S;  // PS[lo] <= x < PS[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (PS[mid] <= x) lo = mid; else hi = mid;
+    }
+    Cursor c;
+    c.s = lo;
+    c.Ps = (PS[lo + 1] - PS[lo]) / U;
+    const int r = x - PS[lo];
+    c.lu = r / c.Ps;
+    c.pi = r - c.lu * c.Ps;
+    return c;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.pi < c.Ps) return;
+    c.pi = 0;
+    if (++c.lu < U) return;
+    c.lu = 0;
+    do { ++c.s; } while (c.s < p.S && PS[c.s + 1] == PS[c.s]);
+    c.Ps = c.s < p.S ? (PS[c.s + 1] - PS[c.s]) / U : 1;
+  };
 
   // ---- pipeline set-up
   if (lane == 0) {
@@ -438,45 +546,56 @@ __global__ void __launch_bounds__(kDecodeThreads)
   }
   __syncwarp();
 
-  const int64_t trow = (int64_t)s * p.max_blocks;
-  int tbl = (lane < n_w) ? p.table[trow + pg0 + warp + lane * kDecodeWarps] : 0;
   const uint32_t page_tx = pool.page_bytes + (T::token_scales ? 2 * bs * 4 : 0);
-
-  auto issue = [&](int i) {
-    if ((i & 31) == 0 && i > 0)
-      tbl = (i + lane < n_w) ? p.table[trow + pg0 + warp + (i + lane) * kDecodeWarps] : 0;
-    const int phys = __shfl_sync(0xffffffffu, tbl, i & 31);
-    if (lane == 0) {
-      const int st = i & (nstage - 1);
-      char* dst = stages + st * p.stage_bytes;
-      const bool ok = phys >= 0 && (int64_t)phys < pool.num_blocks;
-      stage_phys[st] = ok ? phys : -1;
-      if (ok) {
-        mbar_arrive_expect_tx(&bars[st], page_tx);
-        bulk_g2s(dst, pool.pages + ((int64_t)phys * pool.Hkv + h) * pool.page_bytes,
-                 pool.page_bytes, &bars[st]);
-        if constexpr (T::token_scales)
-          bulk_g2s(dst + pool.page_bytes, pool.tok_scales + (int64_t)phys * 2 * bs, 2 * bs * 4,
-                   &bars[st]);
-      } else {
-        set_error(pool.err, ERR_RANGE);
-        mbar_arrive(&bars[st]);
-      }
+  // Block-table entries of the pages to issue, cached one per lane and loaded
+  // 32 to 64 pages ahead: tcur covers issue indices [tbase, tbase+32), tnext
+  // the 32 after, so a table load never stalls a copy issue.
+  auto table_entry = [&](int n) -> int {  // page n of this warp's range
+    if (n >= n_w) return -1;
+    const Cursor c = locate(a0 + n);
+    return p.table[(int64_t)c.s * p.max_blocks + c.pi];
+  };
+  int tbase = 0;
+  int tcur = table_entry(lane), tnext = table_entry(32 + lane);
+  Cursor ic = locate(a0);  // next page to issue (lane 0 tracks it)
+  int n_issued = 0;
+  auto issue_one = [&](int phys) {  // lane 0 only: page at the issue cursor
+    const int st = n_issued & (nstage - 1);
+    char* dst = stages + st * p.stage_bytes;
+    const bool ok = phys >= 0 && (int64_t)phys < pool.num_blocks;
+    stage_phys[st] = ok ? phys : -1;
+    if (ok) {
+      const int h = ic.lu / p.n_ht;
+      mbar_arrive_expect_tx(&bars[st], page_tx);
+      bulk_g2s(dst, pool.pages + ((int64_t)phys * pool.Hkv + h) * pool.page_bytes, pool.page_bytes,
+               &bars[st]);
+      if constexpr (T::token_scales)
+        bulk_g2s(dst + pool.page_bytes, pool.tok_scales + (int64_t)phys * 2 * bs, 2 * bs * 4,
+                 &bars[st]);
+    } else {
+      set_error(pool.err, ERR_RANGE);
+      mbar_arrive(&bars[st]);
     }
   };
+  // All lanes call this (the table cache is spread over the lanes); lane 0 issues.
+  auto issue_next = [&]() {
+    if (n_issued - tbase == 32) {
+      tcur = tnext;
+      tbase += 32;
+      tnext = table_entry(tbase + 32 + lane);
+    }
+    const int phys = __shfl_sync(0xffffffffu, tcur, n_issued - tbase);
+    if (lane == 0) {
+      issue_one(phys);
+      advance(ic);
+    }
+    ++n_issued;
+  };
+  {
+    const int npre = min(n_w, nstage);
+    for (int i = 0; i < npre; ++i) issue_next();
+  }
 
-  const int npre = min(n_w, nstage);
-  for (int i = 0; i < npre; ++i) issue(i);
-
-  // ---- per-warp online-softmax state (heads 2j, 2j+1 of the tile)
-  float m[2] = {kNegInf, kNegInf};
-  float l[2] = {0.f, 0.f};
-  int E = (T::row_scales) ? 100 : 14;  // power-of-two prescale of the P.V operand
-  float o[KS][4];
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-  // Bounded wait for stage i; false (and the timeout bit set) if it gave up.
   auto wait_stage = [&](int i) -> bool {
     const int st = i & (nstage - 1);
     const uint32_t parity = (i >> p.nstage_log2) & 1;
@@ -488,150 +607,234 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     return true;
   };
-  // Sub-tile `sub` of the warp's i-th page as a tile reference (rows = 0 when
-  // the page is absent, out of range or the sub-tile lies past the context).
-  auto tile_of = [&](int i, int sub) -> TileRef {
-    TileRef t;
-    const int st = i & (nstage - 1);
-    const char* stage = stages + st * p.stage_bytes;
-    t.k = stage + sub * pool.sub_bytes;
-    t.v = stage + pool.code_bytes + sub * pool.sub_bytes;
-    t.ks = nullptr;
-    t.vs = nullptr;
-    if constexpr (T::group_scales) {
-      t.ks = reinterpret_cast<const float*>(stage + 2 * pool.code_bytes) + sub * 16 * NG;
-      t.vs = t.ks + bs * NG;
-    } else if constexpr (T::token_scales) {
-      t.ks = reinterpret_cast<const float*>(stage + pool.page_bytes) + sub * 16;
-      t.vs = t.ks + bs;
-    }
-    const int page = pg0 + warp + i * kDecodeWarps;
-    const int nvalid = min(bs, L - page * bs) - sub * 16;
-    t.rows = (i < n_w && stage_phys[st] >= 0) ? max(0, min(16, nvalid)) : 0;
-    return t;
+
+  // ---- per-unit state (heads 2j, 2j+1 of the tile)
+  uint32_t qb[KS][2];
+  uint32_t ql[T::channel ? KS : 1][2];
+  float csc = 0.f;
+  float m[2], l[2], o[KS][4];
+  int E = 0;
+  Cursor cc = locate(a0);     // page being consumed
+  const Cursor first = cc;    // the unit this warp's range starts in
+  int seg_pi0 = cc.pi;        // first page of the current unit in this range
+  int L = 0;                  // context length of the current unit's sequence
+  auto start_unit = [&]() {
+    L = min(p.lens[cc.s], p.max_ctx);
+    load_q<FMT, D>(p, cc.s, cc.lu / p.n_ht, cc.lu % p.n_ht, lane, qb, ql, csc);
+    m[0] = m[1] = kNegInf;
+    l[0] = l[1] = 0.f;
+    E = T::row_scales ? 100 : 14;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    seg_pi0 = cc.pi;
   };
 
-  const bool pair_pages = bs == 16;  // one 16-token sub-tile per page: pages go in pairs
-  for (int i = 0; i < n_w; i += pair_pages ? 2 : 1) {
-    const bool two = pair_pages && i + 1 < n_w;
-    if (!wait_stage(i) || (two && !wait_stage(i + 1))) break;
-    if (pair_pages) {
-      TileRef A = tile_of(i, 0);
-      TileRef B = two ? tile_of(i + 1, 0) : A;
-      if (!two) B.rows = 0;
-      if (A.rows == 0 && B.rows > 0) { TileRef t = A; A = B; B = t; }
-      if (B.rows == 0) { const int r = B.rows; B = A; B.rows = r; }
-      process_pair<FMT, D, NG>(A, B, lane, qb, ql, csc, m, l, E, o);
-    } else {
-      const int page = pg0 + warp + i * kDecodeWarps;
-      const int nsub = (min(bs, L - page * bs) + 15) >> 4;
-      for (int sp = 0; sp < nsub; sp += 2) {
-        TileRef A = tile_of(i, sp);
-        TileRef B = tile_of(i, sp + 1 < nsub ? sp + 1 : sp);
-        if (sp + 1 >= nsub) B.rows = 0;
-        if (A.rows == 0) break;  // page skipped (out-of-range block id)
-        process_pair<FMT, D, NG>(A, B, lane, qb, ql, csc, m, l, E, o);
+  // Write the unit's result (whole unit in this range) or its partial, and
+  // merge the partials if this piece is the unit's last to finish.
+  auto finish_unit = [&](const Cursor& u, int seg_end) {
+    const int h = u.lu / p.n_ht, ht = u.lu % p.n_ht;
+    const int Gt = min(8, p.G - 8 * ht);
+    const float lt0 = warp_sum_over_rows(l[0]), lt1 = warp_sum_over_rows(l[1]);
+    const float inv2E = pow2f(-E);
+    const float* vch = T::channel ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
+    const int64_t row0 = (int64_t)u.s * p.Hq + h * p.G + 8 * ht;
+    if (seg_pi0 == 0 && seg_end == u.Ps) {
+      const float f0 = lt0 > 0.f ? inv2E / lt0 : 0.f, f1 = lt1 > 0.f ? inv2E / lt1 : 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d0 = 16 * mt + g;
+        const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
+        if (2 * j < Gt) {
+          float* dst = p.out + (row0 + 2 * j) * D;
+          dst[d0] = o[mt][0] * f0 * c0;
+          dst[d0 + 8] = o[mt][2] * f0 * c8;
+        }
+        if (2 * j + 1 < Gt) {
+          float* dst = p.out + (row0 + 2 * j + 1) * D;
+          dst[d0] = o[mt][1] * f1 * c0;
+          dst[d0 + 8] = o[mt][3] * f1 * c8;
+        }
       }
+      return;
     }
-    __syncwarp();
-    if (i + nstage < n_w) issue(i + nstage);
-    if (two && i + 1 + nstage < n_w) issue(i + 1 + nstage);
-  }
-
-  // ---- per-warp totals, then merge the warps through shared memory
-  l[0] = warp_sum_over_rows(l[0]);
-  l[1] = warp_sum_over_rows(l[1]);
-  __syncthreads();  // every warp is done with its stages
-  constexpr int OST = D + 4;  // padded row stride (conflict-free stores)
-  float* Os = reinterpret_cast<float*>(smem);            // [W][8][OST]
-  float* Ms = Os + kDecodeWarps * 8 * OST;               // [W][8]
-  float* Ls = Ms + kDecodeWarps * 8;                     // [W][8]
-  int* Es = reinterpret_cast<int*>(Ls + kDecodeWarps * 8);  // [W]
-  {
-    float* ow = Os + warp * 8 * OST;
+    // -- partial: rows (m, l, O) in true units
+    const int slot = (u.s == first.s && u.lu == first.lu) ? 0 : 1;
+    float* base = p.part + ((int64_t)gw * 2 + slot) * kPartRows * (D + 2);
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       const int d0 = 16 * mt + g;
-      ow[(2 * j) * OST + d0] = o[mt][0];
-      ow[(2 * j + 1) * OST + d0] = o[mt][1];
-      ow[(2 * j) * OST + d0 + 8] = o[mt][2];
-      ow[(2 * j + 1) * OST + d0 + 8] = o[mt][3];
+      const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
+      float* r0 = base + (2 * j) * (D + 2) + 2;
+      float* r1 = base + (2 * j + 1) * (D + 2) + 2;
+      r0[d0] = o[mt][0] * inv2E * c0;
+      r0[d0 + 8] = o[mt][2] * inv2E * c8;
+      r1[d0] = o[mt][1] * inv2E * c0;
+      r1[d0 + 8] = o[mt][3] * inv2E * c8;
     }
     if (g == 0) {
-      Ms[warp * 8 + 2 * j] = m[0];
-      Ms[warp * 8 + 2 * j + 1] = m[1];
-      Ls[warp * 8 + 2 * j] = l[0];
-      Ls[warp * 8 + 2 * j + 1] = l[1];
+      base[(2 * j) * (D + 2) + 0] = m[0];
+      base[(2 * j) * (D + 2) + 1] = lt0;
+      base[(2 * j + 1) * (D + 2) + 0] = m[1];
+      base[(2 * j + 1) * (D + 2) + 1] = lt1;
     }
-    if (lane == 0) Es[warp] = E;
-  }
-  __syncthreads();
-  const bool direct = p.nsplit == 1;
-  for (int idx = threadIdx.x; idx < Gt * D; idx += kDecodeThreads) {
-    const int r = idx / D, d = idx - r * D;
-    float mstar = kNegInf;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) mstar = fmaxf(mstar, Ms[w * 8 + r]);
-    float acc = 0.f, wsum = 0.f;
-    if (mstar != kNegInf) {
-#pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
-        const float mw = Ms[w * 8 + r];
-        if (mw == kNegInf) continue;
-        const float f = fast_exp2(mw - mstar);
-        wsum = fmaf(f, Ls[w * 8 + r], wsum);
-        acc = fmaf(f * pow2f(-Es[w]), Os[(w * 8 + r) * OST + d], acc);
+  };
+
+  // ---- main loop: pages of this warp's range, two 16-token sub-tiles at a time
+  start_unit();
+  PairRegs<FMT, D, NG> R;
+  int i = 0;
+  while (i < n_w) {
+    // pages consumed this step: a pair of one-sub-tile pages of the same unit,
+    // or one page of two or more sub-tiles
+    const bool two = bs == 16 && i + 1 < n_w && cc.pi + 1 < cc.Ps;
+    const int npg = two ? 2 : 1;
+    if (!wait_stage(i) || (two && !wait_stage(i + 1))) break;
+    auto issue_after = [&]() {
+      for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
+    };
+    if (two) {
+      const int st0 = i & (nstage - 1), st1 = (i + 1) & (nstage - 1);
+      const int r0 = stage_phys[st0] >= 0 ? min(16, L - cc.pi * 16) : 0;
+      const int r1 = stage_phys[st1] >= 0 ? min(16, L - (cc.pi + 1) * 16) : 0;
+      // an absent page (rows = 0) contributes nothing; keep the valid one in tile 0
+      const int sA = r0 > 0 ? st0 : st1;
+      load_tile<FMT, D, NG>(R, 0, stages + sA * p.stage_bytes, 0, r0 > 0 ? r0 : r1, pool, lane);
+      load_tile<FMT, D, NG>(R, 1, stages + st1 * p.stage_bytes, 0, r0 > 0 ? r1 : 0, pool, lane);
+      if constexpr (T::early_release) {
+        __syncwarp();
+        issue_after();
       }
-      if constexpr (T::channel) acc *= pool.chan_scales[((int64_t)pool.Hkv + h) * D + d];
-    }
-    const int hq = h * p.G + 8 * ht + r;
-    const int64_t row = (int64_t)s * p.Hq + hq;
-    if (direct) {
-      p.out[row * D + d] = wsum > 0.f ? acc / wsum : 0.f;
+      compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
     } else {
-      p.part_o[(row * p.nsplit + split) * D + d] = acc;
-      if (d == 0) {
-        p.part_ml[(row * p.nsplit + split) * 2 + 0] = mstar;
-        p.part_ml[(row * p.nsplit + split) * 2 + 1] = wsum;
+      const int st = i & (nstage - 1);
+      const char* stage = stages + st * p.stage_bytes;
+      const int nvalid = stage_phys[st] >= 0 ? min(bs, L - cc.pi * bs) : 0;
+      const int nsub = (nvalid + 15) >> 4;
+      if (nsub == 0) {
+        if constexpr (T::early_release) {
+          __syncwarp();
+          issue_after();
+        }
+      }
+      for (int sp = 0; sp < nsub; sp += 2) {
+        const int rA = min(16, nvalid - sp * 16);
+        const int rB = sp + 1 < nsub ? min(16, nvalid - (sp + 1) * 16) : 0;
+        load_tile<FMT, D, NG>(R, 0, stage, sp, rA, pool, lane);
+        load_tile<FMT, D, NG>(R, 1, stage, sp + 1 < nsub ? sp + 1 : sp, rB, pool, lane);
+        if constexpr (T::early_release) {
+          if (sp + 2 >= nsub) {
+            __syncwarp();
+            issue_after();
+          }
+        }
+        compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
       }
     }
-  }
-}
-
-// Log-sum-exp merge of the split partials: one CTA of D threads per (seq, q head).
-template <int D>
-__global__ void __launch_bounds__(D) kvq_merge_kernel(const DecodeParams p) {
-  const float kNegInf = __int_as_float(0xff800000u);
-  const int row = blockIdx.x;  // s * Hq + hq
-  const int s = row / p.Hq;
-  const int d = threadIdx.x;
-  int L = min(max(p.lens[s], 0), p.max_ctx);
-  const int npages = (L + p.pool.bs - 1) / p.pool.bs;
-  const int n = (npages + p.pps - 1) / p.pps;
-  const float* ml = p.part_ml + (int64_t)row * p.nsplit * 2;
-  const float* po = p.part_o + (int64_t)row * p.nsplit * D;
-  float mstar = kNegInf;
-  for (int i = 0; i < n; ++i) mstar = fmaxf(mstar, ml[2 * i]);
-  float acc = 0.f, wsum = 0.f;
-  if (mstar != kNegInf) {
-    for (int i = 0; i < n; ++i) {
-      const float mi = ml[2 * i];
-      if (mi == kNegInf) continue;
-      const float f = fast_exp2(mi - mstar);
-      wsum = fmaf(f, ml[2 * i + 1], wsum);
-      acc = fmaf(f, po[(int64_t)i * D + d], acc);
+    if constexpr (!T::early_release) {
+      __syncwarp();
+      issue_after();
+    }
+    // advance the consumer; close the unit at its last page or at the range end
+    i += npg;
+    const Cursor done = cc;
+    const int end_pi = cc.pi + npg;
+    for (int k = 0; k < npg; ++k) advance(cc);
+    if (end_pi == done.Ps || i == n_w) {
+      finish_unit(done, end_pi);
+      if (i < n_w) start_unit();
     }
   }
-  p.out[(int64_t)row * D + d] = wsum > 0.f ? acc / wsum : 0.f;
+  // Let the merge grid launch; it still waits for this grid's completion (and
+  // memory) before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-}  // namespace kvq
-
-namespace kvq {
+// Log-sum-exp merge of the units that the decode kernel's warp ranges cut:
+// unit u's pieces are the partials of warps wf..wl (slot 1 of wf when its range
+// started before the unit, slot 0 otherwise).  Launched as a programmatic
+// dependent of the decode kernel: griddepcontrol.wait returns once the decode
+// grid has completed and its writes are visible.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float kNegInf = __int_as_float(0xff800000u);
+  constexpr int NW = kMergeThreads / 32;
+  constexpr int NE = D / 32;   // output elements per lane
+  constexpr int CH = 8;        // pieces loaded together (one round trip)
+  const int lane = threadIdx.x & 31;
+  const int U = p.pool.Hkv * p.n_ht;
+  const int* PS = p.ps;
+  const int Ttot = __ldcg(PS + p.S);
+  const int nwarps = p.grid * kDecodeWarps;
+  const int ppw = p.ppw_fixed > 0 ? p.ppw_fixed : (Ttot + nwarps - 1) / nwarps;
+  if (ppw <= 0) return;
+  // one task per (unit, Q-head row of its tile); one warp per task
+  const int64_t ntasks = (int64_t)p.S * U * kPartRows;
+  for (int64_t task = (int64_t)blockIdx.x * NW + (threadIdx.x >> 5); task < ntasks;
+       task += (int64_t)gridDim.x * NW) {
+    const int64_t u = task / kPartRows;
+    const int rr = (int)(task % kPartRows);
+    const int s = (int)(u / U), lu = (int)(u % U);
+    const int ht = lu % p.n_ht;
+    if (rr >= min(8, p.G - 8 * ht)) continue;
+    const int ps0 = __ldcg(PS + s), ps1 = __ldcg(PS + s + 1);
+    const int Ps = (ps1 - ps0) / U;
+    if (Ps == 0) continue;
+    const int U0 = ps0 + lu * Ps;
+    const int wf = U0 / ppw, wl = (U0 + Ps - 1) / ppw;
+    if (wf == wl) continue;  // written directly by its warp
+    const int n_u = wl - wf + 1;
+    float M = kNegInf, Lsum = 0.f, acc[NE];
+#pragma unroll
+    for (int i = 0; i < NE; ++i) acc[i] = 0.f;
+    for (int k0 = 0; k0 < n_u; k0 += CH) {
+      float mk[CH], lk[CH], ok[CH][NE];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int k = k0 + c;
+        if (k < n_u) {
+          const int w = wf + k;
+          const int sl = (k == 0 && (int64_t)w * ppw < U0) ? 1 : 0;
+          const float* pr = p.part + (((int64_t)w * 2 + sl) * kPartRows + rr) * (D + 2);
+          mk[c] = __ldcg(pr);
+          lk[c] = __ldcg(pr + 1);
+#pragma unroll
+          for (int i = 0; i < NE; ++i) ok[c][i] = __ldcg(pr + 2 + lane + 32 * i);
+        } else {
+          mk[c] = kNegInf;
+          lk[c] = 0.f;
+#pragma unroll
+          for (int i = 0; i < NE; ++i) ok[c][i] = 0.f;
+        }
+      }
+      float cm = M;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) cm = fmaxf(cm, mk[c]);
+      if (cm == kNegInf) continue;
+      const float fo = M == kNegInf ? 0.f : fast_exp2(M - cm);
+      Lsum *= fo;
+#pragma unroll
+      for (int i = 0; i < NE; ++i) acc[i] *= fo;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const float wgt = mk[c] == kNegInf ? 0.f : fast_exp2(mk[c] - cm);
+        Lsum = fmaf(wgt, lk[c], Lsum);
+#pragma unroll
+        for (int i = 0; i < NE; ++i) acc[i] = fmaf(wgt, ok[c][i], acc[i]);
+      }
+      M = cm;
+    }
+    const int h = lu / p.n_ht;
+    float* dst = p.out + ((int64_t)s * p.Hq + h * p.G + 8 * ht + rr) * D;
+#pragma unroll
+    for (int i = 0; i < NE; ++i) dst[lane + 32 * i] = Lsum > 0.f ? acc[i] / Lsum : 0.f;
+  }
+}
 
 struct DecodeLaunch {
   DecodeParams p;
   dim3 grid;
+  unsigned merge_grid;
   int smem;
   cudaStream_t st;
 };
@@ -651,9 +854,19 @@ cudaError_t run_decode(const DecodeLaunch& l) {
     attr_set[dev] = true;
   }
   kvq_decode_kernel<FMT, D, NG><<<l.grid, kDecodeThreads, l.smem, l.st>>>(l.p);
-  if (l.p.nsplit > 1)
-    kvq_merge_kernel<D><<<static_cast<unsigned>(l.p.S * l.p.Hq), D, 0, l.st>>>(l.p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(l.merge_grid);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = l.st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D>, l.p);
 }
 
 template <int FMT>

@@ -19,13 +19,15 @@ cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_
 
 // Launch geometry of one decode call.
 struct DecodePlan {
-  int pps = 0;          // blocks per split
-  int nsplit = 0;       // splits (grid.x)
+  int grid = 0;         // persistent CTAs
+  int ppw_fixed = 0;    // pages per warp when forced; 0 = balanced
   int n_ht = 0;         // head tiles of 8 Q heads per kv head
   int nstage_log2 = 0;  // pipeline stages per warp = 1 << nstage_log2
   int stage_bytes = 0;  // bytes of one stage
   int smem_bytes = 0;   // dynamic shared memory per CTA
-  size_t ws_bytes = 0;  // workspace (split partials); 0 when nsplit == 1
+  int merge_grid = 0;   // CTAs of the merge kernel
+  size_t ps_bytes = 0;  // page prefix at the start of the workspace
+  size_t ws_bytes = 0;  // page prefix + split partials
 };
 
 // Plan a decode call; `sms` is the device's SM count.  Returns false for an

@@ -115,7 +115,7 @@ def test_tiny_workload_full():
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     for sb in (1, 2, 3, 7):
         np.testing.assert_allclose(run_gpu_decode(pool, w, q, DEV, split_blocks=sb), got,
-                                   rtol=0, atol=1e-5)
+                                   rtol=2e-5, atol=2e-5)
     pool.close()
 
 
@@ -144,9 +144,11 @@ def test_split_k_invariance(bs):
     q = synth.queries(w, 0)
     base = run_gpu_decode(pool, w, q, DEV, split_blocks=10 ** 6)   # one split
     np.testing.assert_allclose(base, ref.decode(q, table, w.context_lens), rtol=0, atol=TOL)
+    # Only the fp32 summation order changes with the split: one block per
+    # piece merges up to ~160 partials, ~160 * 2^-24 relative, hence 2e-5.
     for sb in (1, 2, 7, 0):
         np.testing.assert_allclose(run_gpu_decode(pool, w, q, DEV, split_blocks=sb), base,
-                                   rtol=0, atol=1e-5, err_msg="split_blocks=%d" % sb)
+                                   rtol=2e-5, atol=2e-5, err_msg="split_blocks=%d" % sb)
     pool.close()
 
 
