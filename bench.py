@@ -293,13 +293,23 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=dev)
     sm_scale = w.D ** -0.5
 
+    fused = args.step_api == "fused"
+
     def step(qq, kk, vv, sl, ln, oo, ev=None):
         for l in range(L):
-            pools[l].append(kk[l], vv[l], sl, stream)
-            if ev is not None:
-                ev[l][0].record(stream)
-            kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l], ws,
-                                 0, stream)
+            if fused:
+                # one call: append at position L-1 (slot from the block table),
+                # then the decode as a programmatic dependent of the append
+                if ev is not None:
+                    ev[l][0].record(stream)
+                kvq.kvq_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln, max_ctx,
+                                    sm_scale, oo[l], ws, stream)
+            else:
+                pools[l].append(kk[l], vv[l], sl, stream)
+                if ev is not None:
+                    ev[l][0].record(stream)
+                kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l],
+                                     ws, 0, stream)
             if ev is not None:
                 ev[l][1].record(stream)
 
@@ -347,14 +357,17 @@ def run_ours(args, rank, world, local_rank):
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     q_d, kn_d, vn_d = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
     sl_d, ln_d = torch.empty_like(slots), torch.empty_like(lens)
-    h2d = sum(x.numel() * x.element_size() for x in (q_h, kn_h, vn_h, sl_h, ln_h))
+    # the fused step derives the slots on the device; the separate one copies them
+    h2d_in = (q_h, kn_h, vn_h, ln_h) if fused else (q_h, kn_h, vn_h, sl_h, ln_h)
+    h2d = sum(x.numel() * x.element_size() for x in h2d_in)
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
         kn_d.copy_(kn_h, non_blocking=True)
         vn_d.copy_(vn_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
+        if not fused:
+            sl_d.copy_(sl_h, non_blocking=True)
         ln_d.copy_(ln_h, non_blocking=True)
         step(q_d, kn_d, vn_d, sl_d, ln_d, out)
         out_h.copy_(out, non_blocking=True)
@@ -385,10 +398,15 @@ def run_ours(args, rank, world, local_rank):
     peak = float(peaks["hbm_gbs"])
     dec_avg_ms = float(np.mean(dec_ms))
     fmt0, g0 = w.layer_formats[0]
-    per_launch = layer_bytes(w, fmt0, g0)["decode"]
+    lb0 = layer_bytes(w, fmt0, g0)
+    # the timed call: the fused step (append + decode + merge) or the decode alone
+    per_launch = lb0["decode"] + (lb0["append"] if fused else 0)
     achieved = per_launch / (dec_avg_ms * 1e-3) / 1e9
     # launches: per layer one append, one decode and one split merge
     launches_per_layer = 3
+    call = ("kvq_decode_step call (append kernel, decode kernel launched as its programmatic "
+            "dependent, dependent split merge)" if fused else
+            "kvq_paged_decode call (decode kernel + dependent split merge)")
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
@@ -404,14 +422,15 @@ def run_ours(args, rank, world, local_rank):
             "pool_blocks_per_layer": w.num_blocks,
             "l2": "inputs larger than L2: %d per-layer pools, %.1f GB"
                   % (L, sum(p.buffer.numel() for p in pools) / 1e9),
-            "step": "per layer: kvq_append (1 token/seq) then kvq_paged_decode",
+            "step": ("per layer: kvq_decode_step (append 1 token/seq at L-1, then decode)"
+                     if fused else "per layer: kvq_append (1 token/seq) then kvq_paged_decode"),
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "decode_tok_per_s": round(world * w.S / (ms * 1e-3), 1),
         "bytes_per_step": b,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": read_traffic(w.name),
-                     "kernel": "kvq_paged_decode call (decode kernel + dependent split merge)",
+                     "kernel": call,
                      "bytes_per_launch": per_launch, "avg_launch_ms": round(dec_avg_ms, 5),
                      "peak_source": "%s hbm_gbs" % peak_kind},
         "e2e": {"value": round(world * step_total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -470,6 +489,9 @@ def main():
     ap.add_argument("--workload", default="gqa_64x2048")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
+                    help="fused: one kvq_decode_step call per layer; separate: kvq_append "
+                         "then kvq_paged_decode")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers (profiling runs only; the bench line uses all)")
     args = ap.parse_args()

@@ -178,6 +178,30 @@ kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_
                                void* workspace, size_t ws_bytes, int split_blocks,
                                cudaStream_t stream);
 
+/* One whole decode step of one layer ([KVC] §1.1: the new token's K/V joins
+ * the cache, then the new Q attends over everything cached, itself included):
+ * kvq_append of one token per sequence followed by kvq_paged_decode.
+ *   k_new, v_new : fp16 [num_seqs][kv_heads][head_dim], 16-byte aligned;
+ *                  sequence s's token is stored at position context_lens[s]-1,
+ *                  i.e. in block block_table[s][(L-1)/block_size], offset
+ *                  (L-1)%block_size (the caller has already counted it in L
+ *                  and mapped its block)
+ *   the other arguments and the result are those of kvq_paged_decode, with
+ *   workspace sized by kvq_decode_workspace_bytes.
+ * Results equal kvq_append (slots derived as above) then kvq_paged_decode on
+ * the same stream.  A sequence with L == 0 stores nothing; L > max_context_len
+ * stores nothing and sets OUT_OF_RANGE (the decode clamps as documented); a
+ * negative block id at position L-1 sets OUT_OF_RANGE and stores nothing.
+ * The decode is launched as a programmatic dependent of the append, so its
+ * set-up overlaps the append; it reads the pool only after the append is done.
+ * The caller's k_new/v_new/q buffers must stay valid until the stream reaches
+ * this call, as for every other call. */
+kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
+                           const kvq_half* q, int num_seqs, int num_q_heads,
+                           const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* context_lens, int max_context_len, float sm_scale,
+                           float* out, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Maximum split-K scratch of kvq_paged_decode_noalloc, in bytes (16 MiB). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -223,11 +223,15 @@ size_t kvq_decode_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_
   return kvq_decode_workspace_bytes_ex(pool, num_seqs, num_q_heads, max_context_len, 0);
 }
 
-kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_seqs,
-                               int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
-                               const int32_t* context_lens, int max_context_len, float sm_scale,
-                               float* out, void* workspace, size_t ws_bytes, int split_blocks,
-                               cudaStream_t stream) {
+}  // extern "C"
+
+// Argument checks and plan shared by the decode entry points.
+static kvq_status prepare_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                                 int num_q_heads, const int32_t* block_table,
+                                 int max_blocks_per_seq, const int32_t* context_lens,
+                                 int max_context_len, float sm_scale, float* out, void* workspace,
+                                 size_t ws_bytes, int split_blocks, kvq::DecodeArgs* a,
+                                 kvq::DecodePlan* plan) {
   if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 ||
       max_context_len < 0 || split_blocks < 0)
     return KVQ_ERR_INVALID_ARG;
@@ -239,27 +243,63 @@ kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_
   if (num_seqs > 65535) return KVQ_ERR_UNSUPPORTED;
   if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(q) & 15) return KVQ_ERR_INVALID_ARG;
-  kvq::DecodePlan plan;
   if (!kvq::plan_decode(pool->view, num_seqs, num_q_heads, max_context_len, split_blocks,
-                        device_sms(), &plan))
+                        device_sms(), plan))
     return KVQ_ERR_UNSUPPORTED;
-  if (plan.ws_bytes > 0) {
-    if (workspace == nullptr || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
+  if (plan->ws_bytes > 0) {
+    if (workspace == nullptr || ws_bytes < plan->ws_bytes) return KVQ_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return KVQ_ERR_INVALID_ARG;
   }
+  a->pool = pool->view;
+  a->q = reinterpret_cast<const __half*>(q);
+  a->table = block_table;
+  a->lens = context_lens;
+  a->out = out;
+  a->workspace = workspace;
+  a->S = num_seqs;
+  a->Hq = num_q_heads;
+  a->max_blocks = max_blocks_per_seq;
+  a->max_ctx = max_context_len;
+  a->sm_scale = sm_scale;
+  return KVQ_OK;
+}
+
+extern "C" {
+
+kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                               int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len, float sm_scale,
+                               float* out, void* workspace, size_t ws_bytes, int split_blocks,
+                               cudaStream_t stream) {
   kvq::DecodeArgs a;
-  a.pool = pool->view;
-  a.q = reinterpret_cast<const __half*>(q);
-  a.table = block_table;
-  a.lens = context_lens;
-  a.out = out;
-  a.workspace = workspace;
-  a.S = num_seqs;
-  a.Hq = num_q_heads;
-  a.max_blocks = max_blocks_per_seq;
-  a.max_ctx = max_context_len;
-  a.sm_scale = sm_scale;
+  kvq::DecodePlan plan;
+  const kvq_status st =
+      prepare_decode(pool, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, context_lens,
+                     max_context_len, sm_scale, out, workspace, ws_bytes, split_blocks, &a, &plan);
+  if (st != KVQ_OK || num_seqs == 0) return st;
   return from_cuda(kvq::launch_decode(a, plan, stream));
+}
+
+kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
+                           const kvq_half* q, int num_seqs, int num_q_heads,
+                           const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* context_lens, int max_context_len, float sm_scale,
+                           float* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  kvq::DecodeArgs a;
+  kvq::DecodePlan plan;
+  const kvq_status st =
+      prepare_decode(pool, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, context_lens,
+                     max_context_len, sm_scale, out, workspace, ws_bytes, 0, &a, &plan);
+  if (st != KVQ_OK || num_seqs == 0) return st;
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return KVQ_ERR_INVALID_ARG;
+  cudaError_t e = kvq::launch_step_append(pool->view, reinterpret_cast<const __half*>(k_new),
+                                          reinterpret_cast<const __half*>(v_new), nullptr, num_seqs,
+                                          block_table, context_lens, max_blocks_per_seq,
+                                          max_context_len, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(kvq::launch_decode(a, plan, stream, /*dependent=*/true));
 }
 
 kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,

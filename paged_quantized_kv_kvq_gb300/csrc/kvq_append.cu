@@ -24,8 +24,12 @@ struct AppendParams {
   PoolView pool;
   const __half* k;
   const __half* v;
-  const int64_t* slots;
+  const int64_t* slots;  // null: decode-step form, the slot comes from table/lens
   int64_t T;
+  // decode-step form: token t is sequence t's new token, at position lens[t]-1
+  const int* table;
+  const int* lens;
+  int max_blocks, max_ctx;
 };
 
 __device__ __forceinline__ float absmax8(const __half2 (&x)[4]) {
@@ -58,7 +62,19 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
   const PoolView& pool = p.pool;
   const int64_t t = blockIdx.x;
   const int kv = blockIdx.y;
-  const int64_t slot = p.slots[t];
+  // a decode that depends on this append may launch now: it only reads the
+  // pool after waiting for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  int64_t slot;
+  if (p.slots != nullptr) {
+    slot = p.slots[t];
+  } else {
+    // a length beyond max_ctx is flagged by the decode; nothing is written
+    const int L = p.lens[t];
+    if (L <= 0 || L > p.max_ctx) return;
+    const int blk = p.table[t * p.max_blocks + (L - 1) / pool.bs];
+    slot = blk < 0 ? pool.num_blocks * pool.bs : (int64_t)blk * pool.bs + (L - 1) % pool.bs;
+  }
   if (slot < 0) return;
   if (slot >= pool.num_blocks * pool.bs) {
     if (threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
@@ -225,8 +241,14 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
                           const int64_t* slots, int64_t T, cudaStream_t st) {
+  return launch_step_append(pool, k, v, slots, T, nullptr, nullptr, 0, 0, st);
+}
+
+cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
+                               const int64_t* slots, int64_t T, const int* table, const int* lens,
+                               int max_blocks, int max_ctx, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  AppendParams p{pool, k, v, slots, T};
+  AppendParams p{pool, k, v, slots, T, table, lens, max_blocks, max_ctx};
   dim3 grid(static_cast<unsigned>(T), 2);
   switch (pool.fmt) {
     case FMT_FP16: kvq_append_kernel<FMT_FP16><<<grid, kAppendThreads, 0, st>>>(p); break;

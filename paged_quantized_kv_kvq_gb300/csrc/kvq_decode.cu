@@ -60,7 +60,8 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
   return true;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st,
+                          bool dependent) {
   DecodeLaunch l;
   DecodeParams& p = l.p;
   p.pool = a.pool;
@@ -85,6 +86,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   l.merge_grid = static_cast<unsigned>(plan.merge_grid);
   l.smem = plan.smem_bytes;
   l.st = st;
+  l.dependent = dependent;
   switch (a.pool.fmt) {
     case FMT_INT8_GROUP: return launch_decode_int8_group(l);
     case FMT_FP16: return launch_decode_fp16(l);

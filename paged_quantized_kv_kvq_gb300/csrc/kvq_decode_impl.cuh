@@ -591,6 +591,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     ++n_issued;
   };
+  // Everything above reads only q-side inputs (lengths, block table).  When the
+  // decode is a programmatic dependent of the decode-step append, wait here for
+  // the append to complete before the first page is fetched; otherwise this
+  // returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   {
     const int npre = min(n_w, nstage);
     for (int i = 0; i < npre; ++i) issue_next();
@@ -837,6 +842,7 @@ struct DecodeLaunch {
   unsigned merge_grid;
   int smem;
   cudaStream_t st;
+  bool dependent;  // launch as a programmatic dependent of the previous kernel
 };
 
 constexpr int kMaxDevices = 64;
@@ -853,9 +859,20 @@ cudaError_t run_decode(const DecodeLaunch& l) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  kvq_decode_kernel<FMT, D, NG><<<l.grid, kDecodeThreads, l.smem, l.st>>>(l.p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  {
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = l.grid;
+    dc.blockDim = dim3(kDecodeThreads);
+    dc.dynamicSmemBytes = l.smem;
+    dc.stream = l.st;
+    cudaLaunchAttribute da[1];
+    da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    da[0].val.programmaticStreamSerializationAllowed = 1;
+    dc.attrs = da;
+    dc.numAttrs = l.dependent ? 1 : 0;
+    e = cudaLaunchKernelEx(&dc, kvq_decode_kernel<FMT, D, NG>, l.p);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(l.merge_grid);
   cfg.blockDim = dim3(kMergeThreads);

@@ -12,6 +12,11 @@ namespace kvq {
 
 cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
                           const int64_t* slots, int64_t T, cudaStream_t st);
+// Append with slots from `slots`, or -- when slots is null -- the decode-step
+// form: token t is sequence t's new token, stored at position lens[t]-1.
+cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
+                               const int64_t* slots, int64_t T, const int* table, const int* lens,
+                               int max_blocks, int max_ctx, cudaStream_t st);
 cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,
                              cudaStream_t st);
 cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_t n,
@@ -46,7 +51,10 @@ struct DecodeArgs {
   float sm_scale;
 };
 
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st);
+// `dependent`: launch the decode as a programmatic dependent of the kernel
+// just before it on the stream (the decode-step append).
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st,
+                          bool dependent = false);
 
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;
