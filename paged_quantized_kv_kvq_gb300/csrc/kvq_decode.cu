@@ -20,15 +20,16 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
   constexpr int W = kDecodeWarps;
   const bool tok = pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN;
   const int stage_bytes = round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
-  int nstage_log2 = 2;  // 4 stages per warp at most
-  while (nstage_log2 > 1 && W * (1 << nstage_log2) * stage_bytes > 80 * 1024) --nstage_log2;
-  const int nstage = 1 << nstage_log2;
+  // Pages in flight per SM = CTAs per SM x W x stages; 3 CTAs x 4 warps x 4
+  // stages keeps ~200 KB of copies in flight, above what HBM latency needs.
+  int nstage = kDecodeStages;
+  while (nstage > 2 && W * nstage * stage_bytes > 80 * 1024) --nstage;
   const int smem = round_up(W * nstage * stage_bytes + W * nstage * (8 + 4) + W * 4 + (S + 1) * 4,
                             128);
   if (smem > 227 * 1024) return false;
   const int G = Hq / pool.Hkv;
   const int n_ht = (G + 7) / 8;
-  const int ctas_per_sm = std::max(1, std::min(3, (228 * 1024) / (smem + 1024)));
+  const int ctas_per_sm = std::max(1, std::min(kDecodeCtasPerSm, (228 * 1024) / (smem + 1024)));
   const int64_t units = (int64_t)S * pool.Hkv * n_ht;
   const int64_t max_pages = (std::max(max_ctx, 0) + pool.bs - 1) / pool.bs;
   const int64_t tmax = std::max<int64_t>(units * max_pages, 1);
@@ -46,7 +47,7 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
   plan->grid = static_cast<int>(grid);
   plan->ppw_fixed = ppw_fixed;
   plan->n_ht = n_ht;
-  plan->nstage_log2 = nstage_log2;
+  plan->nstage = nstage;
   plan->stage_bytes = stage_bytes;
   plan->smem_bytes = smem;
   plan->ps_bytes = round_up_sz((size_t)(S + 1) * sizeof(int), 256);
@@ -78,7 +79,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   p.max_blocks = a.max_blocks;
   p.max_ctx = a.max_ctx;
   p.ppw_fixed = plan.ppw_fixed;
-  p.nstage_log2 = plan.nstage_log2;
+  p.nstage = plan.nstage;
   p.stage_bytes = plan.stage_bytes;
   p.grid = plan.grid;
   p.sm_scale_log2 = a.sm_scale * 1.4426950408889634f;

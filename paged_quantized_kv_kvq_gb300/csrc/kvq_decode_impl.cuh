@@ -22,9 +22,10 @@
 //  * Each warp keeps NSTAGE shared-memory stages in flight: lane 0 reads the
 //    block table and issues one bulk (TMA) copy of the (block, kv head) page --
 //    K codes, V codes and group scales are contiguous -- completing on an
-//    mbarrier.  One-byte formats move the page's fragments into registers and
-//    hand the stage back to the copy engine before computing.  Waits are
-//    bounded; a wait that runs out sets an error bit instead of hanging.
+//    mbarrier; a stage goes back to the copy engine once the page's P.V is
+//    done (holding V in shared memory rather than registers keeps the kernel
+//    at 3 CTAs per SM for every format).  Waits are bounded; a wait that runs
+//    out sets an error bit instead of hanging.
 //  * The Q heads of the unit share every loaded page: Q.K^T and P.V run on the
 //    tensor cores as mma.m16n8k16 with the heads on the n dimension, 32 tokens
 //    (two 16-token sub-tiles) per online-softmax update.  Codes are exact in
@@ -46,6 +47,8 @@
 namespace kvq {
 
 constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 4;     // shared-memory stages per warp (at most)
+constexpr int kDecodeCtasPerSm = 3;  // resident CTAs per SM the grid is sized for
 constexpr int kDecodeThreads = kDecodeWarps * 32;
 constexpr int kWaitTries = 4000;   // x 1 ms suspend hint per try: ~4 s upper bound
 constexpr int kPartRows = 8;       // partial rows per (warp, slot): one per Q head of a tile
@@ -61,7 +64,7 @@ struct DecodeParams {
   float* part;         // [warps][2][kPartRows][D + 2]: m, l, O of cut units
   int S, Hq, G, n_ht, max_blocks, max_ctx;
   int ppw_fixed;       // pages per warp; 0 = balance the pages over all warps
-  int nstage_log2;
+  int nstage;          // shared-memory stages per warp (2..4)
   int stage_bytes;
   int grid;            // decode CTAs (the merge kernel derives the warp ranges from it)
   float sm_scale_log2;  // sm_scale * log2(e)
@@ -105,8 +108,6 @@ struct FmtTraits {
   static constexpr bool row_scales = group_scales || token_scales;  // per-(token[,group]) K/V scales
   static constexpr bool channel = FMT == FMT_INT8_CHANNEL;
   static constexpr bool maybe_nan = FMT == FMT_FP16 || FMT == FMT_FP8_TOKEN;
-  // One-byte pages move to registers before compute, freeing the stage early.
-  static constexpr bool early_release = one_byte;
 };
 
 // Word w (4 elements) of a lane's sub-tile -> (lo, hi) fp16x2 pairs.
@@ -143,18 +144,18 @@ struct Cursor {
 };
 
 // Everything one online-softmax update needs from two 16-token sub-tiles,
-// held in registers: K (and, for one-byte formats, V) fragment words, the
-// scales of the two rows this lane owns (tokens g and g+8), the valid rows.
+// held in registers: K fragment words, the scales of the two rows this lane
+// owns (tokens g and g+8), where the V codes sit in shared memory, the valid
+// rows.
 template <int FMT, int D, int NG>
 struct PairRegs {
   using T = FmtTraits<FMT>;
   static constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;
   static constexpr int NS = T::group_scales ? NG : 1;
   uint32_t kw[2][NU32];
-  uint32_t vw[2][T::early_release ? NU32 : 1];
   float ks[2][2][NS];  // [tile][row g | g+8][group]
   float vs[2][2][NS];
-  const char* vtile[2];  // V codes in shared memory (formats that keep the stage)
+  const char* vtile[2];  // V codes in shared memory
   int rows[2];
 };
 
@@ -167,7 +168,6 @@ __device__ __forceinline__ void load_tile(PairRegs<FMT, D, NG>& r, int t, const 
   const int g = lane >> 2;
   load_lane_words<FMT, D>(stage + sub * pool.sub_bytes, lane, r.kw[t]);
   r.vtile[t] = stage + pool.code_bytes + sub * pool.sub_bytes;
-  if constexpr (T::early_release) load_lane_words<FMT, D>(r.vtile[t], lane, r.vw[t]);
   if constexpr (T::row_scales) {
     const float* ks;
     const float* vs;
@@ -336,17 +336,9 @@ __device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
     }
   }
   {
-    uint32_t vwl[2][T::early_release ? 1 : NU32];
-    uint32_t* vwp[2];
+    uint32_t vwp[2][NU32];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      if constexpr (T::early_release) {
-        vwp[t] = r.vw[t];
-      } else {
-        load_lane_words<FMT, D>(r.vtile[t], lane, vwl[t]);
-        vwp[t] = vwl[t];
-      }
-    }
+    for (int t = 0; t < 2; ++t) load_lane_words<FMT, D>(r.vtile[t], lane, vwp[t]);
     if constexpr (T::maybe_nan) {
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -441,7 +433,7 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, int 
 }
 
 template <int FMT, int D, int NG>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     kvq_decode_kernel(const DecodeParams p) {
   using T = FmtTraits<FMT>;
   constexpr int KS = D / 16;
@@ -452,7 +444,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   const int g = lane >> 2, j = lane & 3;
   const PoolView& pool = p.pool;
   const int bs = pool.bs;
-  const int nstage = 1 << p.nstage_log2;
+  const int nstage = p.nstage;
   const int U = pool.Hkv * p.n_ht;  // units per sequence
 
   char* stages = smem + warp * nstage * p.stage_bytes;
@@ -559,8 +551,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
   int tcur = table_entry(lane), tnext = table_entry(32 + lane);
   Cursor ic = locate(a0);  // next page to issue (lane 0 tracks it)
   int n_issued = 0;
+  int pst = 0;  // stage of the next issue (n_issued mod nstage)
   auto issue_one = [&](int phys) {  // lane 0 only: page at the issue cursor
-    const int st = n_issued & (nstage - 1);
+    const int st = pst;
     char* dst = stages + st * p.stage_bytes;
     const bool ok = phys >= 0 && (int64_t)phys < pool.num_blocks;
     stage_phys[st] = ok ? phys : -1;
@@ -590,6 +583,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
       advance(ic);
     }
     ++n_issued;
+    if (++pst == nstage) pst = 0;
   };
   // Everything above reads only q-side inputs (lengths, block table).  When the
   // decode is a programmatic dependent of the decode-step append, wait here for
@@ -601,9 +595,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
     for (int i = 0; i < npre; ++i) issue_next();
   }
 
-  auto wait_stage = [&](int i) -> bool {
-    const int st = i & (nstage - 1);
-    const uint32_t parity = (i >> p.nstage_log2) & 1;
+  // Consumer position: page i sits in stage cst; cph is the parity of that
+  // stage's current fill.
+  int cst = 0;
+  uint32_t cph = 0;
+  auto wait_stage = [&](int st, uint32_t parity) -> bool {
     bool ok = false;
     for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(&bars[st], parity);
     if (!__all_sync(0xffffffffu, ok)) {
@@ -693,54 +689,42 @@ __global__ void __launch_bounds__(kDecodeThreads)
     // or one page of two or more sub-tiles
     const bool two = bs == 16 && i + 1 < n_w && cc.pi + 1 < cc.Ps;
     const int npg = two ? 2 : 1;
-    if (!wait_stage(i) || (two && !wait_stage(i + 1))) break;
+    const bool wrap1 = cst + 1 == nstage;
+    const int st0 = cst, st1 = wrap1 ? 0 : cst + 1;
+    if (!wait_stage(st0, cph) || (two && !wait_stage(st1, wrap1 ? cph ^ 1u : cph))) break;
     auto issue_after = [&]() {
       for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
     };
     if (two) {
-      const int st0 = i & (nstage - 1), st1 = (i + 1) & (nstage - 1);
       const int r0 = stage_phys[st0] >= 0 ? min(16, L - cc.pi * 16) : 0;
       const int r1 = stage_phys[st1] >= 0 ? min(16, L - (cc.pi + 1) * 16) : 0;
       // an absent page (rows = 0) contributes nothing; keep the valid one in tile 0
       const int sA = r0 > 0 ? st0 : st1;
       load_tile<FMT, D, NG>(R, 0, stages + sA * p.stage_bytes, 0, r0 > 0 ? r0 : r1, pool, lane);
       load_tile<FMT, D, NG>(R, 1, stages + st1 * p.stage_bytes, 0, r0 > 0 ? r1 : 0, pool, lane);
-      if constexpr (T::early_release) {
-        __syncwarp();
-        issue_after();
-      }
       compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
     } else {
-      const int st = i & (nstage - 1);
-      const char* stage = stages + st * p.stage_bytes;
-      const int nvalid = stage_phys[st] >= 0 ? min(bs, L - cc.pi * bs) : 0;
+      const char* stage = stages + st0 * p.stage_bytes;
+      const int nvalid = stage_phys[st0] >= 0 ? min(bs, L - cc.pi * bs) : 0;
       const int nsub = (nvalid + 15) >> 4;
-      if (nsub == 0) {
-        if constexpr (T::early_release) {
-          __syncwarp();
-          issue_after();
-        }
-      }
       for (int sp = 0; sp < nsub; sp += 2) {
         const int rA = min(16, nvalid - sp * 16);
         const int rB = sp + 1 < nsub ? min(16, nvalid - (sp + 1) * 16) : 0;
         load_tile<FMT, D, NG>(R, 0, stage, sp, rA, pool, lane);
         load_tile<FMT, D, NG>(R, 1, stage, sp + 1 < nsub ? sp + 1 : sp, rB, pool, lane);
-        if constexpr (T::early_release) {
-          if (sp + 2 >= nsub) {
-            __syncwarp();
-            issue_after();
-          }
-        }
         compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
       }
     }
-    if constexpr (!T::early_release) {
-      __syncwarp();
-      issue_after();
-    }
+    // every lane is done with the stage(s): hand them back to the copy engine
+    __syncwarp();
+    issue_after();
     // advance the consumer; close the unit at its last page or at the range end
     i += npg;
+    for (int k = 0; k < npg; ++k)
+      if (++cst == nstage) {
+        cst = 0;
+        cph ^= 1u;
+      }
     const Cursor done = cc;
     const int end_pi = cc.pi + npg;
     for (int k = 0; k < npg; ++k) advance(cc);

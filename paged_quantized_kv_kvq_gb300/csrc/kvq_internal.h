@@ -27,7 +27,7 @@ struct DecodePlan {
   int grid = 0;         // persistent CTAs
   int ppw_fixed = 0;    // pages per warp when forced; 0 = balanced
   int n_ht = 0;         // head tiles of 8 Q heads per kv head
-  int nstage_log2 = 0;  // pipeline stages per warp = 1 << nstage_log2
+  int nstage = 0;  // pipeline stages per warp
   int stage_bytes = 0;  // bytes of one stage
   int smem_bytes = 0;   // dynamic shared memory per CTA
   int merge_grid = 0;   // CTAs of the merge kernel
