@@ -297,7 +297,7 @@ kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half
   cudaError_t e = kvq::launch_step_append(pool->view, reinterpret_cast<const __half*>(k_new),
                                           reinterpret_cast<const __half*>(v_new), nullptr, num_seqs,
                                           block_table, context_lens, max_blocks_per_seq,
-                                          max_context_len, stream);
+                                          max_context_len, stream, /*dependent=*/true);
   if (e != cudaSuccess) return from_cuda(e);
   return from_cuda(kvq::launch_decode(a, plan, stream, /*dependent=*/true));
 }

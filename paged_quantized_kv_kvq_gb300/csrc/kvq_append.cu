@@ -62,9 +62,12 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
   const PoolView& pool = p.pool;
   const int64_t t = blockIdx.x;
   const int kv = blockIdx.y;
-  // a decode that depends on this append may launch now: it only reads the
-  // pool after waiting for this grid to complete
+  // A decode that depends on this append may launch now: it only reads the
+  // pool after waiting for this grid to complete.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Launched as a programmatic dependent (decode step), wait for the previous
+  // kernel's completion before reading anything; otherwise returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int64_t slot;
   if (p.slots != nullptr) {
     slot = p.slots[t];
@@ -241,24 +244,42 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
                           const int64_t* slots, int64_t T, cudaStream_t st) {
-  return launch_step_append(pool, k, v, slots, T, nullptr, nullptr, 0, 0, st);
+  return launch_step_append(pool, k, v, slots, T, nullptr, nullptr, 0, 0, st, false);
 }
+
+namespace {
+
+template <int FMT>
+cudaError_t launch_append_fmt(const AppendParams& p, dim3 grid, cudaStream_t st, bool dependent) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAppendThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kvq_append_kernel<FMT>, p);
+}
+
+}  // namespace
 
 cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
                                const int64_t* slots, int64_t T, const int* table, const int* lens,
-                               int max_blocks, int max_ctx, cudaStream_t st) {
+                               int max_blocks, int max_ctx, cudaStream_t st, bool dependent) {
   if (T == 0) return cudaSuccess;
   AppendParams p{pool, k, v, slots, T, table, lens, max_blocks, max_ctx};
   dim3 grid(static_cast<unsigned>(T), 2);
   switch (pool.fmt) {
-    case FMT_FP16: kvq_append_kernel<FMT_FP16><<<grid, kAppendThreads, 0, st>>>(p); break;
-    case FMT_INT8_TOKEN: kvq_append_kernel<FMT_INT8_TOKEN><<<grid, kAppendThreads, 0, st>>>(p); break;
-    case FMT_INT8_CHANNEL: kvq_append_kernel<FMT_INT8_CHANNEL><<<grid, kAppendThreads, 0, st>>>(p); break;
-    case FMT_INT8_GROUP: kvq_append_kernel<FMT_INT8_GROUP><<<grid, kAppendThreads, 0, st>>>(p); break;
-    case FMT_FP8_TOKEN: kvq_append_kernel<FMT_FP8_TOKEN><<<grid, kAppendThreads, 0, st>>>(p); break;
+    case FMT_FP16: return launch_append_fmt<FMT_FP16>(p, grid, st, dependent);
+    case FMT_INT8_TOKEN: return launch_append_fmt<FMT_INT8_TOKEN>(p, grid, st, dependent);
+    case FMT_INT8_CHANNEL: return launch_append_fmt<FMT_INT8_CHANNEL>(p, grid, st, dependent);
+    case FMT_INT8_GROUP: return launch_append_fmt<FMT_INT8_GROUP>(p, grid, st, dependent);
+    case FMT_FP8_TOKEN: return launch_append_fmt<FMT_FP8_TOKEN>(p, grid, st, dependent);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,

@@ -447,6 +447,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   const int nstage = p.nstage;
   const int U = pool.Hkv * p.n_ht;  // units per sequence
 
+  // The merge grid may launch now: every CTA of this (persistent) grid is
+  // resident once all have passed this point, and the merge reads nothing of
+  // ours before its griddepcontrol.wait returns on this grid's completion.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   char* stages = smem + warp * nstage * p.stage_bytes;
   uint64_t* bars_base = reinterpret_cast<uint64_t*>(smem + kDecodeWarps * nstage * p.stage_bytes);
   uint64_t* bars = bars_base + warp * nstage;
@@ -489,14 +494,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     }
     if (threadIdx.x == 0) PS[0] = 0;
     __syncthreads();
-    if (blockIdx.x == 0)
-      for (int s = threadIdx.x; s <= p.S; s += kDecodeThreads) p.ps[s] = PS[s];
-  }
-  // sequences with nothing to attend get zeros
-  for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
-    if (PS[s + 1] != PS[s]) continue;
-    float* o = p.out + (int64_t)s * p.Hq * D;
-    for (int i = threadIdx.x; i < p.Hq * D; i += kDecodeThreads) o[i] = 0.f;
   }
 
   const int Ttot = PS[p.S];
@@ -506,7 +503,26 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   const int a0 = (int)min((int64_t)gw * ppw, (int64_t)Ttot);
   const int b0 = (int)min((int64_t)a0 + ppw, (int64_t)Ttot);
   const int n_w = b0 - a0;
-  if (n_w <= 0) return;
+
+  // Writes to the output and the workspace come only after
+  // griddepcontrol.wait: when this grid is a programmatic dependent (of the
+  // decode-step append, itself a dependent of whatever ran before), the
+  // previous merge may still be reading them until then.
+  auto after_wait = [&]() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (gw == 0)  // the page prefix, for the merge kernel
+      for (int s = lane; s <= p.S; s += 32) p.ps[s] = PS[s];
+    // sequences with nothing to attend get zeros
+    for (int s = gw; s < p.S; s += nwarps) {
+      if (PS[s + 1] != PS[s]) continue;
+      float* o = p.out + (int64_t)s * p.Hq * D;
+      for (int i = lane; i < p.Hq * D; i += 32) o[i] = 0.f;
+    }
+  };
+  if (n_w <= 0) {
+    after_wait();
+    return;
+  }
 
   auto locate = [&](int x) -> Cursor {
     int lo = 0, hi = p.S;  // PS[lo] <= x < PS[hi]
@@ -585,11 +601,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     ++n_issued;
     if (++pst == nstage) pst = 0;
   };
-  // Everything above reads only q-side inputs (lengths, block table).  When the
+  // Everything above reads only inputs (lengths, block table).  When the
   // decode is a programmatic dependent of the decode-step append, wait here for
   // the append to complete before the first page is fetched; otherwise this
   // returns at once.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  after_wait();
   {
     const int npre = min(n_w, nstage);
     for (int i = 0; i < npre; ++i) issue_next();
@@ -658,25 +674,34 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
       }
       return;
     }
-    // -- partial: rows (m, l, O) in true units
+    // -- partial: rows (m, l, O) in true units, for the tile's valid heads
     const int slot = (u.s == first.s && u.lu == first.lu) ? 0 : 1;
     float* base = p.part + ((int64_t)gw * 2 + slot) * kPartRows * (D + 2);
+    const bool v0 = 2 * j < Gt, v1 = 2 * j + 1 < Gt;
+    float* r0 = base + (2 * j) * (D + 2);
+    float* r1 = base + (2 * j + 1) * (D + 2);
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       const int d0 = 16 * mt + g;
       const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
-      float* r0 = base + (2 * j) * (D + 2) + 2;
-      float* r1 = base + (2 * j + 1) * (D + 2) + 2;
-      r0[d0] = o[mt][0] * inv2E * c0;
-      r0[d0 + 8] = o[mt][2] * inv2E * c8;
-      r1[d0] = o[mt][1] * inv2E * c0;
-      r1[d0 + 8] = o[mt][3] * inv2E * c8;
+      if (v0) {
+        r0[2 + d0] = o[mt][0] * inv2E * c0;
+        r0[2 + d0 + 8] = o[mt][2] * inv2E * c8;
+      }
+      if (v1) {
+        r1[2 + d0] = o[mt][1] * inv2E * c0;
+        r1[2 + d0 + 8] = o[mt][3] * inv2E * c8;
+      }
     }
     if (g == 0) {
-      base[(2 * j) * (D + 2) + 0] = m[0];
-      base[(2 * j) * (D + 2) + 1] = lt0;
-      base[(2 * j + 1) * (D + 2) + 0] = m[1];
-      base[(2 * j + 1) * (D + 2) + 1] = lt1;
+      if (v0) {
+        r0[0] = m[0];
+        r0[1] = lt0;
+      }
+      if (v1) {
+        r1[0] = m[1];
+        r1[1] = lt1;
+      }
     }
   };
 
@@ -733,9 +758,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
       if (i < n_w) start_unit();
     }
   }
-  // Let the merge grid launch; it still waits for this grid's completion (and
-  // memory) before reading any partial.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Log-sum-exp merge of the units that the decode kernel's warp ranges cut:
@@ -745,6 +767,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
 // grid has completed and its writes are visible.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodeParams p) {
+  // A kernel launched after this one as a programmatic dependent (the next
+  // decode-step append) may launch now; it waits for this grid's completion
+  // before touching anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const float kNegInf = __int_as_float(0xff800000u);
   constexpr int NW = kMergeThreads / 32;

@@ -14,9 +14,11 @@ cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v
                           const int64_t* slots, int64_t T, cudaStream_t st);
 // Append with slots from `slots`, or -- when slots is null -- the decode-step
 // form: token t is sequence t's new token, stored at position lens[t]-1.
+// `dependent`: launch as a programmatic dependent of the previous kernel (the
+// kernel waits for its completion before reading anything).
 cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
                                const int64_t* slots, int64_t T, const int* table, const int* lens,
-                               int max_blocks, int max_ctx, cudaStream_t st);
+                               int max_blocks, int max_ctx, cudaStream_t st, bool dependent);
 cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,
                              cudaStream_t st);
 cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_t n,
