@@ -65,14 +65,24 @@ def layer_bytes(w, fmt, group, seqs=None):
     app_scales = {3: n * w.Hkv * 2 * (w.D // max(group, 1)) * 4, 1: n * 2 * 4, 4: n * 2 * 4}.get(fmt, 0)
     append = n * w.Hkv * w.D * 2 * 2 + n * 8 + n * w.Hkv * w.D * 2 * es + app_scales
     unique_codes = codes
-    if w.shared_prefix_tokens:
-        unique_codes -= (n - 1) * w.shared_prefix_tokens * w.Hkv * w.D * 2 * es
+    unique_decode = decode
+    if w.shared_prefix_tokens and n > 1:
+        # the shared prefix blocks exist once in HBM
+        dup = (n - 1) * w.shared_prefix_tokens
+        unique_codes -= dup * w.Hkv * w.D * 2 * es
+        unique_decode -= dup * w.Hkv * w.D * 2 * es
+        if fmt == 3:
+            unique_decode -= dup * w.Hkv * 2 * (w.D // group) * 4
+        elif fmt in (1, 4):
+            unique_decode -= dup * 2 * 4
     return {"decode": decode, "append": append, "codes": codes, "scales": scales,
-            "unique_codes": unique_codes, "output": n * w.Hq * w.D * 4}
+            "unique_codes": unique_codes, "unique_decode": unique_decode,
+            "output": n * w.Hq * w.D * 4}
 
 
 def step_bytes(w):
-    tot = {"decode": 0, "append": 0, "codes": 0, "scales": 0, "unique_codes": 0, "output": 0}
+    tot = {"decode": 0, "append": 0, "codes": 0, "scales": 0, "unique_codes": 0,
+           "unique_decode": 0, "output": 0}
     for fmt, group in w.layer_formats:
         for k, v in layer_bytes(w, fmt, group).items():
             tot[k] += v
@@ -289,25 +299,47 @@ def run_ours(args, rank, world, local_rank):
     lens = torch.from_numpy(w.context_lens).to(dev)
     max_ctx = int(w.context_lens.max())
     out = torch.empty((L, w.S, w.Hq, w.D), dtype=torch.float32, device=dev)
-    ws_need = max(kvq.kvq_decode_workspace_bytes(p.handle, w.S, w.Hq, max_ctx) for p in pools)
+    # The shared-prefix cascade reads the prefix once per kv head for all
+    # sequences.  The repeated prefix reads of the plain decode hit the 129 MB
+    # L2 and overlap the HBM-bound rest, so the cascade pays only when the
+    # prefix is at least as long as the average suffix ("auto").
+    P = 0
+    if w.shared_prefix_tokens:
+        mean_suffix = float(np.mean(w.context_lens)) - w.shared_prefix_tokens
+        use = {"on": True, "off": False}.get(args.cascade, w.shared_prefix_tokens >= mean_suffix)
+        P = w.shared_prefix_tokens // w.bs if use else 0
+    if P:
+        ws_need = max(kvq.kvq_cascade_workspace_bytes(p.handle, w.S, w.Hq, max_ctx) for p in pools)
+    else:
+        ws_need = max(kvq.kvq_decode_workspace_bytes(p.handle, w.S, w.Hq, max_ctx) for p in pools)
     ws = torch.empty(max(ws_need, 256), dtype=torch.uint8, device=dev)
     sm_scale = w.D ** -0.5
 
     fused = args.step_api == "fused"
 
+    def decode_call(l, qq, ln, oo):
+        if P:
+            kvq.kvq_cascade_decode(pools[l].handle, qq[l], table, ln, max_ctx, P, sm_scale, oo[l],
+                                   ws, stream)
+        else:
+            kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l], ws,
+                                 0, stream)
+
     # No events between layers inside a step: an event record between two
     # kernels ends the programmatic-dependent overlap of the launches.
     def step(qq, kk, vv, sl, ln, oo):
         for l in range(L):
-            if fused:
+            if fused and P:
+                kvq.kvq_cascade_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln,
+                                            max_ctx, P, sm_scale, oo[l], ws, stream)
+            elif fused:
                 # one call: append at position L-1 (slot from the block table),
                 # then the decode as a programmatic dependent of the append
                 kvq.kvq_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln, max_ctx,
                                     sm_scale, oo[l], ws, stream)
             else:
                 pools[l].append(kk[l], vv[l], sl, stream)
-                kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l],
-                                     ws, 0, stream)
+                decode_call(l, qq, ln, oo)
 
     for _ in range(args.warmup):
         step(q, kn, vn, slots, lens, out)
@@ -347,8 +379,7 @@ def run_ours(args, rank, world, local_rank):
         for l in range(L):
             ev = evs[i * L + l]
             ev[0].record(stream)
-            kvq.kvq_paged_decode(pools[l].handle, q[l], table, lens, max_ctx, sm_scale, out[l],
-                                 ws, 0, stream)
+            decode_call(l, q, lens, out)
             ev[1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -405,8 +436,9 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
     dec_avg_ms = float(np.mean(dec_ms))
-    # algorithmic bytes of each layer's call (formats may differ by layer)
-    lbytes = [layer_bytes(w, f, g)["decode"] for f, g in w.layer_formats]
+    # algorithmic HBM bytes of each layer's call (formats may differ by layer;
+    # with the cascade the shared prefix is read once)
+    lbytes = [layer_bytes(w, f, g)["unique_decode" if P else "decode"] for f, g in w.layer_formats]
     per_launch = float(np.mean(lbytes))
     achieved = per_launch / (dec_avg_ms * 1e-3) / 1e9
     # launches: per layer one append, one decode and one split merge
@@ -426,16 +458,22 @@ def run_ours(args, rank, world, local_rank):
             "pool_blocks_per_layer": w.num_blocks,
             "l2": "inputs larger than L2: %d per-layer pools, %.1f GB"
                   % (L, sum(p.buffer.numel() for p in pools) / 1e9),
-            "step": ("per layer: kvq_decode_step (append 1 token/seq at L-1, then decode)"
-                     if fused else "per layer: kvq_append (1 token/seq) then kvq_paged_decode"),
+            "step": ("per layer: kvq_%sdecode_step (append 1 token/seq at L-1, then decode)"
+                     % ("cascade_" if P else "") if fused else
+                     "per layer: kvq_append (1 token/seq) then kvq_%s"
+                     % ("cascade_decode" if P else "paged_decode")),
+            "shared_prefix_blocks_read_once": P,
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "decode_tok_per_s": round(world * w.S / (ms * 1e-3), 1),
         "bytes_per_step": b,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": read_traffic(w.name),
-                     "kernel": "kvq_paged_decode call (decode kernel + dependent split merge), "
-                               "every layer's, %d calls timed one by one after the step region"
+                     "kernel": ("kvq_cascade_decode call (prefix kernel, decode kernel and split "
+                                "merge, each a programmatic dependent of the one before; bytes "
+                                "count the shared prefix once)" if P else
+                                "kvq_paged_decode call (decode kernel + dependent split merge)")
+                               + ", every layer's, %d calls timed one by one after the step region"
                                % (KR * L),
                      "bytes_per_launch": round(per_launch), "avg_launch_ms": round(dec_avg_ms, 5),
                      "peak_source": "%s hbm_gbs" % peak_kind},
@@ -495,6 +533,9 @@ def main():
     ap.add_argument("--workload", default="gqa_64x2048")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cascade", default="auto", choices=["auto", "on", "off"],
+                    help="shared-prefix workloads: attend the prefix once for all sequences "
+                         "(auto: when the prefix is at least the mean suffix length)")
     ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
                     help="fused: one kvq_decode_step call per layer; separate: kvq_append "
                          "then kvq_paged_decode")

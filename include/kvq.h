@@ -202,6 +202,39 @@ kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half
                            const int32_t* context_lens, int max_context_len, float sm_scale,
                            float* out, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Shared-prefix ("cascade") decode ([KVC] §2.2: requests with a common prefix
+ * share its physical blocks; [P402] §三: a shared system prompt): the first
+ * prefix_blocks blocks of every sequence are the same physical blocks, those
+ * of block_table row 0.  They are read once per kv head for all sequences'
+ * Q heads (a partial softmax per (sequence, Q head)), the remaining blocks by
+ * the paged decode, and the two parts are combined by log-sum-exp.
+ *   prefix_blocks : 0 <= prefix_blocks <= max_blocks_per_seq; 0 is plain
+ *                   kvq_paged_decode
+ *   workspace     : >= kvq_cascade_workspace_bytes(..) bytes, 256-byte aligned
+ *   the other arguments and the result are those of kvq_paged_decode.
+ * Precondition (not checked): block_table[s][j] == block_table[0][j] for
+ * every j < prefix_blocks and every s whose context reaches block j.
+ * Sequences shorter than the prefix are handled (their rows stop at their own
+ * length).  Results equal kvq_paged_decode's up to fp32 rounding order. */
+size_t kvq_cascade_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,
+                                   int max_context_len);
+kvq_status kvq_cascade_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                              int num_q_heads, const int32_t* block_table,
+                              int max_blocks_per_seq, const int32_t* context_lens,
+                              int max_context_len, int prefix_blocks, float sm_scale,
+                              float* out, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/* kvq_decode_step with the cascade decode: the new token of sequence s goes to
+ * position context_lens[s]-1, which must lie past the shared prefix (a token
+ * written into a shared block would change every sequence's prefix). */
+kvq_status kvq_cascade_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
+                                   const kvq_half* q, int num_seqs, int num_q_heads,
+                                   const int32_t* block_table, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int max_context_len,
+                                   int prefix_blocks, float sm_scale, float* out,
+                                   void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Maximum split-K scratch of kvq_paged_decode_noalloc, in bytes (16 MiB). */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 

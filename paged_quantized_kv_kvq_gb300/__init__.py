@@ -92,6 +92,10 @@ def _declare(L):
         "kvq_paged_decode_ex": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, i32, P]),
         "kvq_paged_decode_noalloc": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, i32, P]),
         "kvq_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
+        "kvq_cascade_workspace_bytes": (sz, [P, i32, i32, i32]),
+        "kvq_cascade_decode": (i32, [P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz, P]),
+        "kvq_cascade_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz,
+                                          P]),
         "kvq_read_slots": (i32, [P, P, i64, P, P, P]),
         "kvq_get_error": (i32, [P, P]),
         "kvq_status_string": (ctypes.c_char_p, [i32]),
@@ -222,6 +226,44 @@ def kvq_decode_step(pool, k_new, v_new, q, block_table, context_lens, max_contex
         _stream(stream)), "kvq_decode_step")
 
 
+def kvq_cascade_workspace_bytes(pool, num_seqs, num_q_heads, max_context_len) -> int:
+    return int(lib().kvq_cascade_workspace_bytes(pool, num_seqs, num_q_heads, max_context_len))
+
+
+def kvq_cascade_decode(pool, q, block_table, context_lens, max_context_len, prefix_blocks,
+                       sm_scale, out, workspace, stream=None) -> None:
+    """Decode whose first prefix_blocks blocks (shared by every sequence) are
+    attended once for all sequences (kvq_cascade_decode in include/kvq.h)."""
+    import torch
+
+    S, Hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().kvq_cascade_decode(
+        pool, _ptr(q, torch.float16, "q"), S, Hq, _ptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len),
+        int(prefix_blocks), float(sm_scale), _ptr(out, torch.float32, "out"),
+        _ptr(workspace, None, "workspace") if workspace is not None else None, ws_bytes,
+        _stream(stream)), "kvq_cascade_decode")
+
+
+def kvq_cascade_decode_step(pool, k_new, v_new, q, block_table, context_lens, max_context_len,
+                            prefix_blocks, sm_scale, out, workspace, stream=None) -> None:
+    """kvq_decode_step with the shared-prefix cascade decode."""
+    import torch
+
+    S, Hq, _ = q.shape
+    if k_new.shape != v_new.shape or k_new.shape[0] != S:
+        raise ValueError("k_new, v_new must be [num_seqs, kv_heads, head_dim]")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().kvq_cascade_decode_step(
+        pool, _ptr(k_new, torch.float16, "k_new"), _ptr(v_new, torch.float16, "v_new"),
+        _ptr(q, torch.float16, "q"), S, Hq, _ptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len),
+        int(prefix_blocks), float(sm_scale), _ptr(out, torch.float32, "out"),
+        _ptr(workspace, None, "workspace") if workspace is not None else None, ws_bytes,
+        _stream(stream)), "kvq_cascade_decode_step")
+
+
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -318,6 +360,21 @@ class KVPool:
         ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=q.device) if nws else None
         kvq_decode_step(self.handle, k_new, v_new, q, block_table, context_lens, max_context_len,
                         sm_scale, out, ws, stream)
+        return out
+
+    def cascade_decode(self, q, block_table, context_lens, max_context_len, prefix_blocks,
+                       sm_scale=None, out=None, stream=None):
+        import torch
+
+        S, Hq, D = q.shape
+        if sm_scale is None:
+            sm_scale = D ** -0.5
+        if out is None:
+            out = torch.empty((S, Hq, D), dtype=torch.float32, device=q.device)
+        nws = kvq_cascade_workspace_bytes(self.handle, S, Hq, max_context_len)
+        ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+        kvq_cascade_decode(self.handle, q, block_table, context_lens, max_context_len,
+                           prefix_blocks, sm_scale, out, ws, stream)
         return out
 
     def read_slots(self, slots, stream=None):

@@ -302,6 +302,103 @@ kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half
   return from_cuda(kvq::launch_decode(a, plan, stream, /*dependent=*/true));
 }
 
+}  // extern "C"
+
+// Prefix-partial bytes at the start of a cascade workspace.
+static size_t cascade_pre_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads) {
+  const size_t b = (size_t)num_seqs * num_q_heads * (pool->view.D + 2) * sizeof(float);
+  return (b + 255) / 256 * 256;
+}
+
+// Checks, plans and launches of the cascade; k_new/v_new non-null adds the
+// decode-step append in front.
+static kvq_status cascade(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
+                          const kvq_half* q, int num_seqs, int num_q_heads,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* context_lens, int max_context_len, int prefix_blocks,
+                          float sm_scale, float* out, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream) {
+  if (pool == nullptr || prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_q_heads < 1 || num_q_heads % pool->view.Hkv != 0)
+    return KVQ_ERR_INVALID_ARG;
+  const size_t pre_bytes = cascade_pre_bytes(pool, num_seqs, num_q_heads);
+  const bool casc = prefix_blocks > 0;
+  if (casc && (workspace == nullptr || ws_bytes < pre_bytes)) return KVQ_ERR_WORKSPACE;
+  void* dws = casc ? static_cast<char*>(workspace) + pre_bytes : workspace;
+  const size_t dws_bytes = casc ? ws_bytes - pre_bytes : ws_bytes;
+  kvq::DecodeArgs a;
+  kvq::DecodePlan plan;
+  kvq_status st = prepare_decode(pool, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq,
+                                 context_lens, max_context_len, sm_scale, out, dws, dws_bytes, 0,
+                                 &a, &plan);
+  if (st != KVQ_OK || num_seqs == 0) return st;
+  kvq::PrefixPlan pplan;
+  if (casc && !kvq::plan_prefix(pool->view, num_seqs, num_q_heads, prefix_blocks, &pplan))
+    return KVQ_ERR_UNSUPPORTED;
+  const bool step = k_new != nullptr || v_new != nullptr;
+  if (step) {
+    if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+      return KVQ_ERR_INVALID_ARG;
+    cudaError_t e = kvq::launch_step_append(pool->view, reinterpret_cast<const __half*>(k_new),
+                                            reinterpret_cast<const __half*>(v_new), nullptr,
+                                            num_seqs, block_table, context_lens,
+                                            max_blocks_per_seq, max_context_len, stream, true);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (casc) {
+    kvq::PrefixArgs pa;
+    pa.pool = pool->view;
+    pa.q = reinterpret_cast<const __half*>(q);
+    pa.table = block_table;
+    pa.lens = context_lens;
+    pa.pre = static_cast<float*>(workspace);
+    pa.S = num_seqs;
+    pa.Hq = num_q_heads;
+    pa.max_ctx = max_context_len;
+    pa.P = prefix_blocks;
+    pa.sm_scale = sm_scale;
+    cudaError_t e = kvq::launch_prefix(pa, pplan, stream, step);
+    if (e != cudaSuccess) return from_cuda(e);
+    a.skip = prefix_blocks;
+    a.pre = pa.pre;
+  }
+  return from_cuda(kvq::launch_decode(a, plan, stream, step || casc));
+}
+
+extern "C" {
+
+size_t kvq_cascade_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,
+                                   int max_context_len) {
+  if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || num_q_heads % pool->view.Hkv != 0)
+    return 0;
+  return cascade_pre_bytes(pool, num_seqs, num_q_heads) +
+         kvq_decode_workspace_bytes_ex(pool, num_seqs, num_q_heads, max_context_len, 0);
+}
+
+kvq_status kvq_cascade_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                              int num_q_heads, const int32_t* block_table, int max_blocks_per_seq,
+                              const int32_t* context_lens, int max_context_len,
+                              int prefix_blocks, float sm_scale, float* out, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream) {
+  return cascade(const_cast<kvq_pool*>(pool), nullptr, nullptr, q, num_seqs, num_q_heads,
+                 block_table, max_blocks_per_seq, context_lens, max_context_len, prefix_blocks,
+                 sm_scale, out, workspace, ws_bytes, stream);
+}
+
+kvq_status kvq_cascade_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
+                                   const kvq_half* q, int num_seqs, int num_q_heads,
+                                   const int32_t* block_table, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int max_context_len,
+                                   int prefix_blocks, float sm_scale, float* out, void* workspace,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;
+  return cascade(pool, k_new, v_new, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq,
+                 context_lens, max_context_len, prefix_blocks, sm_scale, out, workspace, ws_bytes,
+                 stream);
+}
+
 kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
                             const int32_t* block_table, int max_blocks_per_seq,
                             const int32_t* context_lens, int max_context_len, float sm_scale,

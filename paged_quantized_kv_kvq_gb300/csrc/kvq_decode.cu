@@ -83,6 +83,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   p.stage_bytes = plan.stage_bytes;
   p.grid = plan.grid;
   p.sm_scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.skip = a.skip;
+  p.pre = a.pre;
   l.grid = dim3(static_cast<unsigned>(plan.grid));
   l.merge_grid = static_cast<unsigned>(plan.merge_grid);
   l.smem = plan.smem_bytes;

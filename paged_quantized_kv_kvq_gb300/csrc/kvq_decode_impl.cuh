@@ -62,6 +62,12 @@ struct DecodeParams {
   float* out;          // [S][Hq][D]
   int* ps;             // [S + 1] page prefix over sequences (written by CTA 0 for the merge)
   float* part;         // [warps][2][kPartRows][D + 2]: m, l, O of cut units
+  // Shared-prefix cascade: the first `skip` blocks of every sequence are the
+  // shared prefix, already attended by the prefix kernel, whose partial rows
+  // (m, l, O in true units) are in pre[S][Hq][D + 2]; skip = 0, pre = null
+  // otherwise.
+  const float* pre;
+  int skip;
   int S, Hq, G, n_ht, max_blocks, max_ctx;
   int ppw_fixed;       // pages per warp; 0 = balance the pages over all warps
   int nstage;          // shared-memory stages per warp (2..4)
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
           if (blockIdx.x == 0) set_error(pool.err, ERR_RANGE);
           L = p.max_ctx;
         }
-        v = L > 0 ? (L + bs - 1) / bs * U : 0;
+        v = L > 0 ? max((L + bs - 1) / bs - p.skip, 0) * U : 0;
       }
       int x = v;
 #pragma unroll
@@ -512,11 +518,21 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (gw == 0)  // the page prefix, for the merge kernel
       for (int s = lane; s <= p.S; s += 32) p.ps[s] = PS[s];
-    // sequences with nothing to attend get zeros
+    // sequences with nothing (left) to attend get zeros, or in the cascade
+    // the normalised prefix result
     for (int s = gw; s < p.S; s += nwarps) {
       if (PS[s + 1] != PS[s]) continue;
       float* o = p.out + (int64_t)s * p.Hq * D;
-      for (int i = lane; i < p.Hq * D; i += 32) o[i] = 0.f;
+      if (p.pre == nullptr) {
+        for (int i = lane; i < p.Hq * D; i += 32) o[i] = 0.f;
+      } else {
+        for (int hq = 0; hq < p.Hq; ++hq) {
+          const float* pr = p.pre + ((int64_t)s * p.Hq + hq) * (D + 2);
+          const float lp = pr[1];
+          const float f = lp > 0.f ? 1.f / lp : 0.f;
+          for (int d = lane; d < D; d += 32) o[(int64_t)hq * D + d] = pr[2 + d] * f;
+        }
+      }
     }
   };
   if (n_w <= 0) {
@@ -561,7 +577,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   auto table_entry = [&](int n) -> int {  // page n of this warp's range
     if (n >= n_w) return -1;
     const Cursor c = locate(a0 + n);
-    return p.table[(int64_t)c.s * p.max_blocks + c.pi];
+    return p.table[(int64_t)c.s * p.max_blocks + p.skip + c.pi];
   };
   int tbase = 0;
   int tcur = table_entry(lane), tnext = table_entry(32 + lane);
@@ -636,7 +652,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   int seg_pi0 = cc.pi;        // first page of the current unit in this range
   int L = 0;                  // context length of the current unit's sequence
   auto start_unit = [&]() {
-    L = min(p.lens[cc.s], p.max_ctx);
+    L = min(p.lens[cc.s], p.max_ctx) - p.skip * bs;  // tokens after the skipped prefix
     load_q<FMT, D>(p, cc.s, cc.lu / p.n_ht, cc.lu % p.n_ht, lane, qb, ql, csc);
     m[0] = m[1] = kNegInf;
     l[0] = l[1] = 0.f;
@@ -656,20 +672,45 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     const float* vch = T::channel ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
     const int64_t row0 = (int64_t)u.s * p.Hq + h * p.G + 8 * ht;
     if (seg_pi0 == 0 && seg_end == u.Ps) {
-      const float f0 = lt0 > 0.f ? inv2E / lt0 : 0.f, f1 = lt1 > 0.f ? inv2E / lt1 : 0.f;
+      if (p.pre == nullptr) {
+        const float f0 = lt0 > 0.f ? inv2E / lt0 : 0.f, f1 = lt1 > 0.f ? inv2E / lt1 : 0.f;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        const int d0 = 16 * mt + g;
-        const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
-        if (2 * j < Gt) {
-          float* dst = p.out + (row0 + 2 * j) * D;
-          dst[d0] = o[mt][0] * f0 * c0;
-          dst[d0 + 8] = o[mt][2] * f0 * c8;
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d0 = 16 * mt + g;
+          const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
+          if (2 * j < Gt) {
+            float* dst = p.out + (row0 + 2 * j) * D;
+            dst[d0] = o[mt][0] * f0 * c0;
+            dst[d0 + 8] = o[mt][2] * f0 * c8;
+          }
+          if (2 * j + 1 < Gt) {
+            float* dst = p.out + (row0 + 2 * j + 1) * D;
+            dst[d0] = o[mt][1] * f1 * c0;
+            dst[d0 + 8] = o[mt][3] * f1 * c8;
+          }
         }
-        if (2 * j + 1 < Gt) {
-          float* dst = p.out + (row0 + 2 * j + 1) * D;
-          dst[d0] = o[mt][1] * f1 * c0;
-          dst[d0 + 8] = o[mt][3] * f1 * c8;
+        return;
+      }
+      // cascade: log-sum-exp with the row's prefix partial
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (2 * j + c >= Gt) continue;
+        const float* pr = p.pre + (row0 + 2 * j + c) * (D + 2);
+        const float mp = pr[0], lp = pr[1];
+        const float mu = m[c], lu = c ? lt1 : lt0;
+        const float M = fmaxf(mu, mp);
+        const float wu = mu == kNegInf ? 0.f : fast_exp2(mu - M);
+        const float wp = mp == kNegInf ? 0.f : fast_exp2(mp - M);
+        const float den = fmaf(lu, wu, lp * wp);
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const float fu = wu * inv2E * inv, fp = wp * inv;
+        float* dst = p.out + (row0 + 2 * j + c) * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d0 = 16 * mt + g;
+          const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
+          dst[d0] = fmaf(o[mt][c] * c0, fu, pr[2 + d0] * fp);
+          dst[d0 + 8] = fmaf(o[mt][2 + c] * c8, fu, pr[2 + d0 + 8] * fp);
         }
       }
       return;
@@ -799,9 +840,18 @@ __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodePa
     const int wf = U0 / ppw, wl = (U0 + Ps - 1) / ppw;
     if (wf == wl) continue;  // written directly by its warp
     const int n_u = wl - wf + 1;
+    const int h = lu / p.n_ht;
+    const int64_t orow = (int64_t)s * p.Hq + h * p.G + 8 * ht + rr;
     float M = kNegInf, Lsum = 0.f, acc[NE];
 #pragma unroll
     for (int i = 0; i < NE; ++i) acc[i] = 0.f;
+    if (p.pre != nullptr) {  // cascade: the prefix partial is one more piece
+      const float* pr = p.pre + orow * (D + 2);
+      M = pr[0];
+      Lsum = pr[1];
+#pragma unroll
+      for (int i = 0; i < NE; ++i) acc[i] = pr[2 + lane + 32 * i];
+    }
     for (int k0 = 0; k0 < n_u; k0 += CH) {
       float mk[CH], lk[CH], ok[CH][NE];
 #pragma unroll
@@ -839,8 +889,7 @@ __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodePa
       }
       M = cm;
     }
-    const int h = lu / p.n_ht;
-    float* dst = p.out + ((int64_t)s * p.Hq + h * p.G + 8 * ht + rr) * D;
+    float* dst = p.out + orow * D;
 #pragma unroll
     for (int i = 0; i < NE; ++i) dst[lane + 32 * i] = Lsum > 0.f ? acc[i] / Lsum : 0.f;
   }

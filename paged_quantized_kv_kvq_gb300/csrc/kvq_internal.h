@@ -51,12 +51,35 @@ struct DecodeArgs {
   void* workspace;
   int S, Hq, max_blocks, max_ctx;
   float sm_scale;
+  // shared-prefix cascade: skip the first `skip` blocks of every sequence and
+  // fold in the prefix partials `pre` ([S][Hq][D+2]); 0 / null otherwise
+  int skip = 0;
+  const float* pre = nullptr;
 };
 
 // `dependent`: launch the decode as a programmatic dependent of the kernel
 // just before it on the stream (the decode-step append).
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st,
                           bool dependent = false);
+
+// Shared-prefix attention: the first P blocks of every sequence (those of
+// table row 0) attended once per kv head for all sequences' Q rows; writes the
+// partial rows pre[S][Hq][D+2] (m, l, O) that a decode with skip = P folds in.
+struct PrefixPlan {
+  int grid = 0, ntiles = 0, chunk = 0, nstage = 0, stage_bytes = 0, bar_off = 0, smem_bytes = 0;
+};
+bool plan_prefix(const PoolView& pool, int S, int Hq, int P, PrefixPlan* plan);
+struct PrefixArgs {
+  PoolView pool;
+  const __half* q;
+  const int* table;
+  const int* lens;
+  float* pre;
+  int S, Hq, max_ctx, P;
+  float sm_scale;
+};
+cudaError_t launch_prefix(const PrefixArgs& a, const PrefixPlan& plan, cudaStream_t st,
+                          bool dependent);
 
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;

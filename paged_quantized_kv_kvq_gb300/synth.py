@@ -197,6 +197,24 @@ def workload(name: str, *, S: int | None = None, L: int | None = None,
         fmts = [(INT8_PER_GROUP, 128) if i < nl - n16 else (FP16, 0) for i in range(nl)]
         return Workload("mixed_256", nl, Sx, 32, 8, 128, bsz, nb, lens, table, fmts,
                         np.zeros((0, 2), np.int64), 1.0, 0.0, sd, shared_prefix_tokens=prefix)
+    if name == "shared4k_256":
+        # A prefix-heavy batch: 256 sequences that share a 4096-token prefix
+        # (256 physical blocks) and each add a suffix uniform in [64, 512];
+        # 32 Q / 8 KV heads, head_dim 128, block 16, INT8 per-group 128.
+        sd = 5 if seed is None else seed
+        rng = np.random.default_rng(sd)
+        Sx, bsz = S or 256, bs or 16
+        nl = layers or 32
+        prefix = 4096
+        suffix = rng.integers(64, (L or 512) + 1, size=Sx)
+        lens = (prefix + suffix).astype(np.int32)
+        pblk = prefix // bsz
+        need = pblk + int(sum((int(x) + bsz - 1) // bsz - pblk for x in lens))
+        nb = math.ceil(need / 0.9)
+        table = _table_from_lens(rng, lens, bsz, nb, prefix_blocks=pblk)
+        return Workload("shared4k_256", nl, Sx, 32, 8, 128, bsz, nb, lens, table,
+                        [(INT8_PER_GROUP, 128)] * nl, np.zeros((0, 2), np.int64), 1.0, 0.0, sd,
+                        shared_prefix_tokens=prefix)
     raise KeyError(name)
 
 
