@@ -225,6 +225,27 @@ kvq_status kvq_cascade_decode(const kvq_pool* pool, const kvq_half* q, int num_s
                               float* out, void* workspace, size_t ws_bytes,
                               cudaStream_t stream);
 
+/* Prefill / chunked prefill ([KVC] §1.1: the prompt's tokens are processed
+ * together, each attending causally to every token up to itself; a long prompt
+ * may be split into chunks, each attending to the cache the earlier chunks
+ * wrote): attention of each sequence's new query tokens over its paged cache.
+ *   q             : fp16 [Tq][num_q_heads][head_dim], Tq = q_start[num_seqs]
+ *   q_start       : int32 [num_seqs + 1] (device); sequence s's query tokens
+ *                   are rows q_start[s] .. q_start[s+1]-1, n_s of them
+ *   max_q_len     : host-side upper bound of n_s (sizes the grid)
+ *   context_lens  : int32 [num_seqs]: L_s tokens in the cache, this chunk's
+ *                   included -- its K/V must already be appended (kvq_append);
+ *                   query token i sits at position L_s - n_s + i
+ *   out           : fp32 [Tq][num_q_heads][head_dim]
+ * out[row] = softmax(q . k^T * sm_scale) v over positions 0 .. L_s - n_s + i.
+ * Device errors: L_s < n_s or L_s > max_context_len sets OUT_OF_RANGE (L_s is
+ * clamped; rows with no position left get zeros); a block id outside the
+ * pool sets OUT_OF_RANGE and that block is skipped.  No workspace. */
+kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
+                       const int32_t* q_start, int max_q_len, const int32_t* block_table,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                       float sm_scale, float* out, cudaStream_t stream);
+
 /* kvq_decode_step with the cascade decode: the new token of sequence s goes to
  * position context_lens[s]-1, which must lie past the shared prefix (a token
  * written into a shared block would change every sequence's prefix). */

@@ -93,6 +93,7 @@ def _declare(L):
         "kvq_paged_decode_noalloc": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, i32, P]),
         "kvq_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
         "kvq_cascade_workspace_bytes": (sz, [P, i32, i32, i32]),
+        "kvq_prefill": (i32, [P, P, i32, i32, P, i32, P, i32, P, i32, f32, P, P]),
         "kvq_cascade_decode": (i32, [P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz, P]),
         "kvq_cascade_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz,
                                           P]),
@@ -262,6 +263,21 @@ def kvq_cascade_decode_step(pool, k_new, v_new, q, block_table, context_lens, ma
         int(prefix_blocks), float(sm_scale), _ptr(out, torch.float32, "out"),
         _ptr(workspace, None, "workspace") if workspace is not None else None, ws_bytes,
         _stream(stream)), "kvq_cascade_decode_step")
+
+
+def kvq_prefill(pool, q, q_start, max_q_len, block_table, context_lens, max_context_len, sm_scale,
+                out, stream=None) -> None:
+    """Causal attention of each sequence's new query tokens over its cache
+    (kvq_prefill in include/kvq.h).  q: [Tq, Hq, D] fp16, q_start: [S+1] int32."""
+    import torch
+
+    Tq, Hq, _ = q.shape
+    S = q_start.numel() - 1
+    _check(lib().kvq_prefill(
+        pool, _ptr(q, torch.float16, "q"), S, Hq, _ptr(q_start, torch.int32, "q_start"),
+        int(max_q_len), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len), float(sm_scale),
+        _ptr(out, torch.float32, "out"), _stream(stream)), "kvq_prefill")
 
 
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20

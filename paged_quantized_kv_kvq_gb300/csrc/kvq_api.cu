@@ -333,8 +333,8 @@ static kvq_status cascade(kvq_pool* pool, const kvq_half* k_new, const kvq_half*
                                  context_lens, max_context_len, sm_scale, out, dws, dws_bytes, 0,
                                  &a, &plan);
   if (st != KVQ_OK || num_seqs == 0) return st;
-  kvq::PrefixPlan pplan;
-  if (casc && !kvq::plan_prefix(pool->view, num_seqs, num_q_heads, prefix_blocks, &pplan))
+  kvq::RowsPlan pplan;
+  if (casc && !kvq::plan_rows(pool->view, 0, num_seqs, num_q_heads, num_seqs, &pplan))
     return KVQ_ERR_UNSUPPORTED;
   const bool step = k_new != nullptr || v_new != nullptr;
   if (step) {
@@ -348,21 +348,23 @@ static kvq_status cascade(kvq_pool* pool, const kvq_half* k_new, const kvq_half*
     if (e != cudaSuccess) return from_cuda(e);
   }
   if (casc) {
-    kvq::PrefixArgs pa;
+    kvq::RowsArgs pa;
     pa.pool = pool->view;
     pa.q = reinterpret_cast<const __half*>(q);
     pa.table = block_table;
     pa.lens = context_lens;
-    pa.pre = static_cast<float*>(workspace);
+    pa.out = static_cast<float*>(workspace);
+    pa.mode = 0;
     pa.S = num_seqs;
     pa.Hq = num_q_heads;
+    pa.max_blocks = max_blocks_per_seq;
     pa.max_ctx = max_context_len;
     pa.P = prefix_blocks;
     pa.sm_scale = sm_scale;
-    cudaError_t e = kvq::launch_prefix(pa, pplan, stream, step);
+    cudaError_t e = kvq::launch_rows(pa, pplan, stream, step);
     if (e != cudaSuccess) return from_cuda(e);
     a.skip = prefix_blocks;
-    a.pre = pa.pre;
+    a.pre = pa.out;
   }
   return from_cuda(kvq::launch_decode(a, plan, stream, step || casc));
 }
@@ -397,6 +399,40 @@ kvq_status kvq_cascade_decode_step(kvq_pool* pool, const kvq_half* k_new, const 
   return cascade(pool, k_new, v_new, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq,
                  context_lens, max_context_len, prefix_blocks, sm_scale, out, workspace, ws_bytes,
                  stream);
+}
+
+kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
+                       const int32_t* q_start, int max_q_len, const int32_t* block_table,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                       float sm_scale, float* out, cudaStream_t stream) {
+  if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || max_q_len < 0 ||
+      max_blocks_per_seq < 1 || max_context_len < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_q_len == 0) return KVQ_OK;
+  if (q == nullptr || q_start == nullptr || block_table == nullptr || context_lens == nullptr ||
+      out == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % pool->view.Hkv != 0) return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * pool->view.bs) return KVQ_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) & 15) return KVQ_ERR_INVALID_ARG;
+  kvq::RowsPlan plan;
+  if (!kvq::plan_rows(pool->view, 1, num_seqs, num_q_heads, max_q_len, &plan))
+    return KVQ_ERR_UNSUPPORTED;
+  kvq::RowsArgs a;
+  a.pool = pool->view;
+  a.q = reinterpret_cast<const __half*>(q);
+  a.table = block_table;
+  a.lens = context_lens;
+  a.q_start = q_start;
+  a.out = out;
+  a.mode = 1;
+  a.S = num_seqs;
+  a.Hq = num_q_heads;
+  a.max_blocks = max_blocks_per_seq;
+  a.max_ctx = max_context_len;
+  a.sm_scale = sm_scale;
+  return from_cuda(kvq::launch_rows(a, plan, stream, false));
 }
 
 kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,

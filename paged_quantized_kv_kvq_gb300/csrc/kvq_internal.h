@@ -62,24 +62,30 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st,
                           bool dependent = false);
 
-// Shared-prefix attention: the first P blocks of every sequence (those of
-// table row 0) attended once per kv head for all sequences' Q rows; writes the
-// partial rows pre[S][Hq][D+2] (m, l, O) that a decode with skip = P folds in.
-struct PrefixPlan {
-  int grid = 0, ntiles = 0, chunk = 0, nstage = 0, stage_bytes = 0, bar_off = 0, smem_bytes = 0;
+// Many-rows attention (kvq_rows_impl.cuh).  mode 0 (shared prefix): the
+// first P blocks of every sequence (those of table row 0) attended once per kv
+// head for all sequences' Q rows, writing the partial rows out[S][Hq][D+2]
+// (m, l, O) that a decode with skip = P folds in.  mode 1 (prefill): the
+// query tokens q_start[s]..q_start[s+1]-1 of each sequence attend causally to
+// its cache, writing out[Tq][Hq][D].  rows_per_unit: S for the prefix, the
+// longest chunk for prefill.
+struct RowsPlan {
+  int grid = 0, ntiles = 0, nstage = 0, stage_bytes = 0, bar_off = 0, smem_bytes = 0;
 };
-bool plan_prefix(const PoolView& pool, int S, int Hq, int P, PrefixPlan* plan);
-struct PrefixArgs {
+bool plan_rows(const PoolView& pool, int mode, int S, int Hq, int rows_per_unit, RowsPlan* plan);
+struct RowsArgs {
   PoolView pool;
   const __half* q;
   const int* table;
   const int* lens;
-  float* pre;
-  int S, Hq, max_ctx, P;
+  const int* q_start = nullptr;
+  float* out;
+  int mode = 0;
+  int S, Hq, max_blocks, max_ctx;
+  int P = 0;
   float sm_scale;
 };
-cudaError_t launch_prefix(const PrefixArgs& a, const PrefixPlan& plan, cudaStream_t st,
-                          bool dependent);
+cudaError_t launch_rows(const RowsArgs& a, const RowsPlan& plan, cudaStream_t st, bool dependent);
 
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;

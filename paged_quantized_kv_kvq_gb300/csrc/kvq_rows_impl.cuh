@@ -1,18 +1,24 @@
-// kvq_prefix_impl.cuh -- shared-prefix ("cascade") attention over a quantized
-// KV pool.
+// kvq_rows_impl.cuh -- attention of many Q rows per kv head over a quantized
+// paged KV pool: the shared-prefix cascade and prefill.
 //
 // Method ("KV Cache优化实战：大模型推理显存占用与加速方案详解",
-// 0539edu.com/news/5800990, §2.2 and §4.3 on PagedAttention sharing the blocks
-// of a common prefix between requests; xpshop.cn article-402 §三 on shared
-// system prompts): when every sequence's first P blocks are the same physical
-// blocks, those blocks are attended once for all sequences' Q rows instead of
-// once per sequence.  The result is a partial (running max m, sum l,
-// unnormalised output O, base-2 softmax) per (sequence, Q head) that the paged
-// decode over the remaining blocks folds in by log-sum-exp.
+// 0539edu.com/news/5800990):
+//  * shared prefix (§2.2 and §4.3: PagedAttention lets requests with a common
+//    prefix share its physical blocks; xpshop.cn article-402 §三: shared
+//    system prompts): when every sequence's first P blocks are the same
+//    physical blocks, those blocks are attended once for all sequences' Q rows
+//    instead of once per sequence.  The result is a partial (running max m,
+//    sum l, unnormalised output O, base-2 softmax) per (sequence, Q head) that
+//    the paged decode over the remaining blocks folds in by log-sum-exp.
+//  * prefill (§1.1: the prompt's tokens are processed together, each attending
+//    causally to the tokens up to itself; a long prompt may be processed in
+//    chunks, each chunk attending to the cache written by the earlier ones):
+//    the rows are the chunk's query tokens times the group's Q heads, every row
+//    with its own causal limit, over the sequence's own blocks.
 //
 // GB300 design: a CTA takes one kv head and a tile of 16 Q rows -- a row is a
-// (sequence, Q head of the group) pair, so one tile usually spans several
-// sequences -- and its 4 warps split the prefix blocks between them.  Each
+// (sequence, Q head) pair for the prefix, a (query token, Q head) pair for
+// prefill -- and its 4 warps split the blocks the tile needs between them.  Each
 // warp streams its blocks through bulk-copy stages (as the decode kernel does)
 // and computes with the rows on the M dimension of mma.m16n8k16: Q.K^T takes
 // the K codes of the fragment-native page layout directly as B fragments
@@ -32,26 +38,33 @@
 
 namespace kvq {
 
-constexpr int kPrefixWarps = 4;
-constexpr int kPrefixThreads = kPrefixWarps * 32;
-constexpr int kPrefixRows = 16;  // Q rows per CTA: one mma M tile
+constexpr int kRowsWarps = 4;
+constexpr int kRowsThreads = kRowsWarps * 32;
+constexpr int kRowsTile = 16;  // Q rows per CTA: one mma M tile
 
-struct PrefixParams {
+enum RowsMode : int {
+  ROWS_PREFIX = 0,   // rows (sequence, Q head) over the shared blocks of table row 0
+  ROWS_PREFILL = 1,  // rows (query token, Q head) of one sequence, causal
+};
+
+struct RowsParams {
   PoolView pool;
-  const __half* q;    // [S][Hq][D]
-  const int* table;   // [S][max_blocks]; row 0's first P entries are the shared blocks
-  const int* lens;    // [S]
-  float* pre;         // [S][Hq][D + 2]: m, l, O per (sequence, Q head)
-  int S, Hq, G, max_ctx, P;
-  int ntiles;         // row tiles per kv head: ceil(S * G / 16)
-  int chunk;          // prefix blocks per warp
+  const __half* q;      // prefix: [S][Hq][D]; prefill: [Tq][Hq][D]
+  const int* table;     // [S][max_blocks]
+  const int* lens;      // [S] tokens in the cache (prefill: including the chunk)
+  const int* q_start;   // prefill: [S + 1] first query row of each sequence
+  float* out;           // prefix: [S][Hq][D + 2] partial rows; prefill: [Tq][Hq][D]
+  int mode;
+  int S, Hq, G, max_blocks, max_ctx;
+  int P;                // prefix: shared blocks
+  int ntiles;           // row tiles per (kv head[, sequence])
   int nstage, stage_bytes;
-  int bar_off;        // shared-memory offset of the barriers (past stages and merge rows)
+  int bar_off;          // shared-memory offset of the barriers (past stages and merge rows)
   float sm_scale_log2;
 };
 
 template <int FMT, int D, int NG>
-__global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const PrefixParams p) {
+__global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams p) {
   using T = FmtTraits<FMT>;
   constexpr int KS = D / 16;  // k-steps of Q.K^T
   constexpr int NW = D / 8;   // 8-channel n-tiles of P.V
@@ -67,33 +80,64 @@ __global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const Prefix
   const int g = lane >> 2, j = lane & 3;
   const PoolView& pool = p.pool;
   const int bs = pool.bs;
-  const int h = blockIdx.x / p.ntiles, tile = blockIdx.x % p.ntiles;
   const int nstage = p.nstage;
+  const bool prefill = p.mode == ROWS_PREFILL;
+  // grid: prefix (kv head, tile); prefill (kv head, sequence, tile)
+  const int tile = blockIdx.x % p.ntiles;
+  const int seq = prefill ? (blockIdx.x / p.ntiles) % p.S : 0;
+  const int h = prefill ? blockIdx.x / (p.ntiles * p.S) : blockIdx.x / p.ntiles;
 
-  // The decode that follows reads our output only after its
-  // griddepcontrol.wait on this grid's completion.
+  // A kernel launched after this one as a programmatic dependent reads our
+  // output only after its griddepcontrol.wait on this grid's completion.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   char* stages = smem + warp * nstage * p.stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off) + warp * nstage;
   int* stage_phys =
-      reinterpret_cast<int*>(smem + p.bar_off + kPrefixWarps * nstage * 8) + warp * nstage;
+      reinterpret_cast<int*>(smem + p.bar_off + kRowsWarps * nstage * 8) + warp * nstage;
 
-  // ---- this lane's rows (g and g+8 of the tile) and their token limits
-  const int rows_total = p.S * p.G;
-  const int ptok = p.P * bs;
+  // ---- rows of the tile: the tile's row rr is (sequence rr / G, head rr % G)
+  // for the prefix and (query token rr / G, head rr % G) of sequence `seq`
+  // for prefill; each has a token limit (its context, or its causal end)
+  int rows_total, qbase = 0, ctx = 0, nq = 0;
+  if (prefill) {
+    qbase = p.q_start[seq];
+    nq = p.q_start[seq + 1] - qbase;
+    ctx = p.lens[seq];
+    if (ctx > p.max_ctx || ctx < nq) {
+      if (tile == 0 && h == 0 && threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
+      ctx = min(ctx, p.max_ctx);
+    }
+    rows_total = nq * p.G;
+  } else {
+    rows_total = p.S * p.G;
+  }
+  if (tile * kRowsTile >= rows_total) return;  // past this sequence's chunk
+  const int table_row = prefill ? seq : 0;
+  const int page_cap = prefill ? p.max_blocks : p.P;
+  auto row_of = [&](int rr, int& lim, const __half*& qp, int64_t& orow) {
+    lim = 0;
+    qp = nullptr;
+    orow = -1;
+    if (rr >= rows_total) return;
+    const int hq = h * p.G + rr % p.G;
+    if (prefill) {
+      const int i = rr / p.G;
+      lim = max(0, ctx - nq + i + 1);
+      orow = (int64_t)(qbase + i) * p.Hq + hq;
+    } else {
+      const int s = rr / p.G;
+      lim = max(0, min(min(p.lens[s], p.max_ctx), p.P * bs));
+      orow = (int64_t)s * p.Hq + hq;
+    }
+    qp = p.q + orow * D;
+  };
   int lim[2];
   const __half* qrow[2];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    const int r = tile * kPrefixRows + g + 8 * c;
-    lim[c] = 0;
-    qrow[c] = nullptr;
-    if (r < rows_total) {
-      const int s = r / p.G, hq = h * p.G + r % p.G;
-      lim[c] = max(0, min(min(p.lens[s], p.max_ctx), ptok));
-      qrow[c] = p.q + ((int64_t)s * p.Hq + hq) * D;
-    }
+    int64_t orow;
+    row_of(tile * kRowsTile + g + 8 * c, lim[c], qrow[c], orow);
   }
 
   // ---- Q as A fragments: a0/a2 = row g, channels 16kk+4j..+3; a1/a3 = row g+8
@@ -145,13 +189,17 @@ __global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const Prefix
       }
   }
 
-  // ---- this warp's prefix blocks: only those some row of the warp needs
+  // ---- this warp's blocks: the tile needs blocks [0, np), split in 4 runs
+  // (every warp holds all 16 rows, so wlim is the tile's widest limit)
   int wlim = max(lim[0], lim[1]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) wlim = max(wlim, __shfl_xor_sync(0xffffffffu, wlim, off));
-  const int p0 = warp * p.chunk;
-  const int p1 = min(min(p.P, p0 + p.chunk), (wlim + bs - 1) / bs);
+  const int np = min(page_cap, (wlim + bs - 1) / bs);
+  const int chunk = (np + kRowsWarps - 1) / kRowsWarps;
+  const int p0 = warp * chunk;
+  const int p1 = min(np, p0 + chunk);
   const int n_w = max(p1 - p0, 0);
+  const int* trow = p.table + (int64_t)table_row * p.max_blocks;
 
   if (lane == 0) {
     for (int st = 0; st < nstage; ++st) mbar_init(&bars[st], 1);
@@ -164,12 +212,12 @@ __global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const Prefix
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const uint32_t page_tx = pool.page_bytes + (T::token_scales ? 2 * bs * 4 : 0);
-  const int tcache = lane < n_w ? p.table[p0 + lane] : -1;
+  const int tcache = lane < n_w ? trow[p0 + lane] : -1;
   int n_issued = 0, pst = 0;
   auto issue_next = [&]() {  // all lanes call; lane 0 issues
     const int cached = __shfl_sync(0xffffffffu, tcache, n_issued & 31);
     if (lane == 0) {
-      const int phys = n_issued < 32 ? cached : p.table[p0 + n_issued];
+      const int phys = n_issued < 32 ? cached : trow[p0 + n_issued];
       const int st = pst;
       const bool ok = phys >= 0 && (int64_t)phys < pool.num_blocks;
       stage_phys[st] = ok ? phys : -1;
@@ -235,11 +283,13 @@ __global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const Prefix
         }
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
+          // the scales of tokens no row reads may never have been written
           const int tk = 8 * (x >> 1) + 2 * j + (x & 1);
+          const bool w = tk < nvalid;
 #pragma unroll
           for (int gi = 0; gi < NS; ++gi) {
-            ks[x][gi] = ksp[tk * NS + gi];
-            vs[x][gi] = vsp[tk * NS + gi];
+            ks[x][gi] = w ? ksp[tk * NS + gi] : 0.f;
+            vs[x][gi] = w ? vsp[tk * NS + gi] : 0.f;
           }
         }
       }
@@ -418,7 +468,7 @@ __global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const Prefix
       float lt = l[c];
       lt += __shfl_xor_sync(0xffffffffu, lt, 1);
       lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-      float* row = mb + ((int64_t)warp * kPrefixRows + g + 8 * c) * (D + 2);
+      float* row = mb + ((int64_t)warp * kRowsTile + g + 8 * c) * (D + 2);
       if (j == 0) {
         row[0] = failed ? kNegInf : m[c];
         row[1] = failed ? 0.f : lt;
@@ -433,33 +483,39 @@ __global__ void __launch_bounds__(kPrefixThreads) kvq_prefix_kernel(const Prefix
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < kPrefixRows * D; idx += kPrefixThreads) {
+  for (int idx = threadIdx.x; idx < kRowsTile * D; idx += kRowsThreads) {
     const int rr = idx / D, d = idx % D;
-    const int r = tile * kPrefixRows + rr;
-    if (r >= rows_total) continue;
+    int rlim;
+    const __half* rq;
+    int64_t orow;
+    row_of(tile * kRowsTile + rr, rlim, rq, orow);
+    if (orow < 0) continue;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kPrefixWarps; ++w) M = fmaxf(M, mb[(w * kPrefixRows + rr) * (D + 2)]);
+    for (int w = 0; w < kRowsWarps; ++w) M = fmaxf(M, mb[(w * kRowsTile + rr) * (D + 2)]);
     float Ls = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kPrefixWarps; ++w) {
-      const float* row = mb + (w * kPrefixRows + rr) * (D + 2);
+    for (int w = 0; w < kRowsWarps; ++w) {
+      const float* row = mb + (w * kRowsTile + rr) * (D + 2);
       const float wt = row[0] == kNegInf ? 0.f : fast_exp2(row[0] - M);
       Ls = fmaf(wt, row[1], Ls);
       O = fmaf(wt, row[2 + d], O);
     }
-    const int s = r / p.G, hq = h * p.G + r % p.G;
-    float* dst = p.pre + ((int64_t)s * p.Hq + hq) * (D + 2);
-    dst[2 + d] = O;
-    if (d == 0) {
-      dst[0] = M;
-      dst[1] = Ls;
+    if (prefill) {
+      p.out[orow * D + d] = Ls > 0.f ? O / Ls : 0.f;
+    } else {
+      float* dst = p.out + orow * (D + 2);
+      dst[2 + d] = O;
+      if (d == 0) {
+        dst[0] = M;
+        dst[1] = Ls;
+      }
     }
   }
 }
 
-struct PrefixLaunch {
-  PrefixParams p;
+struct RowsLaunch {
+  RowsParams p;
   dim3 grid;
   int smem;
   cudaStream_t st;
@@ -467,20 +523,20 @@ struct PrefixLaunch {
 };
 
 template <int FMT, int D, int NG>
-cudaError_t run_prefix(const PrefixLaunch& l) {
+cudaError_t run_rows(const RowsLaunch& l) {
   static bool attr_set[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDevices && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kvq_prefix_kernel<FMT, D, NG>,
+    e = cudaFuncSetAttribute(kvq_rows_kernel<FMT, D, NG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = l.grid;
-  cfg.blockDim = dim3(kPrefixThreads);
+  cfg.blockDim = dim3(kRowsThreads);
   cfg.dynamicSmemBytes = l.smem;
   cfg.stream = l.st;
   cudaLaunchAttribute attr[1];
@@ -488,7 +544,7 @@ cudaError_t run_prefix(const PrefixLaunch& l) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = l.dependent ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kvq_prefix_kernel<FMT, D, NG>, l.p);
+  return cudaLaunchKernelEx(&cfg, kvq_rows_kernel<FMT, D, NG>, l.p);
 }
 
 }  // namespace kvq

@@ -1,0 +1,113 @@
+"""GPU parity of prefill / chunked prefill over the paged quantized cache: each
+sequence's new query tokens attend causally to its cache (the chunk's own K/V
+already appended).  The float64 oracle is the decode definition applied per
+query token with the causal length: query token i of sequence s is a decode
+over positions 0 .. L_s - n_s + i through the same block-table row."""
+import numpy as np
+import pytest
+import torch
+
+import paged_quantized_kv_kvq_gb300 as kvq
+from paged_quantized_kv_kvq_gb300 import synth
+from kvq_testutil import TOL, gpu_pool, layer_tokens, oracle_layer
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+FORMATS = [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_GROUP, 32), (kvq.KVQ_INT8_PER_TOKEN, 0),
+           (kvq.KVQ_INT8_PER_CHANNEL, 0), (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0)]
+
+
+def _t(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def _queries(Tq, Hq, D, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((Tq, Hq, D)).astype(np.float16)
+
+
+def _expand(table, lens, nq):
+    """Per query token: its sequence's table row and causal length."""
+    rows, L = [], []
+    for s, (Ls, n) in enumerate(zip(lens, nq)):
+        for i in range(n):
+            rows.append(table[s])
+            L.append(max(0, int(Ls) - int(n) + i + 1))
+    return np.array(rows, np.int32), np.array(L, np.int32)
+
+
+def _case(fmt, group, name="gqa_64x2048", S=3, L=300, nq=(50, 17, 64), lens=None, seed=0, **kw):
+    w = synth.workload(name, S=S, L=L, layers=1, **kw)
+    w.layer_formats = [(fmt, group)]
+    k, v, slots = layer_tokens(w, 0)
+    calib = (k, v) if fmt == kvq.KVQ_INT8_PER_CHANNEL else None
+    pool = gpu_pool(w, fmt, group, DEV, k, v, slots, calib=calib)
+    ref, table, _ = oracle_layer(w, fmt, group, k, v, slots, list(range(w.S)), calib=calib)
+    lens = w.context_lens.copy() if lens is None else np.asarray(lens, np.int32)
+    nq = np.asarray(nq, np.int32)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = _queries(int(qs[-1]), w.Hq, w.D, seed)
+    out = torch.empty((int(qs[-1]), w.Hq, w.D), dtype=torch.float32, device=DEV)
+    kvq.kvq_prefill(pool.handle, _t(q), _t(qs), int(nq.max()), _t(w.block_table), _t(lens),
+                    int(max(lens.max(), 1)), w.D ** -0.5, out)
+    torch.cuda.synchronize()
+    t_exp, l_exp = _expand(table, lens, nq)
+    exp = ref.decode(q, t_exp, l_exp)
+    return pool, out.cpu().numpy(), exp, l_exp
+
+
+@pytest.mark.parametrize("fmt,group", FORMATS)
+def test_prefill_parity(fmt, group):
+    pool, got, exp, _ = _case(fmt, group)
+    assert pool.error() == kvq.KVQ_OK
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    pool.close()
+
+
+def test_prefill_whole_prompt_and_long_context():
+    """A fresh prompt (chunk = whole context) and a chunk deep into a long
+    context, MHA with head_dim 128, and GQA 4:1 with D 64 (tiny)."""
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 128, S=2, L=1300, nq=(1300, 300))
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    assert pool.error() == kvq.KVQ_OK
+    pool.close()
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 64, name="mha_100_int8g64", S=2, L=400,
+                              nq=(33, 1))
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    pool.close()
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 64, name="tiny", S=4, L=None, nq=(17, 5, 64, 3))
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    pool.close()
+
+
+def test_prefill_one_token_chunks_equal_decode():
+    """A chunk of one token per sequence is exactly the decode problem."""
+    w = synth.workload("gqa_64x2048", S=4, L=200, layers=1)
+    fmt, group = w.layer_formats[0]
+    k, v, slots = layer_tokens(w, 0)
+    pool = gpu_pool(w, fmt, group, DEV, k, v, slots)
+    q = synth.queries(w, 0)
+    qs = np.arange(w.S + 1, dtype=np.int32)
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    kvq.kvq_prefill(pool.handle, _t(q), _t(qs), 1, _t(w.block_table), _t(w.context_lens), 200,
+                    w.D ** -0.5, out)
+    dec = pool.decode(_t(q), _t(w.block_table), _t(w.context_lens), 200)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(out.cpu().numpy(), dec.cpu().numpy(), rtol=2e-5, atol=2e-5)
+    pool.close()
+
+
+def test_prefill_edges():
+    """Ragged tiles, a grid wider than the chunks, an empty chunk, and a
+    context shorter than its chunk (flagged; the rows left without a position
+    get zeros)."""
+    pool, got, exp, l_exp = _case(kvq.KVQ_FP16, 0, nq=(5, 0, 1))
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    assert pool.error() == kvq.KVQ_OK
+    pool.close()
+    pool, got, exp, l_exp = _case(kvq.KVQ_INT8_PER_GROUP, 128, nq=(20, 3, 7), lens=(10, 300, 300))
+    assert pool.error() == kvq.KVQ_ERR_OUT_OF_RANGE
+    assert not got[:10].any()          # positions before the start of the context
+    np.testing.assert_allclose(got[10:], exp[10:], rtol=0, atol=TOL)
+    pool.close()
