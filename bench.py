@@ -525,10 +525,110 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_prefill(args, rank, world, local_rank):
+    """Prefill of fresh prompts: per layer, append every prompt token's K/V
+    (quantized) and run causal attention of all prompt tokens over the cache.
+    Metric: algorithmic attention FLOP/s (4 * Hq * D per (query, key) pair
+    with key <= query: Q.K and P.V, 2 FLOP per multiply-add)."""
+    import torch
+
+    import paged_quantized_kv_kvq_gb300 as kvq
+    from paged_quantized_kv_kvq_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    kvq.lib()
+    w = synth.workload(args.workload, S=args.prefill_seqs, layers=args.layers)
+    stream = torch.cuda.current_stream()
+    L = w.layers
+    lens = w.context_lens.astype(np.int64)
+    T = int(lens.sum())
+    slots = torch.from_numpy(np.concatenate([w.slots_for(s, 0, int(lens[s]))
+                                             for s in range(w.S)])).to(dev)
+    qs = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(dev)
+    table = torch.from_numpy(w.block_table).to(dev)
+    ln = torch.from_numpy(w.context_lens).to(dev)
+    pools = [kvq.KVPool(w.num_blocks, w.bs, w.Hkv, w.D, f, g, device=dev) for f, g in w.layer_formats]
+    kin, vin, qin = [], [], []
+    for l in range(L):
+        ks, vs = zip(*[synth.device_kv(w, l, s, 0, int(lens[s]), dev) for s in range(w.S)])
+        kin.append(torch.cat(ks))
+        vin.append(torch.cat(vs))
+        g = torch.Generator(device=dev)
+        g.manual_seed(7919 * (l + 1))
+        qin.append(torch.randn((T, w.Hq, w.D), generator=g, device=dev).half())
+    out = torch.empty((T, w.Hq, w.D), dtype=torch.float32, device=dev)
+    mq = int(lens.max())
+    sm_scale = w.D ** -0.5
+
+    def step():
+        for l in range(L):
+            kvq.kvq_append(pools[l].handle, kin[l], vin[l], slots, stream)
+            kvq.kvq_prefill(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for p in pools:
+        assert p.error() == kvq.KVQ_OK
+    K = args.steps
+    sampler = ClockSampler(gpu_index(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    # the attention kernel alone, per layer, for the roofline
+    KR = max(1, min(K, 10))
+    evs = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in range(KR * L)]
+    for i in range(KR):
+        for l in range(L):
+            evs[i * L + l][0].record(stream)
+            kvq.kvq_prefill(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, out, stream)
+            evs[i * L + l][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / K
+    att_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    pairs = int((lens * (lens + 1) // 2).sum())
+    flop_layer = 4 * pairs * w.Hq * w.D
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    achieved = flop_layer / (att_ms * 1e-3) / 1e12
+    value = world * flop_layer * L / (ms * 1e-3) / 1e12
+    return {
+        "metric": "Paged quantized-KV prefill: causal attention TFLOP/s (algorithmic)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i8 codes x f16 mma -> f32 acc",
+        "data": "synthetic (seeded on-device normal draws)",
+        "config": {"workload": "%s prefill" % w.name, "layers": L, "prompts": w.S,
+                   "prompt_len": int(lens.max()), "q_heads": w.Hq, "kv_heads": w.Hkv,
+                   "head_dim": w.D, "block_size": w.bs,
+                   "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f == 3 else "")
+                                        for f, g in w.layer_formats}),
+                   "step": "per layer: kvq_append (every prompt token) then kvq_prefill"},
+        "prompt_tok_per_s": round(world * T / (ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "kvq_prefill call (mma.sync m16n8k16 f16 -> f32), %d calls timed "
+                               "one by one after the step region" % (KR * L),
+                     "flop_per_launch": flop_layer, "avg_launch_ms": round(att_ms, 4),
+                     "peak_source": "%s bf16_tflops_sustained (f16 has the bf16 rate)" % peak_kind},
+        "gpu_launches": K * L * 2,
+        "clocks": clocks,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 1000 decode steps, 10 prefill steps)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gqa_64x2048")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -539,10 +639,16 @@ def main():
     ap.add_argument("--step-api", default="fused", choices=["fused", "separate"],
                     help="fused: one kvq_decode_step call per layer; separate: kvq_append "
                          "then kvq_paged_decode")
+    ap.add_argument("--op", default="decode", choices=["decode", "prefill"],
+                    help="decode: the decode step (default); prefill: prompt prefill")
+    ap.add_argument("--prefill-seqs", type=int, default=8,
+                    help="prompts in the prefill batch (--op prefill)")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers (profiling runs only; the bench line uses all)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.steps is None:
+        args.steps = 10 if args.op == "prefill" else 1000
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -558,6 +664,13 @@ def main():
 
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+    if args.op == "prefill":
+        res = run_prefill(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:

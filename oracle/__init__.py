@@ -37,6 +37,8 @@ INT8_PER_TOKEN = 1
 INT8_PER_CHANNEL = 2
 INT8_PER_GROUP = 3
 FP8_E4M3_PER_TOKEN = 4
+INT4_PER_GROUP = 5
+GROUP_FORMATS = (INT8_PER_GROUP, INT4_PER_GROUP)
 
 FORMAT_NAMES = {
     FP16: "fp16",
@@ -44,6 +46,7 @@ FORMAT_NAMES = {
     INT8_PER_CHANNEL: "int8_channel",
     INT8_PER_GROUP: "int8_group",
     FP8_E4M3_PER_TOKEN: "fp8_e4m3_token",
+    INT4_PER_GROUP: "int4_group",
 }
 
 
@@ -88,6 +91,8 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_e4m3_encode.argtypes = [f32]
     L.oracle_quant_int8_group.restype = None
     L.oracle_quant_int8_group.argtypes = [P, i32, P, P]
+    L.oracle_quant_int4_group.restype = None
+    L.oracle_quant_int4_group.argtypes = [P, i32, P, P]
     L.oracle_quant_int8_static.restype = None
     L.oracle_quant_int8_static.argtypes = [P, P, i32, P]
     L.oracle_quant_e4m3_group.restype = None
@@ -140,6 +145,14 @@ def quant_int8_group(x) -> tuple[np.ndarray, np.float32]:
     return codes, s[0]
 
 
+def quant_int4_group(x) -> tuple[np.ndarray, np.float32]:
+    x = _f32(x).ravel()
+    codes = np.zeros(x.size, np.int8)
+    s = np.zeros(1, np.float32)
+    lib().oracle_quant_int4_group(_ptr(x), x.size, _ptr(codes), _ptr(s))
+    return codes, s[0]
+
+
 def quant_int8_static(x, scales) -> np.ndarray:
     x = _f32(x).ravel()
     sc = _f32(scales).ravel()
@@ -181,8 +194,8 @@ class OracleCache:
                  head_dim: int, group: int = 0, sentinel_code: int = 0,
                  sentinel_scale: float = 0.0):
         self.fmt, self.bs, self.Hkv, self.D = fmt, block_size, kv_heads, head_dim
-        self.g = group if fmt == INT8_PER_GROUP else 0
-        if fmt == INT8_PER_GROUP and (group <= 0 or head_dim % group):
+        self.g = group if fmt in GROUP_FORMATS else 0
+        if fmt in GROUP_FORMATS and (group <= 0 or head_dim % group):
             raise ValueError("the group size must divide head_dim")
         self.num_slots = num_blocks * block_size
         shape = (self.num_slots, 2, kv_heads, head_dim)
@@ -192,7 +205,7 @@ class OracleCache:
             self.codes = np.full(shape, sentinel_code & 0xFF, np.uint8)
         else:
             self.codes = np.full(shape, sentinel_code, np.int8)
-        if fmt == INT8_PER_GROUP:
+        if fmt in GROUP_FORMATS:
             self.scales = np.full((self.num_slots, 2, kv_heads, head_dim // group),
                                   sentinel_scale, np.float32)
         elif fmt in (INT8_PER_TOKEN, FP8_E4M3_PER_TOKEN):
@@ -249,7 +262,7 @@ class OracleCache:
             vals = table[c]
         else:
             vals = c.astype(np.float64)
-        if self.fmt == INT8_PER_GROUP:
+        if self.fmt in GROUP_FORMATS:
             s = np.repeat(self.scales[:, kv].astype(np.float64), self.g, axis=2)
             return vals * s
         if self.fmt in (INT8_PER_TOKEN, FP8_E4M3_PER_TOKEN):

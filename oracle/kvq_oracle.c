@@ -31,6 +31,10 @@
  *       all kv heads; per-group = g contiguous head_dim elements of one
  *       (token, head, K|V) vector; per-channel = a static [2][Hkv][D] scale set
  *       from calibration tokens (absmax / 127 per channel).
+ *   - INT4, listed beside INT8 and FP8 as the more aggressive option ([KVC]
+ *     §2.3; [P312] §四 measures it): read as the same absmax symmetric rule
+ *     on 4 bits, per group: s = absmax / 7 (fp32), code =
+ *     clamp(round-half-even(x / s), -7, 7), zero group -> s = 0, codes 0.
  *   - Attention: softmax(q.k^T * sm_scale) v over the dequantized cache, in
  *     float64 here ("the same dequantised cache": k^ = code * scale in fp64).
  *
@@ -55,6 +59,7 @@ enum {
     OR_INT8_PER_CHANNEL = 2,
     OR_INT8_PER_GROUP = 3,
     OR_FP8_E4M3_PER_TOKEN = 4,
+    OR_INT4_PER_GROUP = 5,
 };
 
 int oracle_num_threads(void) {
@@ -153,6 +158,29 @@ void oracle_quant_int8_group(const float* x, int n, int8_t* codes, float* scale)
     }
 }
 
+/* One dynamic-scale INT4 group of n values: s = absmax / 7, codes in [-7, 7]
+ * (kept one per byte here). */
+void oracle_quant_int4_group(const float* x, int n, int8_t* codes, float* scale) {
+    float a = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float m = fabsf(x[i]);
+        if (m > a) a = m;
+    }
+    if (a == 0.0f) {
+        *scale = 0.0f;
+        for (int i = 0; i < n; ++i) codes[i] = 0;
+        return;
+    }
+    float s = a / 7.0f;
+    *scale = s;
+    for (int i = 0; i < n; ++i) {
+        float q = nearbyintf(x[i] / s);
+        if (q > 7.0f) q = 7.0f;
+        if (q < -7.0f) q = -7.0f;
+        codes[i] = (int8_t)q;
+    }
+}
+
 /* INT8 with a fixed (calibrated) scale per element: values beyond the
  * calibrated range saturate at +-127; a zero scale gives a zero code. */
 void oracle_quant_int8_static(const float* x, const float* s, int n, int8_t* codes) {
@@ -201,9 +229,10 @@ void oracle_calibrate_channels(const float* x, int64_t T, int C, float* s) {
 /* ------------------------------------------------------------------------- */
 /* The oracle's cache store.  A plain slot-indexed array, deliberately unlike */
 /* any tiled device layout:                                                  */
-/*   codes : [num_slots][2 (K,V)][Hkv][D], one byte per element (int8 or      */
-/*           e4m3), or one float per element for FP16 (the fp16 value, widened)*/
-/*   scales: per-group   [num_slots][2][Hkv][D/g]                              */
+/*   codes : [num_slots][2 (K,V)][Hkv][D], one byte per element (int8, int4   */
+/*           or e4m3), or one float per element for FP16 (the fp16 value,      */
+/*           widened)                                                         */
+/*   scales: per-group   [num_slots][2][Hkv][D/g]  (INT8 and INT4)             */
 /*           per-token   [num_slots][2]                                        */
 /*           per-channel / FP16: unused                                        */
 /* slot = physical_block * block_size + offset_in_block ([KVC] §2.2).          */
@@ -211,7 +240,8 @@ void oracle_calibrate_channels(const float* x, int64_t T, int C, float* s) {
 
 static int scales_per_slot(int fmt, int Hkv, int D, int g) {
     switch (fmt) {
-    case OR_INT8_PER_GROUP: return 2 * Hkv * (D / g);
+    case OR_INT8_PER_GROUP:
+    case OR_INT4_PER_GROUP: return 2 * Hkv * (D / g);
     case OR_INT8_PER_TOKEN:
     case OR_FP8_E4M3_PER_TOKEN: return 2;
     default: return 0;
@@ -249,6 +279,15 @@ void oracle_append(int fmt, int64_t T, int Hkv, int D, int g,
                                                 scales + slot * nsc + (kv * Hkv + h) * ng + gi);
                 break;
             }
+            case OR_INT4_PER_GROUP: {
+                int8_t* c = (int8_t*)codes + base;
+                int ng = D / g;
+                for (int h = 0; h < Hkv; ++h)
+                    for (int gi = 0; gi < ng; ++gi)
+                        oracle_quant_int4_group(x + h * D + gi * g, g, c + h * D + gi * g,
+                                                scales + slot * nsc + (kv * Hkv + h) * ng + gi);
+                break;
+            }
             case OR_INT8_PER_TOKEN: {
                 int8_t* c = (int8_t*)codes + base;
                 oracle_quant_int8_group(x, per, c, scales + slot * nsc + kv);
@@ -278,7 +317,8 @@ static double dequant(int fmt, int Hkv, int D, int g, const void* codes,
     int nsc = scales_per_slot(fmt, Hkv, D, g);
     switch (fmt) {
     case OR_FP16: return (double)((const float*)codes)[idx];
-    case OR_INT8_PER_GROUP: {
+    case OR_INT8_PER_GROUP:
+    case OR_INT4_PER_GROUP: {
         int ng = D / g;
         double s = (double)scales[slot * nsc + (kv * Hkv + h) * ng + d / g];
         return (double)((const int8_t*)codes)[idx] * s;

@@ -60,6 +60,41 @@ def test_int8_error_bound_and_range():
             assert s == np.float32(np.float32(np.abs(x).max()) / np.float32(127))
 
 
+def _golden_int4():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "int4_absmax_cases.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        x, s, c = (p.strip() for p in line.split("|"))
+        rows.append((np.array(x.split(), np.float32), np.float32(s),
+                     np.array(c.split(), np.int8)))
+    return rows
+
+
+@pytest.mark.parametrize("case", range(len(_golden_int4())))
+def test_int4_closed_form(case):
+    x, s_exp, c_exp = _golden_int4()[case]
+    c, s = oracle.quant_int4_group(x)
+    assert s == s_exp
+    np.testing.assert_array_equal(c, c_exp)
+
+
+def test_int4_error_bound_and_range():
+    # |x - c*s| <= s/2, the absmax element maps to +-7, all codes in [-7, 7]
+    rng = np.random.default_rng(12)
+    for n in (16, 32, 64, 128):
+        for _ in range(50):
+            x = (rng.standard_normal(n) * rng.choice([1e-3, 1, 30])).astype(np.float16)
+            c, s = oracle.quant_int4_group(x)
+            xs = x.astype(np.float64)
+            err = np.abs(xs - c.astype(np.float64) * np.float64(s))
+            assert np.all(err <= np.float64(s) * (0.5 + 8 * 2.0 ** -24))
+            assert np.abs(c).max() == 7
+            assert c[np.argmax(np.abs(xs))] == np.sign(xs[np.argmax(np.abs(xs))]) * 7
+            assert s == np.float32(np.float32(np.abs(x).max()) / np.float32(7))
+
+
 def test_int8_static_saturates_and_rounds():
     x = np.array([1.0, -1.0, 300.0, -300.0, 2.5, 0.0, 5.0], np.float32)
     s = np.array([1.0, 1.0, 1.0, 1.0, 1.0, 1.0, 0.0], np.float32)
@@ -145,7 +180,8 @@ def test_kv_size_formula_brute_force(dims):
 
 # ---------------------------------------------------------------- append
 FORMATS = [(oracle.INT8_PER_GROUP, 16), (oracle.INT8_PER_GROUP, 32), (oracle.INT8_PER_TOKEN, 0),
-           (oracle.INT8_PER_CHANNEL, 0), (oracle.FP8_E4M3_PER_TOKEN, 0), (oracle.FP16, 0)]
+           (oracle.INT8_PER_CHANNEL, 0), (oracle.FP8_E4M3_PER_TOKEN, 0), (oracle.FP16, 0),
+           (oracle.INT4_PER_GROUP, 16), (oracle.INT4_PER_GROUP, 32)]
 
 
 def _cache(fmt, g, nb=8, bs=4, hkv=2, d=32, **kw):
@@ -173,10 +209,12 @@ def test_append_places_slots_and_keeps_sentinels(fmt, g):
         for kv, x in ((0, k), (1, v)):
             if fmt == oracle.FP16:
                 np.testing.assert_array_equal(c.codes[slot, kv], x[t].astype(np.float32))
-            elif fmt == oracle.INT8_PER_GROUP:
+            elif fmt in oracle.GROUP_FORMATS:
+                quant = (oracle.quant_int8_group if fmt == oracle.INT8_PER_GROUP
+                         else oracle.quant_int4_group)
                 for h in range(2):
                     for gi in range(32 // g):
-                        cc, s = oracle.quant_int8_group(x[t, h, gi * g:(gi + 1) * g])
+                        cc, s = quant(x[t, h, gi * g:(gi + 1) * g])
                         np.testing.assert_array_equal(c.codes[slot, kv, h, gi * g:(gi + 1) * g], cc)
                         assert c.scales[slot, kv, h, gi] == s
             elif fmt == oracle.INT8_PER_TOKEN:
