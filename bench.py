@@ -34,8 +34,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Paged quantized-KV decode: effective HBM GB/s (% of peak) and decode tok/s"
 FORMAT_NAME = {0: "fp16", 1: "int8 per-token", 2: "int8 per-channel", 3: "int8 per-group",
-               4: "fp8 e4m3 per-token"}
-ESIZE = {0: 2, 1: 1, 2: 1, 3: 1, 4: 1}
+               4: "fp8 e4m3 per-token", 5: "int4 per-group"}
+ESIZE = {0: 2, 1: 1, 2: 1, 3: 1, 4: 1, 5: 0.5}  # bytes per code
+GROUPED = (3, 5)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_traffic.json")
 KERNEL_SOURCES = ["paged_quantized_kv_kvq_gb300/csrc/kvq_decode_impl.cuh",
                   "paged_quantized_kv_kvq_gb300/csrc/kvq_common.cuh",
@@ -50,8 +51,8 @@ def layer_bytes(w, fmt, group, seqs=None):
     n = len(seqs)
     es = ESIZE[fmt]
     tok = int(L.sum())
-    codes = tok * w.Hkv * w.D * 2 * es
-    if fmt == 3:
+    codes = int(tok * w.Hkv * w.D * 2 * es)
+    if fmt in GROUPED:
         scales = tok * w.Hkv * 2 * (w.D // group) * 4
     elif fmt in (1, 4):
         scales = tok * 2 * 4
@@ -62,16 +63,17 @@ def layer_bytes(w, fmt, group, seqs=None):
     q = n * w.Hq * w.D * 2
     tables = int(((L + w.bs - 1) // w.bs).sum()) * 4 + n * 4
     decode = codes + scales + q + tables
-    app_scales = {3: n * w.Hkv * 2 * (w.D // max(group, 1)) * 4, 1: n * 2 * 4, 4: n * 2 * 4}.get(fmt, 0)
-    append = n * w.Hkv * w.D * 2 * 2 + n * 8 + n * w.Hkv * w.D * 2 * es + app_scales
+    app_scales = (n * w.Hkv * 2 * (w.D // max(group, 1)) * 4 if fmt in GROUPED else
+                  {1: n * 2 * 4, 4: n * 2 * 4}.get(fmt, 0))
+    append = n * w.Hkv * w.D * 2 * 2 + n * 8 + int(n * w.Hkv * w.D * 2 * es) + app_scales
     unique_codes = codes
     unique_decode = decode
     if w.shared_prefix_tokens and n > 1:
         # the shared prefix blocks exist once in HBM
         dup = (n - 1) * w.shared_prefix_tokens
-        unique_codes -= dup * w.Hkv * w.D * 2 * es
-        unique_decode -= dup * w.Hkv * w.D * 2 * es
-        if fmt == 3:
+        unique_codes -= int(dup * w.Hkv * w.D * 2 * es)
+        unique_decode -= int(dup * w.Hkv * w.D * 2 * es)
+        if fmt in GROUPED:
             unique_decode -= dup * w.Hkv * 2 * (w.D // group) * 4
         elif fmt in (1, 4):
             unique_decode -= dup * 2 * 4
@@ -453,7 +455,7 @@ def run_ours(args, rank, world, local_rank):
             "context_lens": "%d..%d (mean %.0f)" % (w.context_lens.min(), w.context_lens.max(),
                                                    w.context_lens.mean()),
             "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
-            "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f == 3 else "")
+            "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f in GROUPED else "")
                                  for f, g in w.layer_formats}),
             "pool_blocks_per_layer": w.num_blocks,
             "l2": "inputs larger than L2: %d per-layer pools, %.1f GB"
@@ -609,7 +611,7 @@ def run_prefill(args, rank, world, local_rank):
         "config": {"workload": "%s prefill" % w.name, "layers": L, "prompts": w.S,
                    "prompt_len": int(lens.max()), "q_heads": w.Hq, "kv_heads": w.Hkv,
                    "head_dim": w.D, "block_size": w.bs,
-                   "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f == 3 else "")
+                   "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f in GROUPED else "")
                                         for f, g in w.layer_formats}),
                    "step": "per layer: kvq_append (every prompt token) then kvq_prefill"},
         "prompt_tok_per_s": round(world * T / (ms * 1e-3), 1),

@@ -61,7 +61,10 @@ typedef enum {
     KVQ_INT8_PER_CHANNEL = 2,  /* static fp32 scale per (K|V, kv head, channel)      */
     KVQ_INT8_PER_GROUP = 3,    /* one fp32 scale per `group` contiguous channels of
                                   one (token, kv head, K|V) vector                   */
-    KVQ_FP8_E4M3_PER_TOKEN = 4 /* e4m3 codes, one fp32 scale per (token, K|V)        */
+    KVQ_FP8_E4M3_PER_TOKEN = 4, /* e4m3 codes, one fp32 scale per (token, K|V)       */
+    KVQ_INT4_PER_GROUP = 5     /* 4-bit codes in [-7, 7] ([KVC] §2.3 lists INT4 beside
+                                  INT8/FP8), scale = absmax/7 per `group` channels as
+                                  for KVQ_INT8_PER_GROUP; two codes per byte         */
 } kvq_dtype;
 
 typedef struct kvq_pool kvq_pool; /* opaque; one per layer */
@@ -94,8 +97,8 @@ size_t kvq_pool_bytes(int64_t num_blocks, int block_size, int kv_heads, int head
  *   num_blocks : physical blocks (>= 1)
  *   block_size : tokens per block; a multiple of 16, at most 256
  *   kv_heads   : KV heads (>= 1); head_dim: 64 or 128
- *   group      : channels per scale for KVQ_INT8_PER_GROUP (a multiple of 16
- *                that divides head_dim); ignored for other formats
+ *   group      : channels per scale for KVQ_INT8_PER_GROUP / KVQ_INT4_PER_GROUP
+ *                (a multiple of 16 that divides head_dim); ignored otherwise
  *   device_buf : caller-owned device memory of buf_bytes >= kvq_pool_bytes(..),
  *                256-byte aligned; NULL makes the library cudaMalloc (and later
  *                cudaFree) the pool on the current device.
@@ -129,8 +132,9 @@ kvq_status kvq_calibrate_channel_scales(kvq_pool* pool, const kvq_half* k, const
  *   k, v         : fp16 [T][kv_heads][head_dim]
  *   slot_mapping : int64 [T]; token i goes to block slot/block_size, offset
  *                  slot%block_size.  A negative slot skips the token.
- * Per format: scale s = absmax/127 (INT8 dynamic) or absmax/448 (FP8), fp32
- * IEEE division; code = clamp(round_half_even(x/s), -127, 127) for INT8,
+ * Per format: scale s = absmax/127 (INT8 dynamic), absmax/7 (INT4) or
+ * absmax/448 (FP8), fp32 IEEE division; code = clamp(round_half_even(x/s),
+ * -127, 127) for INT8 (-7, 7 for INT4),
  * e4m3 round-to-nearest-even saturating for FP8; an all-zero group stores s=0
  * and zero codes.  Per-channel uses the pool's static scales.  FP16 stores x.
  * Two tokens with the same slot in one call race (result unspecified).
@@ -288,7 +292,7 @@ kvq_status kvq_paged_decode_noalloc(const kvq_pool* pool, const kvq_half* q, int
 
 /* Read back n slots in a canonical layout (for tests and debugging).
  *   codes_out  : [n][2][kv_heads][head_dim] elements of the pool's code type
- *                (int8, e4m3 byte, or fp16)
+ *                (int8, e4m3 byte, or fp16; INT4 codes come back one per int8)
  *   scales_out : per-group [n][2][kv_heads][head_dim/group] fp32;
  *                per-token [n][2] fp32; may be NULL (and is ignored) for
  *                FP16 and per-channel pools

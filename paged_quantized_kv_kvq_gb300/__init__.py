@@ -28,6 +28,8 @@ KVQ_INT8_PER_TOKEN = 1
 KVQ_INT8_PER_CHANNEL = 2
 KVQ_INT8_PER_GROUP = 3
 KVQ_FP8_E4M3_PER_TOKEN = 4
+KVQ_INT4_PER_GROUP = 5
+GROUP_FORMATS = (KVQ_INT8_PER_GROUP, KVQ_INT4_PER_GROUP)
 
 # kvq_status
 KVQ_OK = 0
@@ -323,7 +325,7 @@ class KVPool:
 
         self.num_blocks, self.block_size, self.kv_heads, self.head_dim = (
             num_blocks, block_size, kv_heads, head_dim)
-        self.dtype, self.group = dtype, (group if dtype == KVQ_INT8_PER_GROUP else 0)
+        self.dtype, self.group = dtype, (group if dtype in GROUP_FORMATS else 0)
         nbytes = kvq_pool_bytes(num_blocks, block_size, kv_heads, head_dim, dtype, self.group)
         if nbytes == 0:
             kvq_pool_layout_query(num_blocks, block_size, kv_heads, head_dim, dtype, self.group)
@@ -401,7 +403,7 @@ class KVPool:
             torch.uint8 if self.dtype == KVQ_FP8_E4M3_PER_TOKEN else torch.int8)
         codes = torch.empty((n, 2, self.kv_heads, self.head_dim), dtype=cdt, device=slots.device)
         scales = None
-        if self.dtype == KVQ_INT8_PER_GROUP:
+        if self.dtype in GROUP_FORMATS:
             scales = torch.empty((n, 2, self.kv_heads, self.head_dim // self.group),
                                  dtype=torch.float32, device=slots.device)
         elif self.dtype in (KVQ_INT8_PER_TOKEN, KVQ_FP8_E4M3_PER_TOKEN):

@@ -23,7 +23,7 @@ namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool valid_dtype(int d) { return d >= KVQ_FP16 && d <= KVQ_FP8_E4M3_PER_TOKEN; }
+bool valid_dtype(int d) { return d >= KVQ_FP16 && d <= KVQ_INT4_PER_GROUP; }
 
 // Geometry check + byte accounting.  Fills `view` offsets relative to base 0.
 kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int group,
@@ -35,7 +35,8 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
   if (bs % 16 != 0 || bs > 256) return KVQ_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
   int ng = 1;
-  if (dtype == KVQ_INT8_PER_GROUP) {
+  const bool grouped = dtype == KVQ_INT8_PER_GROUP || dtype == KVQ_INT4_PER_GROUP;
+  if (grouped) {
     if (group <= 0 || D % group != 0) return KVQ_ERR_INVALID_ARG;
     if (group % 16 != 0) return KVQ_ERR_UNSUPPORTED;
     ng = D / group;
@@ -43,8 +44,10 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
     group = 0;
   }
   const int esize = dtype == KVQ_FP16 ? 2 : 1;
-  const size_t code_bytes = (size_t)bs * D * esize;  // K (or V) codes of one page
-  const size_t page_scale = dtype == KVQ_INT8_PER_GROUP ? 2 * (size_t)bs * ng * 4 : 0;
+  // bytes of one 16-token sub-tile of K (or V) codes: INT4 packs two per byte
+  const int sub_bytes = dtype == KVQ_INT4_PER_GROUP ? 8 * D : 16 * D * esize;
+  const size_t code_bytes = (size_t)bs / 16 * sub_bytes;  // K (or V) codes of one page
+  const size_t page_scale = grouped ? 2 * (size_t)bs * ng * 4 : 0;
   const size_t page_bytes = 2 * code_bytes + page_scale;
   const size_t n_pages = (size_t)num_blocks * Hkv;
   size_t off = kvq::kHeaderBytes;
@@ -59,7 +62,7 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
   off = align_up(off + chan_bytes, 256);
 
   lay->total_bytes = off;
-  lay->code_bytes = 2 * (size_t)num_blocks * bs * Hkv * D * esize;
+  lay->code_bytes = 2 * (size_t)num_blocks * Hkv * code_bytes;
   lay->scale_bytes = n_pages * page_scale + tok_bytes + chan_bytes;
   lay->header_bytes = off - lay->code_bytes - lay->scale_bytes;
   lay->page_bytes = page_bytes;
@@ -72,7 +75,7 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
     view->group = group;
     view->ng = ng;
     view->esize = esize;
-    view->sub_bytes = 16 * D * esize;
+    view->sub_bytes = sub_bytes;
     view->code_bytes = static_cast<int>(code_bytes);
     view->page_bytes = static_cast<int>(page_bytes);
   }
@@ -450,7 +453,8 @@ kvq_status kvq_read_slots(const kvq_pool* pool, const int64_t* slots, int64_t n,
   if (n == 0) return KVQ_OK;
   if (slots == nullptr || codes_out == nullptr || n > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
   const int f = pool->view.fmt;
-  const bool has_scales = f == KVQ_INT8_PER_GROUP || f == KVQ_INT8_PER_TOKEN || f == KVQ_FP8_E4M3_PER_TOKEN;
+  const bool has_scales = f == KVQ_INT8_PER_GROUP || f == KVQ_INT4_PER_GROUP ||
+                          f == KVQ_INT8_PER_TOKEN || f == KVQ_FP8_E4M3_PER_TOKEN;
   return from_cuda(kvq::launch_read_slots(pool->view, slots, n, codes_out,
                                           has_scales ? scales_out : nullptr, stream));
 }

@@ -5,10 +5,11 @@
 // 0539edu.com/news/5800990): each decode step appends the new token's K/V to
 // the cache (§1.1) into fixed-size physical blocks (§2.2); K/V are stored with
 // absmax-symmetric INT8 (per-token, per-channel or per-group-of-128/64 scales)
-// or FP8 (§2.3, §3.3).  Scale = absmax/127 (INT8) or absmax/448 (e4m3) in
-// fp32 with an IEEE division; code = clamp(round_half_even(x / scale), +-127),
-// or e4m3 round-to-nearest-even with saturation; an all-zero group stores
-// scale 0 and zero codes.
+// or FP8 (§2.3, §3.3), or INT4 per group (§2.3 names it beside INT8 and
+// FP8).  Scale = absmax/127 (INT8), absmax/7 (INT4) or absmax/448 (e4m3) in
+// fp32 with an IEEE division; code = clamp(round_half_even(x / scale), +-127)
+// (+-7 for INT4), or e4m3 round-to-nearest-even with saturation; an all-zero
+// group stores scale 0 and zero codes.
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -48,6 +49,22 @@ __device__ __forceinline__ uint8_t quant_i8(float x, float s) {
   float q = rintf(__fdiv_rn(x, s));
   q = fminf(fmaxf(q, -127.f), 127.f);
   return static_cast<uint8_t>(static_cast<int>(q) + 128);
+}
+
+// INT4 code, returned biased (c + 8) as stored in the pool.
+__device__ __forceinline__ uint32_t quant_i4(float x, float s) {
+  if (s == 0.f) return kInt4Bias;
+  float q = rintf(__fdiv_rn(x, s));
+  q = fminf(fmaxf(q, -7.f), 7.f);
+  return static_cast<uint32_t>(static_cast<int>(q) + 8);
+}
+
+// Replace the nibbles under `mask` of a shared 32-bit word: other tokens own
+// the word's other nibbles and may be written by other CTAs at the same time.
+__device__ __forceinline__ void store_nibbles(char* word, uint32_t mask, uint32_t val) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(word);
+  atomicAnd(w, ~mask);
+  atomicOr(w, val);
 }
 
 __device__ __forceinline__ uint8_t quant_e4m3(float x, float s) {
@@ -126,7 +143,45 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
       f[2 * i + 1] = __high2float(xv[i]);
     }
 
-    if constexpr (FMT == FMT_FP16) {
+    if constexpr (FMT == FMT_INT4_GROUP) {
+      // group = g contiguous channels of this head: g/8 consecutive lanes
+      const int lanes = pool.group >> 3;
+      float a = absmax8(xv);
+      for (int o = lanes >> 1; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      const float s = a == 0.f ? 0.f : __fdiv_rn(a, 7.f);
+      uint32_t u[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = quant_i4(f[i], s);
+      if (!act) continue;
+      if ((d0 % pool.group) == 0) {
+        float* sc = reinterpret_cast<float*>(page + 2 * pool.code_bytes) +
+                    (kv * pool.bs + off) * pool.ng + d0 / pool.group;
+        *sc = s;
+      }
+      if (kv == 0) {
+        // channels d0..d0+3 and d0+4..d0+7: four nibbles of one word each
+#pragma unroll
+        for (int hw = 0; hw < 2; ++hw) {
+          uint32_t val = 0, mask = 0;
+          int o = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            int sh;
+            o = k_nibble(tt, d0 + 4 * hw + i, sh);
+            val |= u[4 * hw + i] << sh;
+            mask |= 0xFu << sh;
+          }
+          store_nibbles(tile + o, mask, val);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          int sh;
+          const int o = v_nibble(tt, d0 + i, sh);
+          store_nibbles(tile + o, 0xFu << sh, u[i] << sh);
+        }
+      }
+    } else if constexpr (FMT == FMT_FP16) {
       if (!act) continue;
       const uint16_t* hb = reinterpret_cast<const uint16_t*>(&raw);
       if (kv == 0) {
@@ -219,8 +274,16 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
     const int h = c / D, d = c - h * D;
     const char* page = pool.pages + (blk * pool.Hkv + h) * pool.page_bytes;
     const char* tile = page + (kv == 0 ? 0 : pool.code_bytes) + sub * pool.sub_bytes;
-    const int o = kv == 0 ? k_tile_offset(tt, d, D, es) : v_tile_offset(tt, d, D, es);
     const int64_t dst = (i * 2 + kv) * per + c;
+    if (pool.fmt == FMT_INT4_GROUP) {  // biased nibble -> signed code
+      int sh;
+      const int o = kv == 0 ? k_nibble(tt, d, sh) : v_nibble(tt, d, sh);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + o);
+      reinterpret_cast<int8_t*>(codes_out)[dst] =
+          static_cast<int8_t>(static_cast<int>((w >> sh) & 0xFu) - static_cast<int>(kInt4Bias));
+      continue;
+    }
+    const int o = kv == 0 ? k_tile_offset(tt, d, D, es) : v_tile_offset(tt, d, D, es);
     if (es == 2)
       reinterpret_cast<uint16_t*>(codes_out)[dst] = *reinterpret_cast<const uint16_t*>(tile + o);
     else  // INT8 codes are stored biased; hand back the signed code
@@ -228,7 +291,7 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
           *reinterpret_cast<const uint8_t*>(tile + o) ^ (pool.fmt == FMT_FP8_TOKEN ? 0u : kInt8Bias);
   }
   if (scales_out == nullptr) return;
-  if (pool.fmt == FMT_INT8_GROUP) {
+  if (pool.fmt == FMT_INT8_GROUP || pool.fmt == FMT_INT4_GROUP) {
     const int ns = pool.Hkv * pool.ng;
     for (int c = threadIdx.x; c < ns; c += blockDim.x) {
       const int h = c / pool.ng, gi = c - h * pool.ng;
@@ -278,6 +341,7 @@ cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __ha
     case FMT_INT8_CHANNEL: return launch_append_fmt<FMT_INT8_CHANNEL>(p, grid, st, dependent);
     case FMT_INT8_GROUP: return launch_append_fmt<FMT_INT8_GROUP>(p, grid, st, dependent);
     case FMT_FP8_TOKEN: return launch_append_fmt<FMT_FP8_TOKEN>(p, grid, st, dependent);
+    case FMT_INT4_GROUP: return launch_append_fmt<FMT_INT4_GROUP>(p, grid, st, dependent);
     default: return cudaErrorInvalidValue;
   }
 }

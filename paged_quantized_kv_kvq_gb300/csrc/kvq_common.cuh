@@ -8,7 +8,8 @@
 // exactly the bytes its tensor-core fragments need with 16-byte loads.
 //
 //   header      : 256 B, int32 error word at offset 0
-//   (INT8 codes are stored biased by +128, see kInt8Bias)
+//   (INT8 codes are stored biased by +128, see kInt8Bias; INT4 codes as
+//    nibbles biased by +8, see the INT4 sub-tile layout below)
 //   pages       : [num_blocks][kv_heads] pages of page_bytes each:
 //                   K codes : block_size/16 sub-tiles of 16 tokens x D
 //                   V codes : block_size/16 sub-tiles
@@ -39,6 +40,7 @@ enum Fmt : int {
   FMT_INT8_CHANNEL = 2,
   FMT_INT8_GROUP = 3,
   FMT_FP8_TOKEN = 4,
+  FMT_INT4_GROUP = 5,
 };
 
 enum ErrBits : int {
@@ -70,6 +72,29 @@ __host__ __device__ inline int v_tile_offset(int t, int d, int D, int esize) {
   return (w / wpc) * 512 + lane * 16 + (w % wpc) * 4 * esize + e * esize;
 }
 
+// INT4 sub-tiles hold one 32-bit word per lane per 16-channel step: K word kk
+// of a lane carries channels 16kk + 4j .. +3 of tokens g and g+8 (lane =
+// 4g + j), V word mt carries tokens 2j, 2j+1, 2j+8, 2j+9 of channels 16mt + g
+// and 16mt + g + 8.  Element e of a word is the nibble at bit nib_shift(e),
+// an order in which one mask-and-or yields the fp16 pairs (e0,e1), (e4,e5)
+// and a second, on the word shifted by 4, (e2,e3), (e6,e7).  Words are packed
+// four per 16-byte chunk, chunk c of every lane at c*512 + lane*16.
+__host__ __device__ inline int nib_shift(int e) { return (e & 1) * 16 + (e >> 1) * 4; }
+__host__ __device__ inline int int4_word_offset(int lane, int wi) {
+  return (wi >> 2) * 512 + lane * 16 + (wi & 3) * 4;
+}
+// Byte offset of the word holding element (t, d) of a K sub-tile, and its shift.
+__host__ __device__ inline int k_nibble(int t, int d, int& shift) {
+  shift = nib_shift((t >> 3) * 4 + (d & 3));
+  return int4_word_offset((t & 7) * 4 + ((d & 15) >> 2), d >> 4);
+}
+// Same for a V sub-tile.
+__host__ __device__ inline int v_nibble(int t, int d, int& shift) {
+  shift = nib_shift((t & 1) + 2 * ((t >> 3) & 1) + 4 * ((d >> 3) & 1));
+  return int4_word_offset((d & 7) * 4 + ((t & 7) >> 1), d >> 4);
+}
+constexpr uint32_t kInt4Bias = 8u;
+
 // Plain-old-data view of a pool that kernels receive by value.
 struct PoolView {
   char* pages;
@@ -78,8 +103,8 @@ struct PoolView {
   int* err;
   int64_t num_blocks;
   int bs, Hkv, D, fmt, group, ng, esize;
-  int sub_bytes;    // 16 * D * esize
-  int code_bytes;   // bytes of K (or V) codes in one page = bs * D * esize
+  int sub_bytes;    // bytes of one 16-token sub-tile: 16 * D * esize (INT4: 8 * D)
+  int code_bytes;   // bytes of K (or V) codes in one page = bs * sub_bytes / 16
   int page_bytes;   // 2*code_bytes + (per-group) 2*bs*ng*4
 };
 
@@ -185,6 +210,30 @@ __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_
   const uint16_t wh = static_cast<uint16_t>(w >> 16);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(wl));
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(wh));
+}
+
+// Eight biased INT4 codes (nibbles in the order of nib_shift) -> four fp16x2
+// pairs (e0,e1), (e2,e3), (e4,e5), (e6,e7).  Exact: a low nibble u placed in
+// the mantissa of 1024.0 gives 1024 + u, less 1032 = u - 8; a high nibble
+// (16u) gives 1024 + 16u, times 1/16 less 72 = u - 8 in one rounding-free
+// fused multiply-add.
+__device__ __forceinline__ void i4x8_to_h2x4(uint32_t w, uint32_t& p01, uint32_t& p23,
+                                             uint32_t& p45, uint32_t& p67) {
+  const uint32_t lo = 0x000F000Fu, hi = 0x00F000F0u, magic = 0x64006400u;
+  const uint32_t a = (w & lo) | magic, b = (w & hi) | magic;
+  const uint32_t w8 = w >> 8;
+  const uint32_t c = (w8 & lo) | magic, d = (w8 & hi) | magic;
+  const __half2 sub = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 mul = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+  const __half2 add = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+  __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&a), sub);
+  __half2 r1 = __hfma2(*reinterpret_cast<const __half2*>(&b), mul, add);
+  __half2 r2 = __hsub2(*reinterpret_cast<const __half2*>(&c), sub);
+  __half2 r3 = __hfma2(*reinterpret_cast<const __half2*>(&d), mul, add);
+  p01 = *reinterpret_cast<uint32_t*>(&r0);
+  p23 = *reinterpret_cast<uint32_t*>(&r1);
+  p45 = *reinterpret_cast<uint32_t*>(&r2);
+  p67 = *reinterpret_cast<uint32_t*>(&r3);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

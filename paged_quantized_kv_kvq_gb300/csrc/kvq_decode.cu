@@ -92,6 +92,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   l.dependent = dependent;
   switch (a.pool.fmt) {
     case FMT_INT8_GROUP: return launch_decode_int8_group(l);
+    case FMT_INT4_GROUP: return launch_decode_int4_group(l);
     case FMT_FP16: return launch_decode_fp16(l);
     case FMT_INT8_TOKEN:
     case FMT_FP8_TOKEN: return launch_decode_token(l);

@@ -47,7 +47,7 @@
 namespace kvq {
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 4;     // shared-memory stages per warp (at most)
+constexpr int kDecodeStages = 8;     // shared-memory stages per warp (at most; 80 KB per CTA)
 constexpr int kDecodeCtasPerSm = 3;  // resident CTAs per SM the grid is sized for
 constexpr int kDecodeThreads = kDecodeWarps * 32;
 constexpr int kWaitTries = 4000;   // x 1 ms suspend hint per try: ~4 s upper bound
@@ -109,12 +109,18 @@ __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_
 template <int FMT>
 struct FmtTraits {
   static constexpr bool one_byte = FMT != FMT_FP16;
-  static constexpr bool group_scales = FMT == FMT_INT8_GROUP;
+  static constexpr bool group_scales = FMT == FMT_INT8_GROUP || FMT == FMT_INT4_GROUP;
   static constexpr bool token_scales = FMT == FMT_INT8_TOKEN || FMT == FMT_FP8_TOKEN;
   static constexpr bool row_scales = group_scales || token_scales;  // per-(token[,group]) K/V scales
   static constexpr bool channel = FMT == FMT_INT8_CHANNEL;
   static constexpr bool maybe_nan = FMT == FMT_FP16 || FMT == FMT_FP8_TOKEN;
 };
+
+// 32-bit words a lane holds of one 16-token sub-tile of K (or V).
+template <int FMT, int D>
+__host__ __device__ constexpr int lane_words() {
+  return FMT == FMT_FP16 ? D / 4 : (FMT == FMT_INT4_GROUP ? D / 16 : D / 8);
+}
 
 // Word w (4 elements) of a lane's sub-tile -> (lo, hi) fp16x2 pairs.
 template <int FMT>
@@ -129,11 +135,36 @@ __device__ __forceinline__ void word_to_h2(const uint32_t* words, int w, uint32_
   }
 }
 
-// Copy a lane's share of a sub-tile from shared memory: esize*D/2 bytes.
+// A-fragment words of k-step kk of a K sub-tile (rows = tokens g, g+8; k =
+// channels 16kk + 4j..+3 in the layout's order).
+template <int FMT, int D>
+__device__ __forceinline__ void k_frag(const uint32_t* w, int kk, uint32_t& a0, uint32_t& a1,
+                                       uint32_t& a2, uint32_t& a3) {
+  if constexpr (FMT == FMT_INT4_GROUP) {
+    i4x8_to_h2x4(w[kk], a0, a2, a1, a3);
+  } else {
+    word_to_h2<FMT>(w, kk, a0, a2);           // row g   : channels e=0,1 | e=2,3
+    word_to_h2<FMT>(w, D / 16 + kk, a1, a3);  // row g+8
+  }
+}
+
+// A-fragment words of m-tile mt of a V sub-tile read as V^T (rows = channels
+// 16mt + g, +8; k = tokens 2j, 2j+1 | 2j+8, 2j+9).
+template <int FMT>
+__device__ __forceinline__ void v_frag(const uint32_t* w, int mt, uint32_t& a0, uint32_t& a1,
+                                       uint32_t& a2, uint32_t& a3) {
+  if constexpr (FMT == FMT_INT4_GROUP) {
+    i4x8_to_h2x4(w[mt], a0, a2, a1, a3);
+  } else {
+    word_to_h2<FMT>(w, 2 * mt, a0, a2);      // channel 16mt+g
+    word_to_h2<FMT>(w, 2 * mt + 1, a1, a3);  // channel 16mt+g+8
+  }
+}
+
+// Copy a lane's share of a sub-tile from shared memory (16-byte chunks).
 template <int FMT, int D>
 __device__ __forceinline__ void load_lane_words(const char* tile, int lane, uint32_t* words) {
-  constexpr int esize = FMT == FMT_FP16 ? 2 : 1;
-  constexpr int chunks = D * esize / 32;
+  constexpr int chunks = lane_words<FMT, D>() / 4;
 #pragma unroll
   for (int c = 0; c < chunks; ++c) {
     uint4 v = *reinterpret_cast<const uint4*>(tile + c * 512 + lane * 16);
@@ -156,7 +187,7 @@ struct Cursor {
 template <int FMT, int D, int NG>
 struct PairRegs {
   using T = FmtTraits<FMT>;
-  static constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;
+  static constexpr int NU32 = lane_words<FMT, D>();
   static constexpr int NS = T::group_scales ? NG : 1;
   uint32_t kw[2][NU32];
   float ks[2][2][NS];  // [tile][row g | g+8][group]
@@ -228,8 +259,7 @@ __device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         uint32_t a0, a1, a2, a3;
-        word_to_h2<FMT>(r.kw[t], kk, a0, a2);       // row g   : channels e=0,1 | e=2,3
-        word_to_h2<FMT>(r.kw[t], KS + kk, a1, a3);  // row g+8
+        k_frag<FMT, D>(r.kw[t], kk, a0, a1, a2, a3);
         mma_16816(acc[t][ai], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         if constexpr (T::channel) mma_16816(acc[t][ai], a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
       }
@@ -377,8 +407,7 @@ __device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         uint32_t a0, a1, a2, a3;
-        word_to_h2<FMT>(vwp[t], 2 * mt, a0, a2);      // channel 16mt+g   : tokens 2j,2j+1 | 2j+8,2j+9
-        word_to_h2<FMT>(vwp[t], 2 * mt + 1, a1, a3);  // channel 16mt+g+8
+        v_frag<FMT>(vwp[t], mt, a0, a1, a2, a3);
         mma_16816(o[mt], a0, a1, a2, a3, bh0[t][gi], bh1[t][gi]);
         mma_16816(o[mt], a0, a1, a2, a3, bl0[t][gi], bl1[t][gi]);
       }

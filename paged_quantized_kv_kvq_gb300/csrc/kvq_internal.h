@@ -90,6 +90,7 @@ cudaError_t launch_rows(const RowsArgs& a, const RowsPlan& plan, cudaStream_t st
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;
 cudaError_t launch_decode_int8_group(const DecodeLaunch& l);
+cudaError_t launch_decode_int4_group(const DecodeLaunch& l);
 cudaError_t launch_decode_fp16(const DecodeLaunch& l);
 cudaError_t launch_decode_token(const DecodeLaunch& l);
 cudaError_t launch_decode_channel(const DecodeLaunch& l);

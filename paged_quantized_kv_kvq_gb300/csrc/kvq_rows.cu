@@ -14,7 +14,7 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 template <int FMT>
 cudaError_t run_rows_d(const RowsLaunch& l) {
   const int D = l.p.pool.D, ng = l.p.pool.ng;
-  if constexpr (FMT == FMT_INT8_GROUP) {
+  if constexpr (FMT == FMT_INT8_GROUP || FMT == FMT_INT4_GROUP) {
     if (D == 64) {
       switch (ng) {
         case 1: return run_rows<FMT, 64, 1>(l);
@@ -97,6 +97,7 @@ cudaError_t launch_rows(const RowsArgs& a, const RowsPlan& plan, cudaStream_t st
     case FMT_INT8_CHANNEL: return run_rows_d<FMT_INT8_CHANNEL>(l);
     case FMT_INT8_GROUP: return run_rows_d<FMT_INT8_GROUP>(l);
     case FMT_FP8_TOKEN: return run_rows_d<FMT_FP8_TOKEN>(l);
+    case FMT_INT4_GROUP: return run_rows_d<FMT_INT4_GROUP>(l);
   }
   return cudaErrorInvalidValue;
 }

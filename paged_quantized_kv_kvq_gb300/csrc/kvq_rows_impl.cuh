@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
   using T = FmtTraits<FMT>;
   constexpr int KS = D / 16;  // k-steps of Q.K^T
   constexpr int NW = D / 8;   // 8-channel n-tiles of P.V
-  constexpr int NU32 = (FMT == FMT_FP16 ? 2 : 1) * D / 8;
+  constexpr int NU32 = lane_words<FMT, D>();
   constexpr int KPG = KS / NG;
   constexpr int NS = T::group_scales ? NG : 1;
   constexpr int NB = T::group_scales ? NG : 1;
@@ -307,13 +307,16 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           const int ai = (kk / KPG) * SUB + (SUB == 2 ? (kk & 1) : 0);
+          // k_frag's A-fragment words of token rows g / g+8 are the B
+          // fragments of the n-tiles of tokens 0..7 / 8..15
+          uint32_t b[2][2];
+          k_frag<FMT, D>(kw, kk, b[0][0], b[1][0], b[0][1], b[1][1]);
 #pragma unroll
           for (int n = 0; n < 2; ++n) {
-            uint32_t b0, b1;
-            word_to_h2<FMT>(kw, n * KS + kk, b0, b1);
-            mma_16816(acc[n][ai], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            mma_16816(acc[n][ai], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b[n][0], b[n][1]);
             if constexpr (T::channel)
-              mma_16816(acc[n][ai], qal[kk][0], qal[kk][1], qal[kk][2], qal[kk][3], b0, b1);
+              mma_16816(acc[n][ai], qal[kk][0], qal[kk][1], qal[kk][2], qal[kk][3], b[n][0],
+                        b[n][1]);
           }
         }
 #pragma unroll
@@ -425,13 +428,19 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
             }
           }
         }
+        // v_frag's A-fragment words of channel rows g / g+8 of m-tile mt are
+        // the B fragments of the n-tiles of channels 16mt.. / 16mt+8..
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const int gi = T::group_scales ? (8 * w) / CH : 0;
-          uint32_t b0, b1;
-          word_to_h2<FMT>(vw, w, b0, b1);
-          mma_16816(o[w], ah[gi][0], ah[gi][1], ah[gi][2], ah[gi][3], b0, b1);
-          mma_16816(o[w], alo[gi][0], alo[gi][1], alo[gi][2], alo[gi][3], b0, b1);
+        for (int mt = 0; mt < NW / 2; ++mt) {
+          uint32_t b[2][2];
+          v_frag<FMT>(vw, mt, b[0][0], b[1][0], b[0][1], b[1][1]);
+#pragma unroll
+          for (int n = 0; n < 2; ++n) {
+            const int w = 2 * mt + n;
+            const int gi = T::group_scales ? (8 * w) / CH : 0;
+            mma_16816(o[w], ah[gi][0], ah[gi][1], ah[gi][2], ah[gi][3], b[n][0], b[n][1]);
+            mma_16816(o[w], alo[gi][0], alo[gi][1], alo[gi][2], alo[gi][3], b[n][0], b[n][1]);
+          }
         }
       }
     }

@@ -31,24 +31,28 @@ def test_status_strings(L):
     assert kvq.kvq_status_string(99) == "unknown status"
 
 
-ELEM = {kvq.KVQ_FP16: 2, kvq.KVQ_INT8_PER_TOKEN: 1, kvq.KVQ_INT8_PER_CHANNEL: 1,
-        kvq.KVQ_INT8_PER_GROUP: 1, kvq.KVQ_FP8_E4M3_PER_TOKEN: 1}
+# bytes per element, in halves (INT4 stores two codes per byte)
+HALF_BYTES = {kvq.KVQ_FP16: 4, kvq.KVQ_INT8_PER_TOKEN: 2, kvq.KVQ_INT8_PER_CHANNEL: 2,
+              kvq.KVQ_INT8_PER_GROUP: 2, kvq.KVQ_FP8_E4M3_PER_TOKEN: 2, kvq.KVQ_INT4_PER_GROUP: 1}
 
 
 @pytest.mark.parametrize("dtype,group", [(kvq.KVQ_FP16, 0), (kvq.KVQ_INT8_PER_TOKEN, 0),
                                          (kvq.KVQ_INT8_PER_CHANNEL, 0), (kvq.KVQ_INT8_PER_GROUP, 128),
-                                         (kvq.KVQ_INT8_PER_GROUP, 64), (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0)])
+                                         (kvq.KVQ_INT8_PER_GROUP, 64), (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0),
+                                         (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_INT4_PER_GROUP, 32)])
 @pytest.mark.parametrize("nb,bs,hkv,d", [(9103, 16, 8, 128), (64, 16, 1, 64), (100, 32, 32, 128)])
 def test_code_bytes_follow_formula(L, dtype, group, nb, bs, hkv, d):
-    if dtype == kvq.KVQ_INT8_PER_GROUP and d % group:
+    if dtype in kvq.GROUP_FORMATS and d % group:
         group = d
     lay = kvq.kvq_pool_layout_query(nb, bs, hkv, d, dtype, group)
     tokens = nb * bs  # whole blocks
-    assert lay["code_bytes"] == oracle.kv_cache_bytes(1, tokens, 1, hkv, d, ELEM[dtype])
+    # the size formula with the element size in half bytes, halved
+    assert lay["code_bytes"] == oracle.kv_cache_bytes(1, tokens, 1, hkv, d, HALF_BYTES[dtype]) // 2
     exp_scales = {kvq.KVQ_FP16: 0, kvq.KVQ_INT8_PER_TOKEN: tokens * 2 * 4,
                   kvq.KVQ_FP8_E4M3_PER_TOKEN: tokens * 2 * 4,
                   kvq.KVQ_INT8_PER_CHANNEL: 2 * hkv * d * 4,
-                  kvq.KVQ_INT8_PER_GROUP: tokens * 2 * hkv * (d // max(group, 1)) * 4}[dtype]
+                  kvq.KVQ_INT8_PER_GROUP: tokens * 2 * hkv * (d // max(group, 1)) * 4,
+                  kvq.KVQ_INT4_PER_GROUP: tokens * 2 * hkv * (d // max(group, 1)) * 4}[dtype]
     assert lay["scale_bytes"] == exp_scales
     assert lay["total_bytes"] == kvq.kvq_pool_bytes(nb, bs, hkv, d, dtype, group)
     assert lay["total_bytes"] >= lay["code_bytes"] + lay["scale_bytes"]

@@ -17,7 +17,8 @@ DEV = torch.device("cuda:0")
 
 FORMATS = [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_GROUP, 64), (kvq.KVQ_INT8_PER_GROUP, 32),
            (kvq.KVQ_INT8_PER_GROUP, 16), (kvq.KVQ_INT8_PER_TOKEN, 0), (kvq.KVQ_INT8_PER_CHANNEL, 0),
-           (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0)]
+           (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0), (kvq.KVQ_INT4_PER_GROUP, 128),
+           (kvq.KVQ_INT4_PER_GROUP, 32), (kvq.KVQ_INT4_PER_GROUP, 16)]
 
 
 def _calib(fmt, k, v):
@@ -68,8 +69,11 @@ def test_append_bitexact_and_sentinels(fmt, group, D):
     k, v = x.astype(np.float16)
     slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
     slots[[3, 11, 40]] = -1                             # padding tokens
-    pool = kvq.KVPool(nb, bs, hkv, D, fmt, group, device=DEV, fill_byte=0x5A)
-    ref = oracle.OracleCache(fmt, nb, bs, hkv, D, group, sentinel_code=0x5A)
+    # INT4 pools get a fill whose every nibble is the same (9 = code +1)
+    fill = 0x99 if fmt == kvq.KVQ_INT4_PER_GROUP else 0x5A
+    pool = kvq.KVPool(nb, bs, hkv, D, fmt, group, device=DEV, fill_byte=fill)
+    ref = oracle.OracleCache(fmt, nb, bs, hkv, D, group,
+                             sentinel_code=1 if fmt == kvq.KVQ_INT4_PER_GROUP else fill)
     if fmt == kvq.KVQ_INT8_PER_CHANNEL:
         kvq.kvq_calibrate_channel_scales(pool.handle, torch.from_numpy(k[:50]).to(DEV),
                                          torch.from_numpy(v[:50]).to(DEV))
@@ -83,12 +87,13 @@ def test_append_bitexact_and_sentinels(fmt, group, D):
     # untouched slots still hold the sentinel bytes
     untouched = np.setdiff1d(np.arange(nb * bs), written)
     codes, scales = pool.read_slots(torch.from_numpy(untouched).to(DEV))
-    # the read-back returns signed INT8 codes; the pool stores them biased by 128
-    sentinel = 0x5A ^ 0x80 if fmt in (kvq.KVQ_INT8_PER_TOKEN, kvq.KVQ_INT8_PER_CHANNEL,
-                                      kvq.KVQ_INT8_PER_GROUP) else 0x5A
+    # the read-back returns signed codes; the pool stores INT8 biased by 128
+    # and INT4 nibbles biased by 8
+    sentinel = {kvq.KVQ_INT8_PER_TOKEN: 0x5A ^ 0x80, kvq.KVQ_INT8_PER_CHANNEL: 0x5A ^ 0x80,
+                kvq.KVQ_INT8_PER_GROUP: 0x5A ^ 0x80, kvq.KVQ_INT4_PER_GROUP: 9 - 8}.get(fmt, 0x5A)
     assert np.all(codes.cpu().numpy().view(np.uint8) == sentinel)
     if scales is not None:
-        assert np.all(scales.cpu().numpy().view(np.uint32) == 0x5A5A5A5A)
+        assert np.all(scales.cpu().numpy().view(np.uint32) == fill * 0x01010101)
     pool.close()
 
 
@@ -123,7 +128,7 @@ def test_tiny_workload_full():
     ("mha_100_fp16", dict(S=5, L=300)), ("mha_100_fp8", dict(S=5, L=300)),
     ("mha_100_int8ch", dict(S=5, L=300)), ("mha_100_int8g64", dict(S=5, L=300)),
     ("long_8x32k", dict(S=1, L=3001, bs=16)), ("long_8x32k", dict(S=1, L=3001, bs=32)),
-    ("mixed_256", dict(S=5, L=200, layers=2)),
+    ("mixed_256", dict(S=5, L=200, layers=2)), ("gqa_64x2048_int4", dict(S=3, L=500)),
 ])
 def test_workload_reduced_parity(name, kw):
     w = synth.workload(name, **kw)
