@@ -108,6 +108,25 @@ def read_traffic(workload):
     return rec.get("dram_bytes_per_launch")
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(x, dist, device):
+    """The slowest rank's time: the job ends when its last rank does (every
+    rank reaches this call; no-op for a single process)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job GB/s: every rank processes its own replica of the step (weak
+    scaling), all within the slowest rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -237,6 +256,16 @@ def cpu_baseline(w, budget_s=12.0):
                       "paged decode) run %d times, %.2f s of CPU work, %d algorithmic bytes per run"
                       % (w.layers, n - 1, w.S, reps, dt * reps, nbytes),
             "seconds": dt, "bytes": nbytes}
+
+
+def workload_config(w):
+    return {"workload": w.name, "layers": w.layers, "seqs": w.S,
+            "context_lens": "%d..%d (mean %.0f)" % (w.context_lens.min(), w.context_lens.max(),
+                                                   w.context_lens.mean()),
+            "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
+            "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f in GROUPED else "")
+                                 for f, g in w.layer_formats}),
+            "pool_blocks_per_layer": w.num_blocks}
 
 
 # ----------------------------------------------------------------- our arm
@@ -387,10 +416,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1) / K
     dec_ms = [a.elapsed_time(b) for a, b in evs]
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # -- end to end through the Python API with host buffers
     pin = lambda x: x.cpu().pin_memory()
@@ -424,17 +450,13 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / K2
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / K2, dist, dev)
     for p in pools:
         assert p.error() == kvq.KVQ_OK
 
     b = step_bytes(w)
     step_total = b["decode"] + b["append"]
-    value = world * step_total / (ms * 1e-3) / 1e9
+    value = job_gbs(step_total, world, ms)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
     dec_avg_ms = float(np.mean(dec_ms))
@@ -451,13 +473,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "i8/e4m3 codes x f16 mma -> f32 acc",
         "data": "synthetic (seeded on-device normal draws with the workload's outlier/drift structure)",
         "config": {
-            "workload": w.name, "layers": L, "seqs": w.S,
-            "context_lens": "%d..%d (mean %.0f)" % (w.context_lens.min(), w.context_lens.max(),
-                                                   w.context_lens.mean()),
-            "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D, "block_size": w.bs,
-            "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f in GROUPED else "")
-                                 for f, g in w.layer_formats}),
-            "pool_blocks_per_layer": w.num_blocks,
+            **workload_config(w),
             "l2": "inputs larger than L2: %d per-layer pools, %.1f GB"
                   % (L, sum(p.buffer.numel() for p in pools) / 1e9),
             "step": ("per layer: kvq_%sdecode_step (append 1 token/seq at L-1, then decode)"
@@ -479,7 +495,7 @@ def run_ours(args, rank, world, local_rank):
                                % (KR * L),
                      "bytes_per_launch": round(per_launch), "avg_launch_ms": round(dec_avg_ms, 5),
                      "peak_source": "%s hbm_gbs" % peak_kind},
-        "e2e": {"value": round(world * step_total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_gbs(step_total, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": K2},
         "gpu_launches": K * L * launches_per_layer,
@@ -495,33 +511,30 @@ def run_reference(args):
     from paged_quantized_kv_kvq_gb300 import synth
     import oracle
 
-    import dataclasses
-
     w = synth.workload(args.workload)
     fmt, group = w.layer_formats[0]
     oracle.build()
-    # one step = sequence 0, KV head 0 and its Q heads, of layer 0
-    run = oracle_sample(w, fmt, group, [0], oracle, synth, kv_heads=1)
+    # one step = sequence 0 of layer 0, all its heads
+    run = oracle_sample(w, fmt, group, [0], oracle, synth)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run()
     dt = (time.perf_counter() - t0) / args.steps
-    ws = dataclasses.replace(w, Hkv=1, Hq=w.G)
-    b = layer_bytes(ws, fmt, group, [0])
+    b = layer_bytes(w, fmt, group, [0])
     nbytes = b["decode"] + b["append"]
     v = nbytes / dt / 1e9
-    sample = ("layer 0 of %d, sequence 0 of %d, KV head 0 of %d with its %d Q heads (append of "
-              "the step token + float64 paged decode over %d tokens) per step"
-              % (w.layers, w.S, w.Hkv, w.G, int(w.context_lens[0])))
+    sample = ("layer 0 of %d, sequence 0 of %d with its %d KV / %d Q heads (append of the step "
+              "token + float64 paged decode over %d tokens) per step"
+              % (w.layers, w.S, w.Hkv, w.Hq, int(w.context_lens[0])))
     return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (numpy seeded)",
-            "config": {"workload": w.name},
+            "config": workload_config(w),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s",
-                             "cores": min(oracle.num_threads(), w.G),
+                             "cores": min(oracle.num_threads(), w.Hq),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -574,15 +587,23 @@ def run_prefill(args, rank, world, local_rank):
     for p in pools:
         assert p.error() == kvq.KVQ_OK
     K = args.steps
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
     sampler = ClockSampler(gpu_index(local_rank))
     sampler.start()
     time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
     # the attention kernel alone, per layer, for the roofline
     KR = max(1, min(K, 10))
     evs = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
@@ -594,7 +615,7 @@ def run_prefill(args, rank, world, local_rank):
             evs[i * L + l][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1) / K
+    ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
     att_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
     pairs = int((lens * (lens + 1) // 2).sum())
     flop_layer = 4 * pairs * w.Hq * w.D

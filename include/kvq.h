@@ -290,6 +290,22 @@ kvq_status kvq_paged_decode_noalloc(const kvq_pool* pool, const kvq_half* q, int
                                     int max_context_len, float sm_scale, float* out,
                                     int split_blocks, cudaStream_t stream);
 
+/* Self-test of the bounded pipeline waits (the pages have no counterpart):
+ * kvq_paged_decode with sm_scale 1, except that the first page copy of the
+ * grid's first warp is announced to its barrier but never issued, so that
+ * wait cannot complete.  Every wait of the call gives up after wait_tries
+ * tries of at most ~1 ms (1 <= wait_tries <= 1000); the warp then sets
+ * KVQ_ERR_TIMEOUT in the pool's error word, waits (bounded the same way) for
+ * its other copies in flight and exits.  Nothing hangs or faults and the
+ * context stays usable; kvq_get_error() then returns KVQ_ERR_TIMEOUT.  The
+ * outputs of the units that warp held are unspecified.  Arguments as for
+ * kvq_paged_decode. */
+kvq_status kvq_selftest_decode_timeout(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                                       int num_q_heads, const int32_t* block_table,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, float* out, void* workspace,
+                                       size_t ws_bytes, int wait_tries, cudaStream_t stream);
+
 /* Read back n slots in a canonical layout (for tests and debugging).
  *   codes_out  : [n][2][kv_heads][head_dim] elements of the pool's code type
  *                (int8, e4m3 byte, or fp16; INT4 codes come back one per int8)

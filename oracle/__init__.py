@@ -50,20 +50,48 @@ FORMAT_NAMES = {
 }
 
 
-def build(force: bool = False) -> str:
-    """Compile kvq_oracle.c into liboracle.so (gcc, -O2, no FP contraction,
-    OpenMP when available).  Returns the path of the shared library."""
-    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
-        return _SO
+def compile_source(src: str, so: str) -> str:
+    """Compile one oracle C source into a shared library (gcc, -O2, no FP
+    contraction, OpenMP when available)."""
     base = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-            "-fno-fast-math", _SRC, "-o", _SO + ".tmp", "-lm"]
+            "-fno-fast-math", src, "-o", so + ".tmp", "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
                        capture_output=True, text=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True, text=True)
-    os.replace(_SO + ".tmp", _SO)
-    return _SO
+    os.replace(so + ".tmp", so)
+    return so
+
+
+def build(force: bool = False) -> str:
+    """Compile kvq_oracle.c into liboracle.so.  Returns the library's path."""
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    return compile_source(_SRC, _SO)
+
+
+class use_library:
+    """Context manager: route every oracle call through another build of the
+    oracle (the mutation tests load deliberately broken copies this way)."""
+
+    def __init__(self, so_path: str):
+        self.so_path = so_path
+
+    def __enter__(self):
+        global _lib
+        with _lock:
+            self._saved = _lib
+            L = ctypes.CDLL(self.so_path)
+            _declare(L)
+            _lib = L
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self._saved
+        return False
 
 
 def lib() -> ctypes.CDLL:

@@ -96,6 +96,7 @@ def _declare(L):
         "kvq_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
         "kvq_cascade_workspace_bytes": (sz, [P, i32, i32, i32]),
         "kvq_prefill": (i32, [P, P, i32, i32, P, i32, P, i32, P, i32, f32, P, P]),
+        "kvq_selftest_decode_timeout": (i32, [P, P, i32, i32, P, i32, P, i32, P, P, sz, i32, P]),
         "kvq_cascade_decode": (i32, [P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz, P]),
         "kvq_cascade_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz,
                                           P]),
@@ -280,6 +281,22 @@ def kvq_prefill(pool, q, q_start, max_q_len, block_table, context_lens, max_cont
         int(max_q_len), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
         _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len), float(sm_scale),
         _ptr(out, torch.float32, "out"), _stream(stream)), "kvq_prefill")
+
+
+def kvq_selftest_decode_timeout(pool, q, block_table, context_lens, max_context_len, out,
+                                workspace, wait_tries=20, stream=None) -> None:
+    """Decode with one page copy withheld so that a bounded wait runs out
+    (kvq_selftest_decode_timeout in include/kvq.h)."""
+    import torch
+
+    S, Hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().kvq_selftest_decode_timeout(
+        pool, _ptr(q, torch.float16, "q"), S, Hq, _ptr(block_table, torch.int32, "block_table"),
+        block_table.shape[1], _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len),
+        _ptr(out, torch.float32, "out"),
+        _ptr(workspace, None, "workspace") if workspace is not None else None, ws_bytes,
+        int(wait_tries), _stream(stream)), "kvq_selftest_decode_timeout")
 
 
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -283,6 +283,23 @@ kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_
   return from_cuda(kvq::launch_decode(a, plan, stream));
 }
 
+kvq_status kvq_selftest_decode_timeout(const kvq_pool* pool, const kvq_half* q, int num_seqs,
+                                       int num_q_heads, const int32_t* block_table,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, float* out, void* workspace,
+                                       size_t ws_bytes, int wait_tries, cudaStream_t stream) {
+  if (wait_tries < 1 || wait_tries > 1000) return KVQ_ERR_INVALID_ARG;
+  kvq::DecodeArgs a;
+  kvq::DecodePlan plan;
+  const kvq_status st =
+      prepare_decode(pool, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, context_lens,
+                     max_context_len, 1.0f, out, workspace, ws_bytes, 0, &a, &plan);
+  if (st != KVQ_OK || num_seqs == 0) return st;
+  a.wait_tries = wait_tries;
+  a.fault_issue = 0;  // warp 0's first copy is armed but never issued
+  return from_cuda(kvq::launch_decode(a, plan, stream));
+}
+
 kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
                            const kvq_half* q, int num_seqs, int num_q_heads,
                            const int32_t* block_table, int max_blocks_per_seq,

@@ -49,6 +49,7 @@ enum ErrBits : int {
 };
 
 constexpr int kHeaderBytes = 256;
+constexpr int kWaitTries = 4000;  // bound of a pipeline wait: tries of <= 1 ms each, ~4 s
 constexpr int kMaxDevicesApi = 64;
 
 __host__ __device__ constexpr int fmt_esize(int fmt) { return fmt == FMT_FP16 ? 2 : 1; }

@@ -85,6 +85,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   p.sm_scale_log2 = a.sm_scale * 1.4426950408889634f;
   p.skip = a.skip;
   p.pre = a.pre;
+  p.wait_tries = a.wait_tries;
+  p.fault_issue = a.fault_issue;
   l.grid = dim3(static_cast<unsigned>(plan.grid));
   l.merge_grid = static_cast<unsigned>(plan.merge_grid);
   l.smem = plan.smem_bytes;

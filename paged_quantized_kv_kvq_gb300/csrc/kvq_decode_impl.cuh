@@ -50,7 +50,6 @@ constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 8;     // shared-memory stages per warp (at most; 80 KB per CTA)
 constexpr int kDecodeCtasPerSm = 3;  // resident CTAs per SM the grid is sized for
 constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kWaitTries = 4000;   // x 1 ms suspend hint per try: ~4 s upper bound
 constexpr int kPartRows = 8;       // partial rows per (warp, slot): one per Q head of a tile
 constexpr int kMergeThreads = 128;
 
@@ -70,7 +69,11 @@ struct DecodeParams {
   int skip;
   int S, Hq, G, n_ht, max_blocks, max_ctx;
   int ppw_fixed;       // pages per warp; 0 = balance the pages over all warps
-  int nstage;          // shared-memory stages per warp (2..4)
+  int nstage;          // shared-memory stages per warp
+  int wait_tries;      // bound of every pipeline wait (tries of ~1 ms each)
+  // Self-test of the bounded waits: warp 0 arms the barrier of its copy
+  // number `fault_issue` but issues no copy, so that wait runs out; -1 = off.
+  int fault_issue;
   int stage_bytes;
   int grid;            // decode CTAs (the merge kernel derives the warp ranges from it)
   float sm_scale_log2;  // sm_scale * log2(e)
@@ -618,8 +621,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     char* dst = stages + st * p.stage_bytes;
     const bool ok = phys >= 0 && (int64_t)phys < pool.num_blocks;
     stage_phys[st] = ok ? phys : -1;
-    if (ok) {
-      const int h = ic.lu / p.n_ht;
+    if (ok && p.fault_issue >= 0 && gw == 0 && n_issued == p.fault_issue) {
+      mbar_arrive_expect_tx(&bars[st], page_tx);  // bytes that never come
+    } else if (ok) {
+      const int h = p.n_ht == 1 ? ic.lu : ic.lu / p.n_ht;  // (no division for G <= 8)
       mbar_arrive_expect_tx(&bars[st], page_tx);
       bulk_g2s(dst, pool.pages + ((int64_t)phys * pool.Hkv + h) * pool.page_bytes, pool.page_bytes,
                &bars[st]);
@@ -662,12 +667,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   uint32_t cph = 0;
   auto wait_stage = [&](int st, uint32_t parity) -> bool {
     bool ok = false;
-    for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(&bars[st], parity);
-    if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0) set_error(pool.err, ERR_TIMEOUT);
-      return false;
-    }
-    return true;
+    for (int tries = 0; tries < p.wait_tries && !ok; ++tries) ok = mbar_try_wait(&bars[st], parity);
+    return __all_sync(0xffffffffu, ok);
   };
 
   // ---- per-unit state (heads 2j, 2j+1 of the tile)
@@ -779,6 +780,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   start_unit();
   PairRegs<FMT, D, NG> R;
   int i = 0;
+  bool failed = false;
   while (i < n_w) {
     // pages consumed this step: a pair of one-sub-tile pages of the same unit,
     // or one page of two or more sub-tiles
@@ -786,7 +788,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     const int npg = two ? 2 : 1;
     const bool wrap1 = cst + 1 == nstage;
     const int st0 = cst, st1 = wrap1 ? 0 : cst + 1;
-    if (!wait_stage(st0, cph) || (two && !wait_stage(st1, wrap1 ? cph ^ 1u : cph))) break;
+    if (!wait_stage(st0, cph) || (two && !wait_stage(st1, wrap1 ? cph ^ 1u : cph))) {
+      failed = true;
+      break;
+    }
     auto issue_after = [&]() {
       for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
     };
@@ -826,6 +831,20 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     if (end_pi == done.Ps || i == n_w) {
       finish_unit(done, end_pi);
       if (i < n_w) start_unit();
+    }
+  }
+  if (failed) {
+    // A wait ran out: flag it, then wait (bounded again) for this warp's
+    // copies still in flight so that none lands after the CTA has exited.
+    if (lane == 0) set_error(pool.err, ERR_TIMEOUT);
+    int st = cst;
+    uint32_t ph = cph;
+    for (int k = i; k < n_issued; ++k) {
+      wait_stage(st, ph);
+      if (++st == nstage) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
   }
 }

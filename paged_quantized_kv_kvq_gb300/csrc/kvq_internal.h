@@ -55,6 +55,8 @@ struct DecodeArgs {
   // fold in the prefix partials `pre` ([S][Hq][D+2]); 0 / null otherwise
   int skip = 0;
   const float* pre = nullptr;
+  int wait_tries = kWaitTries;  // bound of each pipeline wait, in ~1 ms tries
+  int fault_issue = -1;   // self-test only: withhold warp 0's copy of this index
 };
 
 // `dependent`: launch the decode as a programmatic dependent of the kernel
