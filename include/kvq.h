@@ -143,6 +143,18 @@ kvq_status kvq_calibrate_channel_scales(kvq_pool* pool, const kvq_half* k, const
 kvq_status kvq_append(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
                       const int64_t* slot_mapping, int64_t T, cudaStream_t stream);
 
+/* Copy whole blocks ([KVC] §4.4: a request that must write into a block it
+ * shares with others first gets its own copy -- copy-on-write).
+ *   src_blocks, dst_blocks : int32 [n]; block dst_blocks[i] becomes a copy of
+ *                            block src_blocks[i]: every kv head's K and V codes,
+ *                            their per-group scales, and (per-token formats)
+ *                            the block's token scales
+ * Pairs run in parallel: a destination must not be another pair's source or
+ * destination.  Device errors: an id outside the pool sets OUT_OF_RANGE and
+ * that pair is skipped. */
+kvq_status kvq_copy_blocks(kvq_pool* pool, const int32_t* src_blocks, const int32_t* dst_blocks,
+                           int n, cudaStream_t stream);
+
 /* Scratch bytes kvq_paged_decode needs for these sizes (split-K partials).
  * May be 0.  Host only. */
 size_t kvq_decode_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,

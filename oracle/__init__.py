@@ -38,6 +38,7 @@ INT8_PER_CHANNEL = 2
 INT8_PER_GROUP = 3
 FP8_E4M3_PER_TOKEN = 4
 INT4_PER_GROUP = 5
+FP8_E5M2 = 6
 GROUP_FORMATS = (INT8_PER_GROUP, INT4_PER_GROUP)
 
 FORMAT_NAMES = {
@@ -47,6 +48,7 @@ FORMAT_NAMES = {
     INT8_PER_GROUP: "int8_group",
     FP8_E4M3_PER_TOKEN: "fp8_e4m3_token",
     INT4_PER_GROUP: "int4_group",
+    FP8_E5M2: "fp8_e5m2",
 }
 
 
@@ -117,6 +119,10 @@ def _declare(L: ctypes.CDLL) -> None:
     L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     L.oracle_e4m3_encode.restype = ctypes.c_uint8
     L.oracle_e4m3_encode.argtypes = [f32]
+    L.oracle_e5m2_decode.restype = f64
+    L.oracle_e5m2_decode.argtypes = [ctypes.c_uint8]
+    L.oracle_e5m2_encode.restype = ctypes.c_uint8
+    L.oracle_e5m2_encode.argtypes = [f32]
     L.oracle_quant_int8_group.restype = None
     L.oracle_quant_int8_group.argtypes = [P, i32, P, P]
     L.oracle_quant_int4_group.restype = None
@@ -163,6 +169,14 @@ def e4m3_decode(code: int) -> float:
 
 def e4m3_encode(x: float) -> int:
     return int(lib().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def e5m2_decode(code: int) -> float:
+    return float(lib().oracle_e5m2_decode(int(code) & 0xFF))
+
+
+def e5m2_encode(x: float) -> int:
+    return int(lib().oracle_e5m2_encode(float(np.float32(x))))
 
 
 def quant_int8_group(x) -> tuple[np.ndarray, np.float32]:
@@ -229,7 +243,7 @@ class OracleCache:
         shape = (self.num_slots, 2, kv_heads, head_dim)
         if fmt == FP16:
             self.codes = np.full(shape, np.float32(sentinel_code), np.float32)
-        elif fmt == FP8_E4M3_PER_TOKEN:
+        elif fmt in (FP8_E4M3_PER_TOKEN, FP8_E5M2):
             self.codes = np.full(shape, sentinel_code & 0xFF, np.uint8)
         else:
             self.codes = np.full(shape, sentinel_code, np.int8)
@@ -261,6 +275,15 @@ class OracleCache:
                             _ptr(slots), _ptr(self.chan_scales), _ptr(self.codes),
                             _ptr(self.scales))
 
+    def copy_blocks(self, src, dst) -> None:
+        """Copy-on-write ("KV Cache优化实战：大模型推理显存占用与加速方案详解" §4.4): block
+        dst[i] takes the codes and scales of every slot of block src[i]."""
+        for s, d in zip(np.asarray(src).ravel(), np.asarray(dst).ravel()):
+            a, b = int(s) * self.bs, int(d) * self.bs
+            self.codes[b:b + self.bs] = self.codes[a:a + self.bs]
+            if self.scales.ndim > 1:
+                self.scales[b:b + self.bs] = self.scales[a:a + self.bs]
+
     def decode(self, q, block_table, context_lens, sm_scale: float | None = None) -> np.ndarray:
         """Float64 attention output [S, Hq, D] over the dequantized cache."""
         q = _f32(q)
@@ -288,6 +311,9 @@ class OracleCache:
         if self.fmt == FP8_E4M3_PER_TOKEN:
             table = np.array([e4m3_decode(i) for i in range(256)], np.float64)
             vals = table[c]
+        elif self.fmt == FP8_E5M2:
+            table = np.array([e5m2_decode(i) for i in range(256)], np.float64)
+            return table[c]
         else:
             vals = c.astype(np.float64)
         if self.fmt in GROUP_FORMATS:

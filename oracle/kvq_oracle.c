@@ -31,6 +31,9 @@
  *       all kv heads; per-group = g contiguous head_dim elements of one
  *       (token, head, K|V) vector; per-channel = a static [2][Hkv][D] scale set
  *       from calibration tokens (absmax / 127 per channel).
+ *   - FP8 e5m2 without a scale, the `fp8_e5m2` KV-cache dtype of [P312] §三:
+ *     code = e5m2 round-to-nearest-even of x itself, saturating to the largest
+ *     finite value (57344); dequantized value = the code's value.
  *   - INT4, listed beside INT8 and FP8 as the more aggressive option ([KVC]
  *     §2.3; [P312] §四 measures it): read as the same absmax symmetric rule
  *     on 4 bits, per group: s = absmax / 7 (fp32), code =
@@ -60,6 +63,7 @@ enum {
     OR_INT8_PER_GROUP = 3,
     OR_FP8_E4M3_PER_TOKEN = 4,
     OR_INT4_PER_GROUP = 5,
+    OR_FP8_E5M2 = 6,
 };
 
 int oracle_num_threads(void) {
@@ -135,6 +139,36 @@ uint8_t oracle_e4m3_encode(float x) {
 /* Quantizers ([KVC] §2.3: absmax symmetric INT8; per-token / per-channel /   */
 /* per-group scales; FP8).  All arithmetic in fp32 as stated in the header.   */
 /* ------------------------------------------------------------------------- */
+
+/* OCP FP8 e5m2: sign, 5 exponent bits (bias 15), 2 mantissa bits; exponent
+ * 31 is infinity (mantissa 0) or NaN.  Value of a code, from the definition. */
+double oracle_e5m2_decode(uint8_t code) {
+    int sign = code >> 7, e = (code >> 2) & 0x1F, m = code & 0x3;
+    double v;
+    if (e == 31) v = m == 0 ? INFINITY : NAN;
+    else if (e == 0) v = ldexp((double)m / 4.0, -14);
+    else v = ldexp(1.0 + (double)m / 4.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Nearest finite e5m2 code by brute force over the non-negative finite codes
+ * (0x00..0x7B), ties to the even mantissa; |x| beyond the largest finite value
+ * saturates to it; the sign is kept (so -0 -> 0x80). */
+uint8_t oracle_e5m2_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    int sign = signbit(x) ? 1 : 0;
+    double a = fabs((double)x);
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7B; ++c) {
+        double d = fabs(oracle_e5m2_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best_d = d;
+            best = (uint8_t)c;
+        }
+    }
+    return (uint8_t)(best | (sign << 7));
+}
 
 /* One dynamic-scale INT8 group of n values. */
 void oracle_quant_int8_group(const float* x, int n, int8_t* codes, float* scale) {
@@ -298,6 +332,11 @@ void oracle_append(int fmt, int64_t T, int Hkv, int D, int g,
                 oracle_quant_e4m3_group(x, per, c, scales + slot * nsc + kv);
                 break;
             }
+            case OR_FP8_E5M2: {
+                uint8_t* c = (uint8_t*)codes + base;
+                for (int i = 0; i < per; ++i) c[i] = oracle_e5m2_encode(x[i]);
+                break;
+            }
             case OR_INT8_PER_CHANNEL: {
                 int8_t* c = (int8_t*)codes + base;
                 oracle_quant_int8_static(x, chan_scales + kv * per, per, c);
@@ -327,6 +366,8 @@ static double dequant(int fmt, int Hkv, int D, int g, const void* codes,
         return (double)((const int8_t*)codes)[idx] * (double)scales[slot * nsc + kv];
     case OR_FP8_E4M3_PER_TOKEN:
         return oracle_e4m3_decode(((const uint8_t*)codes)[idx]) * (double)scales[slot * nsc + kv];
+    case OR_FP8_E5M2:
+        return oracle_e5m2_decode(((const uint8_t*)codes)[idx]);
     case OR_INT8_PER_CHANNEL:
         return (double)((const int8_t*)codes)[idx] *
                (double)chan_scales[(kv * Hkv + h) * D + d];

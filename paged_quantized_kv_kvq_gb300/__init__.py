@@ -88,6 +88,7 @@ def _declare(L):
         "kvq_set_channel_scales": (i32, [P, P, P, P]),
         "kvq_calibrate_channel_scales": (i32, [P, P, P, i64, P]),
         "kvq_append": (i32, [P, P, P, P, i64, P]),
+        "kvq_copy_blocks": (i32, [P, P, P, i32, P]),
         "kvq_decode_workspace_bytes": (sz, [P, i32, i32, i32]),
         "kvq_decode_workspace_bytes_ex": (sz, [P, i32, i32, i32, i32]),
         "kvq_paged_decode": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
@@ -190,6 +191,17 @@ def kvq_append(pool, k, v, slot_mapping, stream=None) -> None:
     _check(lib().kvq_append(pool, _ptr(k, torch.float16, "k"), _ptr(v, torch.float16, "v"),
                             _ptr(slot_mapping, torch.int64, "slot_mapping"), k.shape[0],
                             _stream(stream)), "kvq_append")
+
+
+def kvq_copy_blocks(pool, src_blocks, dst_blocks, stream=None) -> None:
+    """Block dst_blocks[i] becomes a copy of block src_blocks[i] (copy-on-write)."""
+    import torch
+
+    if src_blocks.numel() != dst_blocks.numel():
+        raise ValueError("src_blocks and dst_blocks must have the same length")
+    _check(lib().kvq_copy_blocks(pool, _ptr(src_blocks, torch.int32, "src_blocks"),
+                                 _ptr(dst_blocks, torch.int32, "dst_blocks"), src_blocks.numel(),
+                                 _stream(stream)), "kvq_copy_blocks")
 
 
 def kvq_decode_workspace_bytes(pool, num_seqs, num_q_heads, max_context_len, split_blocks=0) -> int:

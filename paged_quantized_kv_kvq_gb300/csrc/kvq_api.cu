@@ -210,6 +210,14 @@ kvq_status kvq_append(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
                                       reinterpret_cast<const __half*>(v), slot_mapping, T, stream));
 }
 
+kvq_status kvq_copy_blocks(kvq_pool* pool, const int32_t* src_blocks, const int32_t* dst_blocks,
+                           int n, cudaStream_t stream) {
+  if (pool == nullptr || n < 0) return KVQ_ERR_INVALID_ARG;
+  if (n == 0) return KVQ_OK;
+  if (src_blocks == nullptr || dst_blocks == nullptr || n > 0x7fffffff) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(kvq::launch_copy_blocks(pool->view, src_blocks, dst_blocks, n, stream));
+}
+
 size_t kvq_decode_workspace_bytes_ex(const kvq_pool* pool, int num_seqs, int num_q_heads,
                                      int max_context_len, int split_blocks) {
   if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || num_q_heads % pool->view.Hkv != 0)

@@ -304,7 +304,32 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
   }
 }
 
+// Copy-on-write: block dst[i] becomes a copy of block src[i] -- every kv
+// head's page (codes and group scales) and, per-token formats, the block's
+// token scales.  One CTA per (pair, kv head), 16-byte vector copies.
+__global__ void kvq_copy_blocks_kernel(PoolView pool, const int* src, const int* dst, int n) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int s = src[i], d = dst[i];
+  if (s < 0 || d < 0 || (int64_t)s >= pool.num_blocks || (int64_t)d >= pool.num_blocks) {
+    if (h == 0 && threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
+    return;
+  }
+  const uint4* from = reinterpret_cast<const uint4*>(pool.pages + ((int64_t)s * pool.Hkv + h) * pool.page_bytes);
+  uint4* to = reinterpret_cast<uint4*>(pool.pages + ((int64_t)d * pool.Hkv + h) * pool.page_bytes);
+  for (int k = threadIdx.x; k < pool.page_bytes / 16; k += blockDim.x) to[k] = from[k];
+  if (h == 0 && (pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN))
+    for (int k = threadIdx.x; k < 2 * pool.bs; k += blockDim.x)
+      pool.tok_scales[(int64_t)d * 2 * pool.bs + k] = pool.tok_scales[(int64_t)s * 2 * pool.bs + k];
+}
+
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_copy_blocks(const PoolView& pool, const int* src, const int* dst, int n,
+                               cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  kvq_copy_blocks_kernel<<<dim3(static_cast<unsigned>(n), pool.Hkv), 128, 0, st>>>(pool, src, dst, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
                           const int64_t* slots, int64_t T, cudaStream_t st) {
   return launch_step_append(pool, k, v, slots, T, nullptr, nullptr, 0, 0, st, false);

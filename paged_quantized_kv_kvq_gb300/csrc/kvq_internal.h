@@ -19,6 +19,8 @@ cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v
 cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
                                const int64_t* slots, int64_t T, const int* table, const int* lens,
                                int max_blocks, int max_ctx, cudaStream_t st, bool dependent);
+cudaError_t launch_copy_blocks(const PoolView& pool, const int* src, const int* dst, int n,
+                               cudaStream_t st);
 cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,
                              cudaStream_t st);
 cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_t n,

@@ -270,3 +270,36 @@ def test_host_validation():
         kvq.kvq_append(pool.handle, q[:, :8].float(), q[:, :8].float(),
                        torch.zeros(2, dtype=torch.int64, device=DEV))
     pool.close()
+
+
+@pytest.mark.parametrize("fmt,group", [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_TOKEN, 0),
+                                       (kvq.KVQ_FP16, 0), (kvq.KVQ_INT4_PER_GROUP, 32),
+                                       (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0)])
+def test_copy_blocks_copy_on_write(fmt, group):
+    w = synth.workload("gqa_64x2048", S=3, L=200, layers=1)
+    w.layer_formats = [(fmt, group)]
+    pool, ref, table, (k, v, slots) = _layer_case(w, 0, fmt, group)
+    used = set(np.unique(w.block_table[w.block_table >= 0]).tolist())
+    free = np.array([b for b in range(w.num_blocks) if b not in used][:5], np.int32)
+    src = w.block_table[1, :5].astype(np.int32)
+    q = synth.queries(w, 0)
+    before = run_gpu_decode(pool, w, q, DEV)
+    kvq.kvq_copy_blocks(pool.handle, torch.from_numpy(src).to(DEV), torch.from_numpy(free).to(DEV))
+    assert pool.error() == kvq.KVQ_OK
+    # the copies hold exactly the source blocks' codes and scales
+    s_slots = (src[:, None].astype(np.int64) * w.bs + np.arange(w.bs)).ravel()
+    d_slots = (free[:, None].astype(np.int64) * w.bs + np.arange(w.bs)).ravel()
+    cs, ss = pool.read_slots(torch.from_numpy(s_slots).to(DEV))
+    cd, sd = pool.read_slots(torch.from_numpy(d_slots).to(DEV))
+    np.testing.assert_array_equal(cd.cpu().numpy(), cs.cpu().numpy())
+    if ss is not None:
+        np.testing.assert_array_equal(sd.cpu().numpy().view(np.uint32), ss.cpu().numpy().view(np.uint32))
+    # a table that reads the copies decodes to the same bits
+    t2 = w.block_table.copy()
+    t2[1, :5] = free
+    np.testing.assert_array_equal(run_gpu_decode(pool, w, q, DEV, table=t2), before)
+    # out-of-pool ids are flagged and skipped
+    bad = torch.tensor([w.num_blocks + 3], dtype=torch.int32, device=DEV)
+    kvq.kvq_copy_blocks(pool.handle, bad, torch.tensor([int(free[0])], dtype=torch.int32, device=DEV))
+    assert pool.error() == kvq.KVQ_ERR_OUT_OF_RANGE
+    pool.close()

@@ -25,8 +25,14 @@ MUTATIONS = [
     ("int4 scale constant 7 -> 8", "float s = a / 7.0f;", "float s = a / 8.0f;",
      [lambda: [pins.test_int4_closed_form(i) for i in range(len(pins._golden_int4()))],
       pins.test_int4_error_bound_and_range]),
-    ("e4m3 ties to odd", "(d == best_d && (c & 1) == 0)", "(d == best_d && (c & 1) == 1)",
+    ("e4m3 ties to odd",
+     "oracle_e4m3_decode((uint8_t)c) - a);\n            if (d < best_d || (d == best_d && (c & 1) == 0))",
+     "oracle_e4m3_decode((uint8_t)c) - a);\n            if (d < best_d || (d == best_d && (c & 1) == 1))",
      [pins.test_e4m3_exhaustive_roundtrip_and_even_ties, pins.test_e4m3_matches_torch_cast]),
+    ("e5m2 exponent bias 15 -> 16", "else v = ldexp(1.0 + (double)m / 4.0, e - 15);",
+     "else v = ldexp(1.0 + (double)m / 4.0, e - 16);",
+     [lambda: [pins.test_e5m2_golden(x, c) for x, c in pins._golden_e5m2()],
+      pins.test_e5m2_exhaustive_roundtrip_and_even_ties]),
     ("decode drops the softmax scale", "z[t] = sm_scale * acc;", "z[t] = acc;",
      [lambda: pins.test_decode_matches_dense_bruteforce(oracle.INT8_PER_GROUP, 16)]),
     ("decode maps Q heads to KV heads modulo (interleaved groups)", "int h = hq / G;",

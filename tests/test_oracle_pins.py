@@ -150,6 +150,48 @@ def test_e4m3_matches_torch_cast():
     np.testing.assert_array_equal(ours, ref)
 
 
+def _golden_e5m2():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "e5m2_cases.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        x, c = (p.strip() for p in line.split("|"))
+        rows.append((float(x), int(c, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("value,code", _golden_e5m2())
+def test_e5m2_golden(value, code):
+    assert oracle.e5m2_encode(value) == code
+
+
+def test_e5m2_exhaustive_roundtrip_and_even_ties():
+    finite = [c for c in range(256) if ((c >> 2) & 0x1F) != 0x1F]
+    vals = {c: oracle.e5m2_decode(c) for c in finite}
+    for c in finite:
+        assert oracle.e5m2_encode(vals[c]) == c
+    assert np.isinf(oracle.e5m2_decode(0x7C)) and np.isnan(oracle.e5m2_decode(0x7D))
+    for c in range(0, 0x7B):
+        mid = (vals[c] + vals[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e5m2_encode(mid) == even
+        assert oracle.e5m2_encode(-mid) == even | 0x80
+    # an e5m2 code is the top byte of the fp16 with the same value
+    for c in finite:
+        assert np.array([c << 8], np.uint16).view(np.float16)[0] == np.float16(vals[c])
+
+
+def test_e5m2_matches_torch_cast():
+    # library cross-check: torch's CPU float8_e5m2 cast on in-range values
+    rng = np.random.default_rng(6)
+    x = np.concatenate([rng.standard_normal(4000) * 50, rng.standard_normal(2000) * 1e-3,
+                        rng.uniform(-57344, 57344, 2000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    ours = np.array([oracle.e5m2_encode(v) for v in x], np.uint8)
+    np.testing.assert_array_equal(ours, ref)
+
+
 def test_e4m3_group_scale():
     c, s = oracle.quant_e4m3_group(np.array([448, 1, -224, 0.5], np.float32))
     assert s == 1.0
@@ -181,7 +223,7 @@ def test_kv_size_formula_brute_force(dims):
 # ---------------------------------------------------------------- append
 FORMATS = [(oracle.INT8_PER_GROUP, 16), (oracle.INT8_PER_GROUP, 32), (oracle.INT8_PER_TOKEN, 0),
            (oracle.INT8_PER_CHANNEL, 0), (oracle.FP8_E4M3_PER_TOKEN, 0), (oracle.FP16, 0),
-           (oracle.INT4_PER_GROUP, 16), (oracle.INT4_PER_GROUP, 32)]
+           (oracle.INT4_PER_GROUP, 16), (oracle.INT4_PER_GROUP, 32), (oracle.FP8_E5M2, 0)]
 
 
 def _cache(fmt, g, nb=8, bs=4, hkv=2, d=32, **kw):
@@ -225,6 +267,9 @@ def test_append_places_slots_and_keeps_sentinels(fmt, g):
                 cc, s = oracle.quant_e4m3_group(x[t])
                 np.testing.assert_array_equal(c.codes[slot, kv].ravel(), cc)
                 assert c.scales[slot, kv] == s
+            elif fmt == oracle.FP8_E5M2:
+                cc = [oracle.e5m2_encode(val) for val in x[t].ravel()]
+                np.testing.assert_array_equal(c.codes[slot, kv].ravel(), cc)
             else:
                 cc = oracle.quant_int8_static(x[t], c.chan_scales[kv])
                 np.testing.assert_array_equal(c.codes[slot, kv].ravel(), cc)
@@ -395,3 +440,20 @@ def test_fp16_layer_equals_plain_attention():
             qq = torch.from_numpy(q[s, hq].astype(np.float64))
             ref = torch.softmax(K[:, hq // 2] @ qq / np.sqrt(32), 0) @ V[:, hq // 2]
             np.testing.assert_allclose(got[s, hq], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_copy_blocks_then_remap_gives_identical_decode():
+    # copy-on-write: after copying blocks, a table that reads the copies gives
+    # the same output bit for bit, and the copies hold the source's codes
+    c, q, table, lens = _filled(oracle.INT8_PER_GROUP, 16, seed=9, nb=40)
+    used = set(np.unique(table).tolist())
+    free = [b for b in range(c.num_slots // c.bs) if b not in used][:3]
+    src = table[2, :3].copy()
+    before = c.decode(q, table, lens)
+    c.copy_blocks(src, free)
+    for s, d in zip(src, free):
+        np.testing.assert_array_equal(c.codes[d * c.bs:(d + 1) * c.bs], c.codes[s * c.bs:(s + 1) * c.bs])
+        np.testing.assert_array_equal(c.scales[d * c.bs:(d + 1) * c.bs], c.scales[s * c.bs:(s + 1) * c.bs])
+    t2 = table.copy()
+    t2[2, :3] = free
+    np.testing.assert_array_equal(c.decode(q, t2, lens), before)
