@@ -34,8 +34,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Paged quantized-KV decode: effective HBM GB/s (% of peak) and decode tok/s"
 FORMAT_NAME = {0: "fp16", 1: "int8 per-token", 2: "int8 per-channel", 3: "int8 per-group",
-               4: "fp8 e4m3 per-token", 5: "int4 per-group"}
-ESIZE = {0: 2, 1: 1, 2: 1, 3: 1, 4: 1, 5: 0.5}  # bytes per code
+               4: "fp8 e4m3 per-token", 5: "int4 per-group", 6: "fp8 e5m2 (no scale)"}
+ESIZE = {0: 2, 1: 1, 2: 1, 3: 1, 4: 1, 5: 0.5, 6: 1}  # bytes per code
 GROUPED = (3, 5)
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_traffic.json")
 KERNEL_SOURCES = ["paged_quantized_kv_kvq_gb300/csrc/kvq_decode_impl.cuh",

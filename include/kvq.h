@@ -62,9 +62,11 @@ typedef enum {
     KVQ_INT8_PER_GROUP = 3,    /* one fp32 scale per `group` contiguous channels of
                                   one (token, kv head, K|V) vector                   */
     KVQ_FP8_E4M3_PER_TOKEN = 4, /* e4m3 codes, one fp32 scale per (token, K|V)       */
-    KVQ_INT4_PER_GROUP = 5     /* 4-bit codes in [-7, 7] ([KVC] §2.3 lists INT4 beside
+    KVQ_INT4_PER_GROUP = 5,    /* 4-bit codes in [-7, 7] ([KVC] §2.3 lists INT4 beside
                                   INT8/FP8), scale = absmax/7 per `group` channels as
                                   for KVQ_INT8_PER_GROUP; two codes per byte         */
+    KVQ_FP8_E5M2 = 6           /* e5m2 codes of the values themselves, no scale
+                                  ([P312] §三: kv_cache_dtype fp8_e5m2); saturating  */
 } kvq_dtype;
 
 typedef struct kvq_pool kvq_pool; /* opaque; one per layer */
@@ -133,8 +135,9 @@ kvq_status kvq_calibrate_channel_scales(kvq_pool* pool, const kvq_half* k, const
  *   slot_mapping : int64 [T]; token i goes to block slot/block_size, offset
  *                  slot%block_size.  A negative slot skips the token.
  * Per format: scale s = absmax/127 (INT8 dynamic), absmax/7 (INT4) or
- * absmax/448 (FP8), fp32 IEEE division; code = clamp(round_half_even(x/s),
- * -127, 127) for INT8 (-7, 7 for INT4),
+ * absmax/448 (FP8 e4m3), fp32 IEEE division; code = clamp(round_half_even(x/s),
+ * -127, 127) for INT8 (-7, 7 for INT4), e5m2 round-to-nearest-even of x
+ * itself saturating at 57344 for KVQ_FP8_E5M2,
  * e4m3 round-to-nearest-even saturating for FP8; an all-zero group stores s=0
  * and zero codes.  Per-channel uses the pool's static scales.  FP16 stores x.
  * Two tokens with the same slot in one call race (result unspecified).

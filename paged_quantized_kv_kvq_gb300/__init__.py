@@ -29,6 +29,7 @@ KVQ_INT8_PER_CHANNEL = 2
 KVQ_INT8_PER_GROUP = 3
 KVQ_FP8_E4M3_PER_TOKEN = 4
 KVQ_INT4_PER_GROUP = 5
+KVQ_FP8_E5M2 = 6
 GROUP_FORMATS = (KVQ_INT8_PER_GROUP, KVQ_INT4_PER_GROUP)
 
 # kvq_status
@@ -429,7 +430,7 @@ class KVPool:
 
         n = slots.numel()
         cdt = torch.float16 if self.dtype == KVQ_FP16 else (
-            torch.uint8 if self.dtype == KVQ_FP8_E4M3_PER_TOKEN else torch.int8)
+            torch.uint8 if self.dtype in (KVQ_FP8_E4M3_PER_TOKEN, KVQ_FP8_E5M2) else torch.int8)
         codes = torch.empty((n, 2, self.kv_heads, self.head_dim), dtype=cdt, device=slots.device)
         scales = None
         if self.dtype in GROUP_FORMATS:

@@ -23,7 +23,7 @@ namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool valid_dtype(int d) { return d >= KVQ_FP16 && d <= KVQ_INT4_PER_GROUP; }
+bool valid_dtype(int d) { return d >= KVQ_FP16 && d <= KVQ_FP8_E5M2; }
 
 // Geometry check + byte accounting.  Fills `view` offsets relative to base 0.
 kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int group,

@@ -5,7 +5,8 @@
 // 0539edu.com/news/5800990): each decode step appends the new token's K/V to
 // the cache (§1.1) into fixed-size physical blocks (§2.2); K/V are stored with
 // absmax-symmetric INT8 (per-token, per-channel or per-group-of-128/64 scales)
-// or FP8 (§2.3, §3.3), or INT4 per group (§2.3 names it beside INT8 and
+// or FP8 (§2.3, §3.3; e5m2 without a scale, the fp8_e5m2 KV dtype of
+// xpshop.cn article-312 §三), or INT4 per group (§2.3 names it beside INT8 and
 // FP8).  Scale = absmax/127 (INT8), absmax/7 (INT4) or absmax/448 (e4m3) in
 // fp32 with an IEEE division; code = clamp(round_half_even(x / scale), +-127)
 // (+-7 for INT4), or e4m3 round-to-nearest-even with saturation; an all-zero
@@ -214,6 +215,10 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
       } else if constexpr (FMT == FMT_FP8_TOKEN) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) code[i] = quant_e4m3(f[i], tok_scale);
+      } else if constexpr (FMT == FMT_FP8_E5M2) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          code[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(f[i], __NV_SATFINITE, __NV_E5M2));
       } else {  // FMT_INT8_CHANNEL
         const float* cs = pool.chan_scales + ((int64_t)kv * Hkv + h) * D + d0;
 #pragma unroll
@@ -288,7 +293,8 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
       reinterpret_cast<uint16_t*>(codes_out)[dst] = *reinterpret_cast<const uint16_t*>(tile + o);
     else  // INT8 codes are stored biased; hand back the signed code
       reinterpret_cast<uint8_t*>(codes_out)[dst] =
-          *reinterpret_cast<const uint8_t*>(tile + o) ^ (pool.fmt == FMT_FP8_TOKEN ? 0u : kInt8Bias);
+          *reinterpret_cast<const uint8_t*>(tile + o) ^
+          (pool.fmt == FMT_FP8_TOKEN || pool.fmt == FMT_FP8_E5M2 ? 0u : kInt8Bias);
   }
   if (scales_out == nullptr) return;
   if (pool.fmt == FMT_INT8_GROUP || pool.fmt == FMT_INT4_GROUP) {
@@ -367,6 +373,7 @@ cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __ha
     case FMT_INT8_GROUP: return launch_append_fmt<FMT_INT8_GROUP>(p, grid, st, dependent);
     case FMT_FP8_TOKEN: return launch_append_fmt<FMT_FP8_TOKEN>(p, grid, st, dependent);
     case FMT_INT4_GROUP: return launch_append_fmt<FMT_INT4_GROUP>(p, grid, st, dependent);
+    case FMT_FP8_E5M2: return launch_append_fmt<FMT_FP8_E5M2>(p, grid, st, dependent);
     default: return cudaErrorInvalidValue;
   }
 }

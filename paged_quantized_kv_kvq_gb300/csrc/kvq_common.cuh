@@ -41,6 +41,7 @@ enum Fmt : int {
   FMT_INT8_GROUP = 3,
   FMT_FP8_TOKEN = 4,
   FMT_INT4_GROUP = 5,
+  FMT_FP8_E5M2 = 6,
 };
 
 enum ErrBits : int {
@@ -203,6 +204,13 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t u, uint32_t& lo, uint32_t&
   __half2 hf = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
   lo = *reinterpret_cast<uint32_t*>(&lf);
   hi = *reinterpret_cast<uint32_t*>(&hf);
+}
+
+// Four e5m2 codes -> two fp16x2.  An e5m2 code is the top byte of the fp16
+// with the same value, so each byte only moves up: (c0,c1), (c2,c3).
+__device__ __forceinline__ void e5m2x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = prmt(w, 0u, 0x1404u);
+  hi = prmt(w, 0u, 0x3424u);
 }
 
 // Four e4m3 codes -> two fp16x2 (exact: every e4m3 value is an fp16 value).

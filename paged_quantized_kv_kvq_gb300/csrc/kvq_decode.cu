@@ -99,6 +99,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
     case FMT_INT8_TOKEN:
     case FMT_FP8_TOKEN: return launch_decode_token(l);
     case FMT_INT8_CHANNEL: return launch_decode_channel(l);
+    case FMT_FP8_E5M2: return launch_decode_e5m2(l);
   }
   return cudaErrorInvalidValue;
 }

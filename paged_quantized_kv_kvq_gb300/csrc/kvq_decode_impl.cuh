@@ -116,7 +116,7 @@ struct FmtTraits {
   static constexpr bool token_scales = FMT == FMT_INT8_TOKEN || FMT == FMT_FP8_TOKEN;
   static constexpr bool row_scales = group_scales || token_scales;  // per-(token[,group]) K/V scales
   static constexpr bool channel = FMT == FMT_INT8_CHANNEL;
-  static constexpr bool maybe_nan = FMT == FMT_FP16 || FMT == FMT_FP8_TOKEN;
+  static constexpr bool maybe_nan = FMT == FMT_FP16 || FMT == FMT_FP8_TOKEN || FMT == FMT_FP8_E5M2;
 };
 
 // 32-bit words a lane holds of one 16-token sub-tile of K (or V).
@@ -133,6 +133,8 @@ __device__ __forceinline__ void word_to_h2(const uint32_t* words, int w, uint32_
     hi = words[2 * w + 1];
   } else if constexpr (FMT == FMT_FP8_TOKEN) {
     e4m3x4_to_h2x2(words[w], lo, hi);
+  } else if constexpr (FMT == FMT_FP8_E5M2) {
+    e5m2x4_to_h2x2(words[w], lo, hi);
   } else {
     i8x4_to_h2x2(words[w], lo, hi);
   }

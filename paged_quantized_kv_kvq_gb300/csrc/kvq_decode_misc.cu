@@ -14,4 +14,6 @@ cudaError_t launch_decode_token(const DecodeLaunch& l) {
 
 cudaError_t launch_decode_channel(const DecodeLaunch& l) { return run_decode_d<FMT_INT8_CHANNEL>(l); }
 
+cudaError_t launch_decode_e5m2(const DecodeLaunch& l) { return run_decode_d<FMT_FP8_E5M2>(l); }
+
 }  // namespace kvq

@@ -98,5 +98,6 @@ cudaError_t launch_decode_int4_group(const DecodeLaunch& l);
 cudaError_t launch_decode_fp16(const DecodeLaunch& l);
 cudaError_t launch_decode_token(const DecodeLaunch& l);
 cudaError_t launch_decode_channel(const DecodeLaunch& l);
+cudaError_t launch_decode_e5m2(const DecodeLaunch& l);
 
 }  // namespace kvq

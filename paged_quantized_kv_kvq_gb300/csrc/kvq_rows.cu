@@ -98,6 +98,7 @@ cudaError_t launch_rows(const RowsArgs& a, const RowsPlan& plan, cudaStream_t st
     case FMT_INT8_GROUP: return run_rows_d<FMT_INT8_GROUP>(l);
     case FMT_FP8_TOKEN: return run_rows_d<FMT_FP8_TOKEN>(l);
     case FMT_INT4_GROUP: return run_rows_d<FMT_INT4_GROUP>(l);
+    case FMT_FP8_E5M2: return run_rows_d<FMT_FP8_E5M2>(l);
   }
   return cudaErrorInvalidValue;
 }

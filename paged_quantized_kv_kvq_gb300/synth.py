@@ -26,6 +26,7 @@ INT8_PER_CHANNEL = 2
 INT8_PER_GROUP = 3
 FP8_E4M3_PER_TOKEN = 4
 INT4_PER_GROUP = 5
+FP8_E5M2 = 6
 
 
 @dataclasses.dataclass
@@ -131,11 +132,11 @@ def workload(name: str, *, S: int | None = None, L: int | None = None,
         table = _table_from_lens(rng, lens, bsz, nb)
         return Workload("tiny", layers or 1, len(lens), 4, 1, 64, bsz, nb, lens, table,
                         [(INT8_PER_GROUP, 64)], _outliers(rng, 1, 64, 2), 20.0, 0.0, sd)
-    if name in ("gqa_64x2048", "gqa_64x2048_int4"):
+    if name in ("gqa_64x2048", "gqa_64x2048_int4", "gqa_64x2048_e5m2"):
         # 32 layers, 64 x 2048, 32 Q / 8 KV heads, head_dim 128, block 16,
-        # INT8 per-group 128 (the _int4 variant: INT4 per-group 128), pool =
-        # 90% of the needed blocks + 10% headroom, N(0,1) with 1% of the Hkv*D
-        # channels x10.
+        # INT8 per-group 128 (variants: _int4 INT4 per-group 128, _e5m2
+        # unscaled FP8 e5m2), pool = 90% of the needed blocks + 10% headroom,
+        # N(0,1) with 1% of the Hkv*D channels x10.
         sd = 1 if seed is None else seed
         rng = np.random.default_rng(sd)
         Sx, Lx, bsz = S or 64, L or 2048, bs or 16
@@ -143,9 +144,10 @@ def workload(name: str, *, S: int | None = None, L: int | None = None,
         need = Sx * ((Lx + bsz - 1) // bsz)
         nb = math.ceil(need / 0.9)
         table = _table_from_lens(rng, lens, bsz, nb)
-        fmt = INT4_PER_GROUP if name.endswith("_int4") else INT8_PER_GROUP
+        fmt = {"int4": (INT4_PER_GROUP, 128), "e5m2": (FP8_E5M2, 0)}.get(
+            name.rsplit("_", 1)[1], (INT8_PER_GROUP, 128))
         return Workload(name, layers or 32, Sx, 32, 8, 128, bsz, nb, lens, table,
-                        [(fmt, 128)] * (layers or 32),
+                        [fmt] * (layers or 32),
                         _outliers(rng, 8, 128, max(1, round(0.01 * 8 * 128))), 10.0, 0.0, sd)
     if name.startswith("mha_100"):
         # 32 layers, 100 sequences with lengths uniform in [256, 2048], MHA 32/32,

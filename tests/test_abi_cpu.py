@@ -33,13 +33,15 @@ def test_status_strings(L):
 
 # bytes per element, in halves (INT4 stores two codes per byte)
 HALF_BYTES = {kvq.KVQ_FP16: 4, kvq.KVQ_INT8_PER_TOKEN: 2, kvq.KVQ_INT8_PER_CHANNEL: 2,
-              kvq.KVQ_INT8_PER_GROUP: 2, kvq.KVQ_FP8_E4M3_PER_TOKEN: 2, kvq.KVQ_INT4_PER_GROUP: 1}
+              kvq.KVQ_INT8_PER_GROUP: 2, kvq.KVQ_FP8_E4M3_PER_TOKEN: 2, kvq.KVQ_INT4_PER_GROUP: 1,
+              kvq.KVQ_FP8_E5M2: 2}
 
 
 @pytest.mark.parametrize("dtype,group", [(kvq.KVQ_FP16, 0), (kvq.KVQ_INT8_PER_TOKEN, 0),
                                          (kvq.KVQ_INT8_PER_CHANNEL, 0), (kvq.KVQ_INT8_PER_GROUP, 128),
                                          (kvq.KVQ_INT8_PER_GROUP, 64), (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0),
-                                         (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_INT4_PER_GROUP, 32)])
+                                         (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_INT4_PER_GROUP, 32),
+                                         (kvq.KVQ_FP8_E5M2, 0)])
 @pytest.mark.parametrize("nb,bs,hkv,d", [(9103, 16, 8, 128), (64, 16, 1, 64), (100, 32, 32, 128)])
 def test_code_bytes_follow_formula(L, dtype, group, nb, bs, hkv, d):
     if dtype in kvq.GROUP_FORMATS and d % group:
@@ -52,7 +54,8 @@ def test_code_bytes_follow_formula(L, dtype, group, nb, bs, hkv, d):
                   kvq.KVQ_FP8_E4M3_PER_TOKEN: tokens * 2 * 4,
                   kvq.KVQ_INT8_PER_CHANNEL: 2 * hkv * d * 4,
                   kvq.KVQ_INT8_PER_GROUP: tokens * 2 * hkv * (d // max(group, 1)) * 4,
-                  kvq.KVQ_INT4_PER_GROUP: tokens * 2 * hkv * (d // max(group, 1)) * 4}[dtype]
+                  kvq.KVQ_INT4_PER_GROUP: tokens * 2 * hkv * (d // max(group, 1)) * 4,
+                  kvq.KVQ_FP8_E5M2: 0}[dtype]
     assert lay["scale_bytes"] == exp_scales
     assert lay["total_bytes"] == kvq.kvq_pool_bytes(nb, bs, hkv, d, dtype, group)
     assert lay["total_bytes"] >= lay["code_bytes"] + lay["scale_bytes"]

@@ -18,7 +18,7 @@ REORDER = 3e-5
 
 FORMATS = [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_GROUP, 32), (kvq.KVQ_INT8_PER_TOKEN, 0),
            (kvq.KVQ_INT8_PER_CHANNEL, 0), (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0),
-           (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_INT4_PER_GROUP, 32)]
+           (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_INT4_PER_GROUP, 32), (kvq.KVQ_FP8_E5M2, 0)]
 
 
 def _t(x):

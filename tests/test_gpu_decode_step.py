@@ -55,7 +55,7 @@ def _step_case(name, fmt, group, **kw):
 @pytest.mark.parametrize("fmt,group", [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_GROUP, 32),
                                        (kvq.KVQ_INT8_PER_TOKEN, 0), (kvq.KVQ_INT8_PER_CHANNEL, 0),
                                        (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0),
-                                       (kvq.KVQ_INT4_PER_GROUP, 128)])
+                                       (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_FP8_E5M2, 0)])
 def test_decode_step_parity(fmt, group):
     w, pool, (k, v, slots), q, got = _step_case("gqa_64x2048", fmt, group, S=5, L=333)
     # the same step as two separate calls on a second pool gives the same bits

@@ -18,7 +18,7 @@ DEV = torch.device("cuda:0")
 FORMATS = [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_GROUP, 64), (kvq.KVQ_INT8_PER_GROUP, 32),
            (kvq.KVQ_INT8_PER_GROUP, 16), (kvq.KVQ_INT8_PER_TOKEN, 0), (kvq.KVQ_INT8_PER_CHANNEL, 0),
            (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0), (kvq.KVQ_INT4_PER_GROUP, 128),
-           (kvq.KVQ_INT4_PER_GROUP, 32), (kvq.KVQ_INT4_PER_GROUP, 16)]
+           (kvq.KVQ_INT4_PER_GROUP, 32), (kvq.KVQ_INT4_PER_GROUP, 16), (kvq.KVQ_FP8_E5M2, 0)]
 
 
 def _calib(fmt, k, v):
@@ -129,6 +129,7 @@ def test_tiny_workload_full():
     ("mha_100_int8ch", dict(S=5, L=300)), ("mha_100_int8g64", dict(S=5, L=300)),
     ("long_8x32k", dict(S=1, L=3001, bs=16)), ("long_8x32k", dict(S=1, L=3001, bs=32)),
     ("mixed_256", dict(S=5, L=200, layers=2)), ("gqa_64x2048_int4", dict(S=3, L=500)),
+    ("gqa_64x2048_e5m2", dict(S=3, L=500)),
 ])
 def test_workload_reduced_parity(name, kw):
     w = synth.workload(name, **kw)
