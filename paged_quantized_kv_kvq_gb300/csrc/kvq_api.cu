@@ -362,7 +362,7 @@ static kvq_status cascade(kvq_pool* pool, const kvq_half* k_new, const kvq_half*
                                  &a, &plan);
   if (st != KVQ_OK || num_seqs == 0) return st;
   kvq::RowsPlan pplan;
-  if (casc && !kvq::plan_rows(pool->view, 0, num_seqs, num_q_heads, num_seqs, &pplan))
+  if (casc && !kvq::plan_rows(pool->view, num_seqs, num_q_heads, &pplan))
     return KVQ_ERR_UNSUPPORTED;
   const bool step = k_new != nullptr || v_new != nullptr;
   if (step) {
@@ -382,7 +382,6 @@ static kvq_status cascade(kvq_pool* pool, const kvq_half* k_new, const kvq_half*
     pa.table = block_table;
     pa.lens = context_lens;
     pa.out = static_cast<float*>(workspace);
-    pa.mode = 0;
     pa.S = num_seqs;
     pa.Hq = num_q_heads;
     pa.max_blocks = max_blocks_per_seq;
@@ -444,23 +443,10 @@ kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, in
   if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * pool->view.bs) return KVQ_ERR_INVALID_ARG;
   if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(q) & 15) return KVQ_ERR_INVALID_ARG;
-  kvq::RowsPlan plan;
-  if (!kvq::plan_rows(pool->view, 1, num_seqs, num_q_heads, max_q_len, &plan))
-    return KVQ_ERR_UNSUPPORTED;
-  kvq::RowsArgs a;
-  a.pool = pool->view;
-  a.q = reinterpret_cast<const __half*>(q);
-  a.table = block_table;
-  a.lens = context_lens;
-  a.q_start = q_start;
-  a.out = out;
-  a.mode = 1;
-  a.S = num_seqs;
-  a.Hq = num_q_heads;
-  a.max_blocks = max_blocks_per_seq;
-  a.max_ctx = max_context_len;
-  a.sm_scale = sm_scale;
-  return from_cuda(kvq::launch_rows(a, plan, stream, false));
+  const cudaError_t e = kvq::launch_prefill(
+      pool->view, reinterpret_cast<const __half*>(q), num_seqs, num_q_heads, q_start, max_q_len,
+      block_table, max_blocks_per_seq, context_lens, max_context_len, sm_scale, out, stream);
+  return e == cudaErrorInvalidValue ? KVQ_ERR_UNSUPPORTED : from_cuda(e);
 }
 
 kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,

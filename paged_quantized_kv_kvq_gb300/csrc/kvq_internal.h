@@ -66,30 +66,31 @@ struct DecodeArgs {
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st,
                           bool dependent = false);
 
-// Many-rows attention (kvq_rows_impl.cuh).  mode 0 (shared prefix): the
-// first P blocks of every sequence (those of table row 0) attended once per kv
-// head for all sequences' Q rows, writing the partial rows out[S][Hq][D+2]
-// (m, l, O) that a decode with skip = P folds in.  mode 1 (prefill): the
-// query tokens q_start[s]..q_start[s+1]-1 of each sequence attend causally to
-// its cache, writing out[Tq][Hq][D].  rows_per_unit: S for the prefix, the
-// longest chunk for prefill.
+// Shared-prefix attention (kvq_rows_impl.cuh): the first P blocks of every
+// sequence (those of table row 0) attended once per kv head for all
+// sequences' Q rows, writing the partial rows out[S][Hq][D+2] (m, l, O) that
+// a decode with skip = P folds in.
 struct RowsPlan {
   int grid = 0, ntiles = 0, nstage = 0, stage_bytes = 0, bar_off = 0, smem_bytes = 0;
 };
-bool plan_rows(const PoolView& pool, int mode, int S, int Hq, int rows_per_unit, RowsPlan* plan);
+bool plan_rows(const PoolView& pool, int S, int Hq, RowsPlan* plan);
 struct RowsArgs {
   PoolView pool;
   const __half* q;
   const int* table;
   const int* lens;
-  const int* q_start = nullptr;
   float* out;
-  int mode = 0;
   int S, Hq, max_blocks, max_ctx;
   int P = 0;
   float sm_scale;
 };
 cudaError_t launch_rows(const RowsArgs& a, const RowsPlan& plan, cudaStream_t st, bool dependent);
+
+// Prefill / chunked prefill (kvq_prefill_impl.cuh): the query tokens
+// q_start[s]..q_start[s+1]-1 of each sequence attend causally to its cache.
+cudaError_t launch_prefill(const PoolView& pool, const __half* q, int S, int Hq, const int* q_start,
+                           int max_q_len, const int* table, int max_blocks, const int* lens,
+                           int max_ctx, float sm_scale, float* out, cudaStream_t st);
 
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;

@@ -1,5 +1,5 @@
-// kvq_rows.cu -- launch planning and format dispatch of the many-rows
-// attention kernel (kvq_rows_impl.cuh): the shared-prefix cascade and prefill.
+// kvq_rows.cu -- launch planning and format dispatch of the shared-prefix
+// attention kernel (kvq_rows_impl.cuh).
 #include <algorithm>
 
 #include "kvq_internal.h"
@@ -41,21 +41,19 @@ cudaError_t run_rows_d(const RowsLaunch& l) {
 
 }  // namespace
 
-bool plan_rows(const PoolView& pool, int mode, int S, int Hq, int rows_per_unit, RowsPlan* plan) {
+bool plan_rows(const PoolView& pool, int S, int Hq, RowsPlan* plan) {
   constexpr int W = kRowsWarps;
   const bool tok = pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN;
   const int stage_bytes = round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
   const int G = Hq / pool.Hkv;
-  // prefix: one unit of S*G rows per kv head; prefill: one unit of
-  // max_q_len*G rows per (kv head, sequence)
-  const int64_t ntiles = ((int64_t)rows_per_unit * G + kRowsTile - 1) / kRowsTile;
+  const int64_t ntiles = ((int64_t)S * G + kRowsTile - 1) / kRowsTile;  // per kv head
   int nstage = 4;
   while (nstage > 2 && W * nstage * stage_bytes > 80 * 1024) --nstage;
   const int merge_bytes = W * kRowsTile * (pool.D + 2) * 4;
   const int bar_off = round_up(std::max(W * nstage * stage_bytes, merge_bytes), 128);
   const int smem = round_up(bar_off + W * nstage * (8 + 4), 128);
   if (smem > 227 * 1024 || ntiles < 1) return false;
-  const int64_t grid = (int64_t)pool.Hkv * ntiles * (mode == ROWS_PREFILL ? S : 1);
+  const int64_t grid = (int64_t)pool.Hkv * ntiles;
   if (grid > 0x7fffffffLL) return false;
   plan->grid = static_cast<int>(grid);
   plan->ntiles = static_cast<int>(ntiles);
@@ -73,9 +71,7 @@ cudaError_t launch_rows(const RowsArgs& a, const RowsPlan& plan, cudaStream_t st
   p.q = a.q;
   p.table = a.table;
   p.lens = a.lens;
-  p.q_start = a.q_start;
   p.out = a.out;
-  p.mode = a.mode;
   p.S = a.S;
   p.Hq = a.Hq;
   p.G = a.Hq / a.pool.Hkv;

@@ -1,24 +1,18 @@
-// kvq_rows_impl.cuh -- attention of many Q rows per kv head over a quantized
-// paged KV pool: the shared-prefix cascade and prefill.
+// kvq_rows_impl.cuh -- shared-prefix ("cascade") attention over a quantized
+// paged KV pool: many sequences' Q rows against the blocks they share.
 //
 // Method ("KV Cache优化实战：大模型推理显存占用与加速方案详解",
-// 0539edu.com/news/5800990):
-//  * shared prefix (§2.2 and §4.3: PagedAttention lets requests with a common
-//    prefix share its physical blocks; xpshop.cn article-402 §三: shared
-//    system prompts): when every sequence's first P blocks are the same
-//    physical blocks, those blocks are attended once for all sequences' Q rows
-//    instead of once per sequence.  The result is a partial (running max m,
-//    sum l, unnormalised output O, base-2 softmax) per (sequence, Q head) that
-//    the paged decode over the remaining blocks folds in by log-sum-exp.
-//  * prefill (§1.1: the prompt's tokens are processed together, each attending
-//    causally to the tokens up to itself; a long prompt may be processed in
-//    chunks, each chunk attending to the cache written by the earlier ones):
-//    the rows are the chunk's query tokens times the group's Q heads, every row
-//    with its own causal limit, over the sequence's own blocks.
+// 0539edu.com/news/5800990, §2.2 and §4.3: PagedAttention lets requests with
+// a common prefix share its physical blocks; xpshop.cn article-402 §三: shared
+// system prompts): when every sequence's first P blocks are the same physical
+// blocks, those blocks are attended once for all sequences' Q rows instead of
+// once per sequence.  The result is a partial (running max m, sum l,
+// unnormalised output O, base-2 softmax) per (sequence, Q head) that the paged
+// decode over the remaining blocks folds in by log-sum-exp.
 //
 // GB300 design: a CTA takes one kv head and a tile of 16 Q rows -- a row is a
-// (sequence, Q head) pair for the prefix, a (query token, Q head) pair for
-// prefill -- and its 4 warps split the blocks the tile needs between them.  Each
+// (sequence, Q head) pair, so a tile usually spans several sequences -- and
+// its 4 warps split the shared blocks between them.  Each
 // warp streams its blocks through bulk-copy stages (as the decode kernel does)
 // and computes with the rows on the M dimension of mma.m16n8k16: Q.K^T takes
 // the K codes of the fragment-native page layout directly as B fragments
@@ -42,22 +36,15 @@ constexpr int kRowsWarps = 4;
 constexpr int kRowsThreads = kRowsWarps * 32;
 constexpr int kRowsTile = 16;  // Q rows per CTA: one mma M tile
 
-enum RowsMode : int {
-  ROWS_PREFIX = 0,   // rows (sequence, Q head) over the shared blocks of table row 0
-  ROWS_PREFILL = 1,  // rows (query token, Q head) of one sequence, causal
-};
-
 struct RowsParams {
   PoolView pool;
-  const __half* q;      // prefix: [S][Hq][D]; prefill: [Tq][Hq][D]
-  const int* table;     // [S][max_blocks]
-  const int* lens;      // [S] tokens in the cache (prefill: including the chunk)
-  const int* q_start;   // prefill: [S + 1] first query row of each sequence
-  float* out;           // prefix: [S][Hq][D + 2] partial rows; prefill: [Tq][Hq][D]
-  int mode;
+  const __half* q;      // [S][Hq][D]
+  const int* table;     // [S][max_blocks]; row 0's first P entries are the shared blocks
+  const int* lens;      // [S]
+  float* out;           // [S][Hq][D + 2] partial rows (m, l, O)
   int S, Hq, G, max_blocks, max_ctx;
-  int P;                // prefix: shared blocks
-  int ntiles;           // row tiles per (kv head[, sequence])
+  int P;                // shared blocks
+  int ntiles;           // row tiles per kv head
   int nstage, stage_bytes;
   int bar_off;          // shared-memory offset of the barriers (past stages and merge rows)
   float sm_scale_log2;
@@ -81,11 +68,8 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
   const PoolView& pool = p.pool;
   const int bs = pool.bs;
   const int nstage = p.nstage;
-  const bool prefill = p.mode == ROWS_PREFILL;
-  // grid: prefix (kv head, tile); prefill (kv head, sequence, tile)
-  const int tile = blockIdx.x % p.ntiles;
-  const int seq = prefill ? (blockIdx.x / p.ntiles) % p.S : 0;
-  const int h = prefill ? blockIdx.x / (p.ntiles * p.S) : blockIdx.x / p.ntiles;
+  const int tile = blockIdx.x % p.ntiles;  // grid: (kv head, tile)
+  const int h = blockIdx.x / p.ntiles;
 
   // A kernel launched after this one as a programmatic dependent reads our
   // output only after its griddepcontrol.wait on this grid's completion.
@@ -96,40 +80,17 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
   int* stage_phys =
       reinterpret_cast<int*>(smem + p.bar_off + kRowsWarps * nstage * 8) + warp * nstage;
 
-  // ---- rows of the tile: the tile's row rr is (sequence rr / G, head rr % G)
-  // for the prefix and (query token rr / G, head rr % G) of sequence `seq`
-  // for prefill; each has a token limit (its context, or its causal end)
-  int rows_total, qbase = 0, ctx = 0, nq = 0;
-  if (prefill) {
-    qbase = p.q_start[seq];
-    nq = p.q_start[seq + 1] - qbase;
-    ctx = p.lens[seq];
-    if (ctx > p.max_ctx || ctx < nq) {
-      if (tile == 0 && h == 0 && threadIdx.x == 0) set_error(pool.err, ERR_RANGE);
-      ctx = min(ctx, p.max_ctx);
-    }
-    rows_total = nq * p.G;
-  } else {
-    rows_total = p.S * p.G;
-  }
-  if (tile * kRowsTile >= rows_total) return;  // past this sequence's chunk
-  const int table_row = prefill ? seq : 0;
-  const int page_cap = prefill ? p.max_blocks : p.P;
+  // ---- rows of the tile: row rr is (sequence rr / G, Q head rr % G) of kv
+  // head h; its token limit is its own context length, at most the prefix
+  const int rows_total = p.S * p.G;
   auto row_of = [&](int rr, int& lim, const __half*& qp, int64_t& orow) {
     lim = 0;
     qp = nullptr;
     orow = -1;
     if (rr >= rows_total) return;
-    const int hq = h * p.G + rr % p.G;
-    if (prefill) {
-      const int i = rr / p.G;
-      lim = max(0, ctx - nq + i + 1);
-      orow = (int64_t)(qbase + i) * p.Hq + hq;
-    } else {
-      const int s = rr / p.G;
-      lim = max(0, min(min(p.lens[s], p.max_ctx), p.P * bs));
-      orow = (int64_t)s * p.Hq + hq;
-    }
+    const int s = rr / p.G;
+    lim = max(0, min(min(p.lens[s], p.max_ctx), p.P * bs));
+    orow = (int64_t)s * p.Hq + h * p.G + rr % p.G;
     qp = p.q + orow * D;
   };
   int lim[2];
@@ -194,12 +155,12 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
   int wlim = max(lim[0], lim[1]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) wlim = max(wlim, __shfl_xor_sync(0xffffffffu, wlim, off));
-  const int np = min(page_cap, (wlim + bs - 1) / bs);
+  const int np = min(p.P, (wlim + bs - 1) / bs);
   const int chunk = (np + kRowsWarps - 1) / kRowsWarps;
   const int p0 = warp * chunk;
   const int p1 = min(np, p0 + chunk);
   const int n_w = max(p1 - p0, 0);
-  const int* trow = p.table + (int64_t)table_row * p.max_blocks;
+  const int* trow = p.table;  // table row 0 names the shared blocks
 
   if (lane == 0) {
     for (int st = 0; st < nstage; ++st) mbar_init(&bars[st], 1);
@@ -510,15 +471,11 @@ __global__ void __launch_bounds__(kRowsThreads) kvq_rows_kernel(const RowsParams
       Ls = fmaf(wt, row[1], Ls);
       O = fmaf(wt, row[2 + d], O);
     }
-    if (prefill) {
-      p.out[orow * D + d] = Ls > 0.f ? O / Ls : 0.f;
-    } else {
-      float* dst = p.out + orow * (D + 2);
-      dst[2 + d] = O;
-      if (d == 0) {
-        dst[0] = M;
-        dst[1] = Ls;
-      }
+    float* dst = p.out + orow * (D + 2);
+    dst[2 + d] = O;
+    if (d == 0) {
+      dst[0] = M;
+      dst[1] = Ls;
     }
   }
 }
