@@ -35,7 +35,7 @@
  *     code = e5m2 round-to-nearest-even of x itself, saturating to the largest
  *     finite value (57344); dequantized value = the code's value.
  *   - INT4, listed beside INT8 and FP8 as the more aggressive option ([KVC]
- *     §2.3; [P312] §四 measures it): read as the same absmax symmetric rule
+ *     §2.3; measured in [KVC] §3.3 and [P402] §三): read as the same absmax symmetric rule
  *     on 4 bits, per group: s = absmax / 7 (fp32), code =
  *     clamp(round-half-even(x / s), -7, 7), zero group -> s = 0, codes 0.
  *   - Attention: softmax(q.k^T * sm_scale) v over the dequantized cache, in
