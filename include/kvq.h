@@ -221,8 +221,8 @@ kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half
                            const int32_t* context_lens, int max_context_len, float sm_scale,
                            float* out, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
-/* Shared-prefix ("cascade") decode ([KVC] §2.2: requests with a common prefix
- * share its physical blocks; [P402] §三: a shared system prompt): the first
+/* Shared-prefix ("cascade") decode ([KVC] §2.2, §4.4: requests with a common
+ * prefix -- a system prompt, a fixed history -- share its physical blocks): the first
  * prefix_blocks blocks of every sequence are the same physical blocks, those
  * of block_table row 0.  They are read once per kv head for all sequences'
  * Q heads (a partial softmax per (sequence, Q head)), the remaining blocks by

@@ -2,9 +2,9 @@
 // paged KV pool: many sequences' Q rows against the blocks they share.
 //
 // Method ("KV Cache优化实战：大模型推理显存占用与加速方案详解",
-// 0539edu.com/news/5800990, §2.2 and §4.3: PagedAttention lets requests with
-// a common prefix share its physical blocks; xpshop.cn article-402 §三: shared
-// system prompts): when every sequence's first P blocks are the same physical
+// 0539edu.com/news/5800990, §2.2 and §4.4: PagedAttention lets requests with
+// a common prefix -- a system prompt, a fixed history -- share its physical
+// blocks): when every sequence's first P blocks are the same physical
 // blocks, those blocks are attended once for all sequences' Q rows instead of
 // once per sequence.  The result is a partial (running max m, sum l,
 // unnormalised output O, base-2 softmax) per (sequence, Q head) that the paged
