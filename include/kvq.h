@@ -158,6 +158,32 @@ kvq_status kvq_append(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
 kvq_status kvq_copy_blocks(kvq_pool* pool, const int32_t* src_blocks, const int32_t* dst_blocks,
                            int n, cudaStream_t stream);
 
+/* Per-head mixed precision ([P312] §六: the attention heads that quantization
+ * hurts stay FP16, the others are quantized): hold two pools per layer over a
+ * contiguous split of the kv heads (permute the heads once so that the FP16
+ * ones come first) and address each pool's slice of the full per-token rows
+ * with a row stride.
+ *   kvq_append_strided      : kvq_append with k, v pointing at the pool's first
+ *                             kv head; token t's K/V row starts row_stride
+ *                             elements after token t-1's (row_stride >=
+ *                             kv_heads*head_dim, a multiple of 8)
+ *   kvq_paged_decode_strided: kvq_paged_decode with q pointing at the first Q
+ *                             head of the pool's groups and sequence s's row
+ *                             q_row_stride elements after s-1's (a multiple of
+ *                             8, >= num_q_heads*head_dim); out likewise with
+ *                             out_row_stride (>= num_q_heads*head_dim), so the
+ *                             two pools' calls fill disjoint heads of one
+ *                             output.  num_q_heads counts this pool's Q heads. */
+kvq_status kvq_append_strided(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
+                              int64_t row_stride, const int64_t* slot_mapping, int64_t T,
+                              cudaStream_t stream);
+kvq_status kvq_paged_decode_strided(const kvq_pool* pool, const kvq_half* q,
+                                    int64_t q_row_stride, int num_seqs, int num_q_heads,
+                                    const int32_t* block_table, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context_len,
+                                    float sm_scale, float* out, int64_t out_row_stride,
+                                    void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Scratch bytes kvq_paged_decode needs for these sizes (split-K partials).
  * May be 0.  Host only. */
 size_t kvq_decode_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,

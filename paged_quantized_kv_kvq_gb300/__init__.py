@@ -90,6 +90,9 @@ def _declare(L):
         "kvq_calibrate_channel_scales": (i32, [P, P, P, i64, P]),
         "kvq_append": (i32, [P, P, P, P, i64, P]),
         "kvq_copy_blocks": (i32, [P, P, P, i32, P]),
+        "kvq_append_strided": (i32, [P, P, P, i64, P, i64, P]),
+        "kvq_paged_decode_strided": (i32, [P, P, i64, i32, i32, P, i32, P, i32, f32, P, i64, P, sz,
+                                           P]),
         "kvq_decode_workspace_bytes": (sz, [P, i32, i32, i32]),
         "kvq_decode_workspace_bytes_ex": (sz, [P, i32, i32, i32, i32]),
         "kvq_paged_decode": (i32, [P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
@@ -192,6 +195,46 @@ def kvq_append(pool, k, v, slot_mapping, stream=None) -> None:
     _check(lib().kvq_append(pool, _ptr(k, torch.float16, "k"), _ptr(v, torch.float16, "v"),
                             _ptr(slot_mapping, torch.int64, "slot_mapping"), k.shape[0],
                             _stream(stream)), "kvq_append")
+
+
+def _rows_view(t, dtype, name):
+    """Pointer and row stride (elements) of a [rows, heads, head_dim] view whose
+    heads and channels are contiguous (a head slice of wider rows)."""
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("%s must be [rows, heads, head_dim] with contiguous heads" % name)
+    return ctypes.c_void_p(t.data_ptr()), int(t.stride(0))
+
+
+def kvq_append_strided(pool, k, v, slot_mapping, stream=None) -> None:
+    """kvq_append for head slices of wider token rows (per-head mixed precision)."""
+    import torch
+
+    kp, ks = _rows_view(k, torch.float16, "k")
+    vp, vs = _rows_view(v, torch.float16, "v")
+    if ks != vs or k.shape != v.shape or k.shape[0] != slot_mapping.numel():
+        raise ValueError("k and v must be equal-shaped views with the same row stride")
+    _check(lib().kvq_append_strided(pool, kp, vp, ks, _ptr(slot_mapping, torch.int64, "slot_mapping"),
+                                    k.shape[0], _stream(stream)), "kvq_append_strided")
+
+
+def kvq_paged_decode_strided(pool, q, block_table, context_lens, max_context_len, sm_scale, out,
+                             workspace=None, stream=None) -> None:
+    """kvq_paged_decode for head slices of wider q / out rows (per-head mixed precision)."""
+    import torch
+
+    qp, qs = _rows_view(q, torch.float16, "q")
+    op, os_ = _rows_view(out, torch.float32, "out")
+    S, Hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().kvq_paged_decode_strided(
+        pool, qp, qs, S, Hq, _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len), float(sm_scale),
+        op, os_, _ptr(workspace, None, "workspace") if workspace is not None else None, ws_bytes,
+        _stream(stream)), "kvq_paged_decode_strided")
 
 
 def kvq_copy_blocks(pool, src_blocks, dst_blocks, stream=None) -> None:

@@ -218,6 +218,21 @@ kvq_status kvq_copy_blocks(kvq_pool* pool, const int32_t* src_blocks, const int3
   return from_cuda(kvq::launch_copy_blocks(pool->view, src_blocks, dst_blocks, n, stream));
 }
 
+kvq_status kvq_append_strided(kvq_pool* pool, const kvq_half* k, const kvq_half* v,
+                              int64_t row_stride, const int64_t* slot_mapping, int64_t T,
+                              cudaStream_t stream) {
+  if (pool == nullptr || T < 0) return KVQ_ERR_INVALID_ARG;
+  if (T == 0) return KVQ_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (T > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
+  if (row_stride < (int64_t)pool->view.Hkv * pool->view.D || row_stride % 8 != 0)
+    return KVQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(kvq::launch_step_append(pool->view, reinterpret_cast<const __half*>(k),
+                                           reinterpret_cast<const __half*>(v), slot_mapping, T,
+                                           nullptr, nullptr, 0, 0, stream, false, row_stride));
+}
+
 size_t kvq_decode_workspace_bytes_ex(const kvq_pool* pool, int num_seqs, int num_q_heads,
                                      int max_context_len, int split_blocks) {
   if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || num_q_heads % pool->view.Hkv != 0)
@@ -305,6 +320,25 @@ kvq_status kvq_selftest_decode_timeout(const kvq_pool* pool, const kvq_half* q, 
   if (st != KVQ_OK || num_seqs == 0) return st;
   a.wait_tries = wait_tries;
   a.fault_issue = 0;  // warp 0's first copy is armed but never issued
+  return from_cuda(kvq::launch_decode(a, plan, stream));
+}
+
+kvq_status kvq_paged_decode_strided(const kvq_pool* pool, const kvq_half* q,
+                                    int64_t q_row_stride, int num_seqs, int num_q_heads,
+                                    const int32_t* block_table, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context_len,
+                                    float sm_scale, float* out, int64_t out_row_stride,
+                                    void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  kvq::DecodeArgs a;
+  kvq::DecodePlan plan;
+  const kvq_status st =
+      prepare_decode(pool, q, num_seqs, num_q_heads, block_table, max_blocks_per_seq, context_lens,
+                     max_context_len, sm_scale, out, workspace, ws_bytes, 0, &a, &plan);
+  if (st != KVQ_OK || num_seqs == 0) return st;
+  const int64_t row = (int64_t)num_q_heads * pool->view.D;
+  if (q_row_stride < row || q_row_stride % 8 != 0 || out_row_stride < row) return KVQ_ERR_INVALID_ARG;
+  a.q_stride = q_row_stride;
+  a.out_stride = out_row_stride;
   return from_cuda(kvq::launch_decode(a, plan, stream));
 }
 

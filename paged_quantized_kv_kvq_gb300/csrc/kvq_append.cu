@@ -32,6 +32,7 @@ struct AppendParams {
   const int* table;
   const int* lens;
   int max_blocks, max_ctx;
+  int64_t x_stride;  // elements between consecutive tokens of k and v
 };
 
 __device__ __forceinline__ float absmax8(const __half2 (&x)[4]) {
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
   const int sub = off >> 4, tt = off & 15;
   const int D = pool.D, Hkv = pool.Hkv;
   const int per = Hkv * D;
-  const __half* x = (kv == 0 ? p.k : p.v) + t * per;
+  const __half* x = (kv == 0 ? p.k : p.v) + t * p.x_stride;
 
   __shared__ float red[kAppendThreads / 32];
   float tok_scale = 0.f;
@@ -338,7 +339,7 @@ cudaError_t launch_copy_blocks(const PoolView& pool, const int* src, const int* 
 
 cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
                           const int64_t* slots, int64_t T, cudaStream_t st) {
-  return launch_step_append(pool, k, v, slots, T, nullptr, nullptr, 0, 0, st, false);
+  return launch_step_append(pool, k, v, slots, T, nullptr, nullptr, 0, 0, st, false, 0);
 }
 
 namespace {
@@ -362,9 +363,11 @@ cudaError_t launch_append_fmt(const AppendParams& p, dim3 grid, cudaStream_t st,
 
 cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
                                const int64_t* slots, int64_t T, const int* table, const int* lens,
-                               int max_blocks, int max_ctx, cudaStream_t st, bool dependent) {
+                               int max_blocks, int max_ctx, cudaStream_t st, bool dependent,
+                               int64_t x_stride) {
   if (T == 0) return cudaSuccess;
-  AppendParams p{pool, k, v, slots, T, table, lens, max_blocks, max_ctx};
+  AppendParams p{pool, k, v, slots, T, table, lens, max_blocks, max_ctx,
+                 x_stride > 0 ? x_stride : (int64_t)pool.Hkv * pool.D};
   dim3 grid(static_cast<unsigned>(T), 2);
   switch (pool.fmt) {
     case FMT_FP16: return launch_append_fmt<FMT_FP16>(p, grid, st, dependent);

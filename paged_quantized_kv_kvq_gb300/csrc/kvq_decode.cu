@@ -70,6 +70,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   p.table = a.table;
   p.lens = a.lens;
   p.out = a.out;
+  p.q_stride = a.q_stride > 0 ? a.q_stride : (int64_t)a.Hq * a.pool.D;
+  p.out_stride = a.out_stride > 0 ? a.out_stride : (int64_t)a.Hq * a.pool.D;
   p.ps = static_cast<int*>(a.workspace);
   p.part = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + plan.ps_bytes);
   p.S = a.S;

@@ -55,10 +55,11 @@ constexpr int kMergeThreads = 128;
 
 struct DecodeParams {
   PoolView pool;
-  const __half* q;     // [S][Hq][D]
+  const __half* q;     // [S][Hq][D], rows q_stride elements apart
   const int* table;    // [S][max_blocks]
   const int* lens;     // [S]
-  float* out;          // [S][Hq][D]
+  float* out;          // [S][Hq][D], rows out_stride elements apart
+  int64_t q_stride, out_stride;
   int* ps;             // [S + 1] page prefix over sequences (written by CTA 0 for the merge)
   float* part;         // [warps][2][kPartRows][D + 2]: m, l, O of cut units
   // Shared-prefix cascade: the first `skip` blocks of every sequence are the
@@ -434,7 +435,7 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, int 
   const int Gt = min(8, p.G - 8 * ht);
   const bool hv = g < Gt;
   const int hq = h * p.G + 8 * ht + (hv ? g : 0);
-  const __half* qp = p.q + ((int64_t)s * p.Hq + hq) * D;
+  const __half* qp = p.q + (int64_t)s * p.q_stride + (int64_t)hq * D;
   csc = p.sm_scale_log2;
   if constexpr (!FmtTraits<FMT>::channel) {
 #pragma unroll
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     // the normalised prefix result
     for (int s = gw; s < p.S; s += nwarps) {
       if (PS[s + 1] != PS[s]) continue;
-      float* o = p.out + (int64_t)s * p.Hq * D;
+      float* o = p.out + (int64_t)s * p.out_stride;
       if (p.pre == nullptr) {
         for (int i = lane; i < p.Hq * D; i += 32) o[i] = 0.f;
       } else {
@@ -702,7 +703,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     const float lt0 = warp_sum_over_rows(l[0]), lt1 = warp_sum_over_rows(l[1]);
     const float inv2E = pow2f(-E);
     const float* vch = T::channel ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
-    const int64_t row0 = (int64_t)u.s * p.Hq + h * p.G + 8 * ht;
+    const int64_t row0 = (int64_t)u.s * p.Hq + h * p.G + 8 * ht;  // (prefix partial rows)
+    float* obase = p.out + (int64_t)u.s * p.out_stride + (int64_t)(h * p.G + 8 * ht) * D;
     if (seg_pi0 == 0 && seg_end == u.Ps) {
       if (p.pre == nullptr) {
         const float f0 = lt0 > 0.f ? inv2E / lt0 : 0.f, f1 = lt1 > 0.f ? inv2E / lt1 : 0.f;
@@ -711,12 +713,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
           const int d0 = 16 * mt + g;
           const float c0 = T::channel ? vch[d0] : 1.f, c8 = T::channel ? vch[d0 + 8] : 1.f;
           if (2 * j < Gt) {
-            float* dst = p.out + (row0 + 2 * j) * D;
+            float* dst = obase + (2 * j) * D;
             dst[d0] = o[mt][0] * f0 * c0;
             dst[d0 + 8] = o[mt][2] * f0 * c8;
           }
           if (2 * j + 1 < Gt) {
-            float* dst = p.out + (row0 + 2 * j + 1) * D;
+            float* dst = obase + (2 * j + 1) * D;
             dst[d0] = o[mt][1] * f1 * c0;
             dst[d0 + 8] = o[mt][3] * f1 * c8;
           }
@@ -736,7 +738,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
         const float den = fmaf(lu, wu, lp * wp);
         const float inv = den > 0.f ? 1.f / den : 0.f;
         const float fu = wu * inv2E * inv, fp = wp * inv;
-        float* dst = p.out + (row0 + 2 * j + c) * D;
+        float* dst = obase + (2 * j + c) * D;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           const int d0 = 16 * mt + g;
@@ -939,7 +941,7 @@ __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodePa
       }
       M = cm;
     }
-    float* dst = p.out + orow * D;
+    float* dst = p.out + (int64_t)s * p.out_stride + (int64_t)(h * p.G + 8 * ht + rr) * D;
 #pragma unroll
     for (int i = 0; i < NE; ++i) dst[lane + 32 * i] = Lsum > 0.f ? acc[i] / Lsum : 0.f;
   }

@@ -15,10 +15,12 @@ cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v
 // Append with slots from `slots`, or -- when slots is null -- the decode-step
 // form: token t is sequence t's new token, stored at position lens[t]-1.
 // `dependent`: launch as a programmatic dependent of the previous kernel (the
-// kernel waits for its completion before reading anything).
+// kernel waits for its completion before reading anything).  `x_stride`:
+// elements between consecutive tokens of k and v (0 = kv_heads * head_dim).
 cudaError_t launch_step_append(const PoolView& pool, const __half* k, const __half* v,
                                const int64_t* slots, int64_t T, const int* table, const int* lens,
-                               int max_blocks, int max_ctx, cudaStream_t st, bool dependent);
+                               int max_blocks, int max_ctx, cudaStream_t st, bool dependent,
+                               int64_t x_stride = 0);
 cudaError_t launch_copy_blocks(const PoolView& pool, const int* src, const int* dst, int n,
                                cudaStream_t st);
 cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half* v, int64_t T,
@@ -57,6 +59,7 @@ struct DecodeArgs {
   // fold in the prefix partials `pre` ([S][Hq][D+2]); 0 / null otherwise
   int skip = 0;
   const float* pre = nullptr;
+  int64_t q_stride = 0, out_stride = 0;  // elements between sequences' rows; 0 = Hq * D
   int wait_tries = kWaitTries;  // bound of each pipeline wait, in ~1 ms tries
   int fault_issue = -1;   // self-test only: withhold warp 0's copy of this index
 };
