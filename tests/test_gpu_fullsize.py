@@ -1,0 +1,134 @@
+"""Full-size parity: each decode workload at its full size, one layer (every
+layer of a step runs the same launches), through the call the bench times --
+kvq_decode_step (append of each sequence's new token, then the decode as a
+dependent launch), or kvq_cascade_decode_step for the long shared prefix --
+so the persistent grid, the split of the context over warps and the merge
+are the ones of the measured runs.  The oracle computes sampled sequences
+one by one: their cached tokens are the seeded host draws the oracle also
+gets; every other cached token is a device normal draw (it only has to be
+there, at its slot, for the launch to be the full one).  Outputs of the
+sampled sequences within 1e-3 of the float64 oracle; their new tokens' codes
+and scales bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import paged_quantized_kv_kvq_gb300 as kvq
+from paged_quantized_kv_kvq_gb300 import synth
+from kvq_testutil import TOL, oracle_layer, oracle_slots
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+CHUNK = 1 << 16
+
+
+def _t(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def _full_pool(w, layer, fmt, group, k, v, slots, calib):
+    """Pool with every cached token of the workload: device draws first, then
+    the sampled sequences' host tokens over their own slots."""
+    pool = kvq.KVPool(w.num_blocks, w.bs, w.Hkv, w.D, fmt, group, device=DEV)
+    if fmt == kvq.KVQ_INT8_PER_CHANNEL:
+        kvq.kvq_calibrate_channel_scales(pool.handle, _t(calib[0]), _t(calib[1]))
+    fill = _t(w.fill_slots())
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1000 + layer)
+    for a in range(0, fill.numel(), CHUNK):
+        b = min(fill.numel(), a + CHUNK)
+        kd = torch.randn((b - a, w.Hkv, w.D), generator=gen, device=DEV).half()
+        vd = torch.randn((b - a, w.Hkv, w.D), generator=gen, device=DEV).half()
+        pool.append(kd, vd, fill[a:b])
+    for a in range(0, len(slots), CHUNK):
+        b = min(len(slots), a + CHUNK)
+        pool.append(_t(k[a:b]), _t(v[a:b]), _t(slots[a:b]))
+    return pool
+
+
+def _sample_tokens(w, layer, seqs):
+    """Host K/V and slots of the sampled sequences' cached tokens (shared
+    prefix included once) followed by their new tokens at position L-1."""
+    idx = w.fill_token_index()
+    keep = np.isin(idx[:, 0], seqs)
+    if w.shared_prefix_tokens and 0 not in seqs:
+        keep |= (idx[:, 0] == 0) & (idx[:, 1] < w.shared_prefix_tokens)
+    step_idx = np.stack([np.asarray(seqs, np.int64), w.context_lens[seqs].astype(np.int64) - 1], 1)
+    k, v = synth.kv_tokens(w, layer, np.concatenate([idx[keep], step_idx]))
+    slots = np.concatenate([w.fill_slots()[keep], w.step_slots()[seqs]])
+    return k, v, slots
+
+
+def _check(name, layer, seqs, fmt=None, group=None, cascade=False, **kw):
+    w = synth.workload(name, layers=layer + 1, **kw)
+    if fmt is None:
+        fmt, group = w.layer_formats[layer]
+    n = len(seqs)
+    k, v, slots = _sample_tokens(w, layer, seqs)
+    calib = (k, v) if fmt == kvq.KVQ_INT8_PER_CHANNEL else None
+    pool = _full_pool(w, layer, fmt, group, k[:-n], v[:-n], slots[:-n], calib)
+    # this step's new tokens: device draws, the sampled sequences' from the host
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(2000 + layer)
+    ks = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=DEV).half()
+    vs = torch.randn((w.S, w.Hkv, w.D), generator=gen, device=DEV).half()
+    ks[list(seqs)] = _t(k[-n:])
+    vs[list(seqs)] = _t(v[-n:])
+    q = synth.queries(w, layer)
+    table, lens = _t(w.block_table), _t(w.context_lens)
+    mc = int(w.context_lens.max())
+    out = torch.empty((w.S, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    if cascade:
+        P = w.shared_prefix_tokens // w.bs
+        ws = torch.empty(kvq.kvq_cascade_workspace_bytes(pool.handle, w.S, w.Hq, mc),
+                         dtype=torch.uint8, device=DEV)
+        kvq.kvq_cascade_decode_step(pool.handle, ks, vs, _t(q), table, lens, mc, P,
+                                    w.D ** -0.5, out, ws)
+    else:
+        pool.decode_step(ks, vs, _t(q), table, lens, mc, out=out)
+    torch.cuda.synchronize()
+    assert pool.error() == kvq.KVQ_OK
+    ref, rtable, remap = oracle_layer(w, fmt, group, k, v, slots, list(seqs), calib=calib)
+    # the sampled sequences' new tokens: codes and scales as the oracle's append
+    codes, scales = pool.read_slots(_t(slots[-n:]))
+    rs = oracle_slots(remap, slots[-n:], w.bs)
+    c = codes.cpu().numpy()
+    if fmt == kvq.KVQ_FP16:
+        np.testing.assert_array_equal(c.astype(np.float32), ref.codes[rs])
+    else:
+        np.testing.assert_array_equal(c.view(np.uint8), ref.codes[rs].view(np.uint8))
+    if scales is not None:
+        np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32),
+                                      ref.scales[rs].view(np.uint32))
+    exp = ref.decode(np.ascontiguousarray(q[list(seqs)]), rtable, w.context_lens[list(seqs)])
+    got = out.cpu().numpy()[list(seqs)]
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL, err_msg="%s layer %d" % (name, layer))
+    pool.close()
+
+
+@pytest.mark.parametrize("name", ["gqa_64x2048", "gqa_64x2048_int4", "gqa_64x2048_e5m2"])
+def test_gqa_64x2048_full(name):
+    # first, middle and last sequence: the last ends the persistent grid's range
+    _check(name, 0, [0, 31, 63])
+
+
+@pytest.mark.parametrize("name", ["mha_100_fp16", "mha_100_fp8", "mha_100_int8ch",
+                                  "mha_100_int8g64"])
+def test_mha_100_full(name):
+    _check(name, 0, [0, 57, 99])
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_long_8x32k_full(bs):
+    # the last sequence (its 32K-token drift walk is the slow host draw)
+    _check("long_8x32k", 0, [7], bs=bs)
+
+
+@pytest.mark.parametrize("layer", [0, 31])
+def test_mixed_256_full(layer):
+    # layer 0 INT8 per-group 128, layer 31 FP16; the 512-token prefix is shared
+    _check("mixed_256", layer, [0, 128, 255])
+
+
+def test_shared4k_256_cascade_full():
+    _check("shared4k_256", 0, [0, 255], cascade=True)
