@@ -26,13 +26,15 @@ def _t(x):
     return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
 
 
-def _full_pool(w, layer, fmt, group, k, v, slots, calib):
-    """Pool with every cached token of the workload: device draws first, then
-    the sampled sequences' host tokens over their own slots."""
+def _full_pool(w, layer, fmt, group, k, v, slots, calib, with_step=False):
+    """Pool with every cached token of the workload (and this step's, with
+    with_step): device draws first, then the sampled sequences' host tokens
+    over their own slots."""
     pool = kvq.KVPool(w.num_blocks, w.bs, w.Hkv, w.D, fmt, group, device=DEV)
     if fmt == kvq.KVQ_INT8_PER_CHANNEL:
         kvq.kvq_calibrate_channel_scales(pool.handle, _t(calib[0]), _t(calib[1]))
-    fill = _t(w.fill_slots())
+    fs = w.fill_slots()
+    fill = _t(np.concatenate([fs, w.step_slots()]) if with_step else fs)
     gen = torch.Generator(device=DEV)
     gen.manual_seed(1000 + layer)
     for a in range(0, fill.numel(), CHUNK):
@@ -132,3 +134,41 @@ def test_mixed_256_full(layer):
 
 def test_shared4k_256_cascade_full():
     _check("shared4k_256", 0, [0, 255], cascade=True)
+
+
+def test_prefill_8x2048_full():
+    """Prompt prefill at the size the bench times: 8 prompts of 2048 tokens of
+    the 64x2048 layout (INT8 per-group 128), each whole prompt one chunk, all
+    in one kvq_prefill call; sampled query rows of the first and last prompt
+    (the first rows, the sub-tile and page edges, the middle and the end),
+    each against the oracle's decode over its causal length."""
+    w = synth.workload("gqa_64x2048", S=8, layers=1)
+    fmt, group = w.layer_formats[0]
+    seqs = [0, 7]
+    k, v, slots = _sample_tokens(w, 0, seqs)
+    pool = _full_pool(w, 0, fmt, group, k, v, slots, None, with_step=True)
+    lens = w.context_lens.astype(np.int64)
+    qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(qs[-1])
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(3000)
+    q = torch.randn((T, w.Hq, w.D), generator=gen, device=DEV).half()
+    rng = np.random.default_rng(11)
+    qh = {s: rng.standard_normal((int(lens[s]), w.Hq, w.D)).astype(np.float16) for s in seqs}
+    for s in seqs:
+        q[int(qs[s]):int(qs[s + 1])] = _t(qh[s])
+    out = torch.empty((T, w.Hq, w.D), dtype=torch.float32, device=DEV)
+    kvq.kvq_prefill(pool.handle, q, _t(qs), int(lens.max()), _t(w.block_table), _t(w.context_lens),
+                    int(lens.max()), w.D ** -0.5, out)
+    torch.cuda.synchronize()
+    assert pool.error() == kvq.KVQ_OK
+    ref, rtable, _ = oracle_layer(w, fmt, group, k, v, slots, seqs)
+    got = out.cpu().numpy()
+    for i, s in enumerate(seqs):
+        n = int(lens[s])
+        rows = np.array([0, 1, 15, 16, 17, 31, 32, 1000, n - 17, n - 2, n - 1])
+        exp = ref.decode(np.ascontiguousarray(qh[s][rows]), np.repeat(rtable[i:i + 1], len(rows), 0),
+                         (rows + 1).astype(np.int32))
+        np.testing.assert_allclose(got[int(qs[s]) + rows], exp, rtol=0, atol=TOL,
+                                   err_msg="prompt %d" % s)
+    pool.close()
