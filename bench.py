@@ -278,7 +278,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     kvq.lib()
-    w = synth.workload(args.workload, layers=args.layers)
+    w = synth.workload(args.workload, layers=args.layers, bs=args.block_size)
     stream = torch.cuda.current_stream()
 
     # -- per-layer pools, filled with the cached tokens (untimed set-up)
@@ -338,6 +338,7 @@ def run_ours(args, rank, world, local_rank):
     if w.shared_prefix_tokens:
         mean_suffix = float(np.mean(w.context_lens)) - w.shared_prefix_tokens
         use = {"on": True, "off": False}.get(args.cascade, w.shared_prefix_tokens >= mean_suffix)
+        use = use and w.bs != 8  # the cascade takes blocks of 16 tokens or more
         P = w.shared_prefix_tokens // w.bs if use else 0
     if P:
         ws_need = max(kvq.kvq_cascade_workspace_bytes(p.handle, w.S, w.Hq, max_ctx) for p in pools)
@@ -486,7 +487,7 @@ def run_ours(args, rank, world, local_rank):
         "decode_tok_per_s": round(world * w.S / (ms * 1e-3), 1),
         "bytes_per_step": b,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": read_traffic(w.name),
+                     "frac": round(achieved / peak, 4), "traffic": read_traffic(w.name) if w.bs == 16 else None,
                      "kernel": ("kvq_cascade_decode call (prefix kernel, decode kernel and split "
                                 "merge, each a programmatic dependent of the one before; bytes "
                                 "count the shared prefix once)" if P else
@@ -511,7 +512,7 @@ def run_reference(args):
     from paged_quantized_kv_kvq_gb300 import synth
     import oracle
 
-    w = synth.workload(args.workload)
+    w = synth.workload(args.workload, bs=args.block_size)
     fmt, group = w.layer_formats[0]
     oracle.build()
     # one step = sequence 0 of layer 0, all its heads
@@ -666,6 +667,8 @@ def main():
                     help="decode: the decode step (default); prefill: prompt prefill")
     ap.add_argument("--prefill-seqs", type=int, default=8,
                     help="prompts in the prefill batch (--op prefill)")
+    ap.add_argument("--block-size", type=int, default=None,
+                    help="tokens per block (default: the workload's; 8 or a multiple of 16)")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers (profiling runs only; the bench line uses all)")
     args = ap.parse_args()
@@ -699,7 +702,7 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             from paged_quantized_kv_kvq_gb300 import synth
 
-            res["cpu_baseline"] = cpu_baseline(synth.workload(args.workload))
+            res["cpu_baseline"] = cpu_baseline(synth.workload(args.workload, bs=args.block_size))
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -97,7 +97,12 @@ size_t kvq_pool_bytes(int64_t num_blocks, int block_size, int kv_heads, int head
  * 16 tokens, reached through a per-request block table; [P312] §三: blocks of
  * 16 or 32 tokens).
  *   num_blocks : physical blocks (>= 1)
- *   block_size : tokens per block; a multiple of 16, at most 256
+ *   block_size : tokens per block: 8, or a multiple of 16 up to 256 ([KVC]
+ *                §3.2: 8 for short contexts at high concurrency, 16 or 32 for
+ *                long ones).  INT4 pools take multiples of 16 only; pools of
+ *                8-token blocks serve append, decode and block copy, while
+ *                kvq_prefill and the cascade with prefix_blocks > 0 refuse
+ *                them with UNSUPPORTED.
  *   kv_heads   : KV heads (>= 1); head_dim: 64 or 128
  *   group      : channels per scale for KVQ_INT8_PER_GROUP / KVQ_INT4_PER_GROUP
  *                (a multiple of 16 that divides head_dim); ignored otherwise
@@ -260,7 +265,8 @@ kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half
  * Precondition (not checked): block_table[s][j] == block_table[0][j] for
  * every j < prefix_blocks and every s whose context reaches block j.
  * Sequences shorter than the prefix are handled (their rows stop at their own
- * length).  Results equal kvq_paged_decode's up to fp32 rounding order. */
+ * length).  Results equal kvq_paged_decode's up to fp32 rounding order.
+ * Pools of 8-token blocks: prefix_blocks > 0 returns UNSUPPORTED. */
 size_t kvq_cascade_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_heads,
                                    int max_context_len);
 kvq_status kvq_cascade_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs,
@@ -285,7 +291,8 @@ kvq_status kvq_cascade_decode(const kvq_pool* pool, const kvq_half* q, int num_s
  * out[row] = softmax(q . k^T * sm_scale) v over positions 0 .. L_s - n_s + i.
  * Device errors: L_s < n_s or L_s > max_context_len sets OUT_OF_RANGE (L_s is
  * clamped; rows with no position left get zeros); a block id outside the
- * pool sets OUT_OF_RANGE and that block is skipped.  No workspace. */
+ * pool sets OUT_OF_RANGE and that block is skipped.  No workspace.  Pools of
+ * 8-token blocks return UNSUPPORTED. */
 kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
                        const int32_t* q_start, int max_q_len, const int32_t* block_table,
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,

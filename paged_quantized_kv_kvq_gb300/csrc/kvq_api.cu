@@ -32,7 +32,10 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
   if (num_blocks < 1 || bs < 1 || Hkv < 1 || D < 1 || !valid_dtype(dtype) || lay == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (D % 16 != 0) return KVQ_ERR_INVALID_ARG;
-  if (bs % 16 != 0 || bs > 256) return KVQ_ERR_UNSUPPORTED;
+  // blocks of 8 tokens (half a sub-tile per page) or multiples of 16; INT4's
+  // words pack tokens t and t+8 together and take multiples of 16 only
+  if ((bs % 16 != 0 && bs != 8) || bs > 256) return KVQ_ERR_UNSUPPORTED;
+  if (bs == 8 && dtype == KVQ_INT4_PER_GROUP) return KVQ_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
   int ng = 1;
   const bool grouped = dtype == KVQ_INT8_PER_GROUP || dtype == KVQ_INT4_PER_GROUP;
@@ -46,7 +49,7 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
   const int esize = dtype == KVQ_FP16 ? 2 : 1;
   // bytes of one 16-token sub-tile of K (or V) codes: INT4 packs two per byte
   const int sub_bytes = dtype == KVQ_INT4_PER_GROUP ? 8 * D : 16 * D * esize;
-  const size_t code_bytes = (size_t)bs / 16 * sub_bytes;  // K (or V) codes of one page
+  const size_t code_bytes = (size_t)bs * sub_bytes / 16;  // K (or V) codes of one page
   const size_t page_scale = grouped ? 2 * (size_t)bs * ng * 4 : 0;
   const size_t page_bytes = 2 * code_bytes + page_scale;
   const size_t n_pages = (size_t)num_blocks * Hkv;
@@ -386,6 +389,8 @@ static kvq_status cascade(kvq_pool* pool, const kvq_half* k_new, const kvq_half*
     return KVQ_ERR_INVALID_ARG;
   const size_t pre_bytes = cascade_pre_bytes(pool, num_seqs, num_q_heads);
   const bool casc = prefix_blocks > 0;
+  // the prefix kernel reads whole 16-token sub-tiles from one page
+  if (casc && pool->view.bs == 8) return KVQ_ERR_UNSUPPORTED;
   if (casc && (workspace == nullptr || ws_bytes < pre_bytes)) return KVQ_ERR_WORKSPACE;
   void* dws = casc ? static_cast<char*>(workspace) + pre_bytes : workspace;
   const size_t dws_bytes = casc ? ws_bytes - pre_bytes : ws_bytes;
@@ -469,6 +474,8 @@ kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, in
   if (pool == nullptr || num_seqs < 0 || num_q_heads < 1 || max_q_len < 0 ||
       max_blocks_per_seq < 1 || max_context_len < 0)
     return KVQ_ERR_INVALID_ARG;
+  // the prefill kernel converts whole 16-token sub-tiles of one page
+  if (pool->view.bs == 8) return KVQ_ERR_UNSUPPORTED;
   if (num_seqs == 0 || max_q_len == 0) return KVQ_OK;
   if (q == nullptr || q_start == nullptr || block_table == nullptr || context_lens == nullptr ||
       out == nullptr)

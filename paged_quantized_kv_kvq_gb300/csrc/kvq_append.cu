@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<uint16_t*>(tile + v_tile_offset(tt, d0 + i, D, 2)) = hb[i];
+          *reinterpret_cast<uint16_t*>(tile + v_code_offset(tt, d0 + i, D, 2, pool.bs)) = hb[i];
       }
     } else {
       uint8_t code[8];
@@ -233,7 +233,8 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
         *reinterpret_cast<uint32_t*>(tile + k_tile_offset(tt, d0 + 4, D, 1)) = w1;
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) tile[v_tile_offset(tt, d0 + i, D, 1)] = static_cast<char>(code[i]);
+        for (int i = 0; i < 8; ++i)
+          tile[v_code_offset(tt, d0 + i, D, 1, pool.bs)] = static_cast<char>(code[i]);
       }
     }
   }
@@ -289,7 +290,7 @@ __global__ void kvq_read_slots_kernel(PoolView pool, const int64_t* slots, int64
           static_cast<int8_t>(static_cast<int>((w >> sh) & 0xFu) - static_cast<int>(kInt4Bias));
       continue;
     }
-    const int o = kv == 0 ? k_tile_offset(tt, d, D, es) : v_tile_offset(tt, d, D, es);
+    const int o = kv == 0 ? k_tile_offset(tt, d, D, es) : v_code_offset(tt, d, D, es, pool.bs);
     if (es == 2)
       reinterpret_cast<uint16_t*>(codes_out)[dst] = *reinterpret_cast<const uint16_t*>(tile + o);
     else  // INT8 codes are stored biased; hand back the signed code

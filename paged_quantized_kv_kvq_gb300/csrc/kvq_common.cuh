@@ -12,6 +12,7 @@
 //    nibbles biased by +8, see the INT4 sub-tile layout below)
 //   pages       : [num_blocks][kv_heads] pages of page_bytes each:
 //                   K codes : block_size/16 sub-tiles of 16 tokens x D
+//                             (block size 8: half a sub-tile, see below)
 //                   V codes : block_size/16 sub-tiles
 //                   K scales: [block_size][D/group] fp32   (per-group only)
 //                   V scales: [block_size][D/group] fp32   (per-group only)
@@ -74,6 +75,29 @@ __host__ __device__ inline int v_tile_offset(int t, int d, int D, int esize) {
   return (w / wpc) * 512 + lane * 16 + (w % wpc) * 4 * esize + e * esize;
 }
 
+// Block size 8: a page holds half a sub-tile.  Its K codes are the first half
+// of the K layout above (tokens 0..7 are the rows g of every lane, the first
+// half of each lane's words).  Its V codes use their own order, since a V word
+// above mixes tokens t and t+8: element (t, d) of an 8-token page sits in lane
+// ((d%8)*4 + t/2), word w = d/16, byte e = t%2 + 2*((d/8)%2), so that a lane's
+// word holds channels 16w + g and 16w + g + 8 at tokens 2j, 2j+1 -- the half of
+// the V^T A fragment that one page supplies; the next page of the sequence
+// supplies the other half (tokens 8 + 2j, 8 + 2j + 1).
+__host__ __device__ inline int v_half_offset(int t, int d, int D, int esize) {
+  (void)D;
+  const int lane = (d & 7) * 4 + (t >> 1);
+  const int w = d >> 4;
+  const int e = (t & 1) + 2 * ((d >> 3) & 1);
+  const int wpc = 4 / esize;
+  return (w / wpc) * 512 + lane * 16 + (w % wpc) * 4 * esize + e * esize;
+}
+
+// Byte offset of element (t, d) of the V codes of a sub-tile (block size 16
+// or more) or of an 8-token page.
+__host__ __device__ inline int v_code_offset(int t, int d, int D, int esize, int bs) {
+  return bs == 8 ? v_half_offset(t, d, D, esize) : v_tile_offset(t, d, D, esize);
+}
+
 // INT4 sub-tiles hold one 32-bit word per lane per 16-channel step: K word kk
 // of a lane carries channels 16kk + 4j .. +3 of tokens g and g+8 (lane =
 // 4g + j), V word mt carries tokens 2j, 2j+1, 2j+8, 2j+9 of channels 16mt + g
@@ -107,6 +131,7 @@ struct PoolView {
   int bs, Hkv, D, fmt, group, ng, esize;
   int sub_bytes;    // bytes of one 16-token sub-tile: 16 * D * esize (INT4: 8 * D)
   int code_bytes;   // bytes of K (or V) codes in one page = bs * sub_bytes / 16
+                    // (block size 8: half a sub-tile)
   int page_bytes;   // 2*code_bytes + (per-group) 2*bs*ng*4
 };
 

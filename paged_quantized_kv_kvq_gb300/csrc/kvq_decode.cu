@@ -22,8 +22,10 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
   const int stage_bytes = round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
   // Pages in flight per SM = CTAs per SM x W x stages; 3 CTAs x 4 warps x 4
   // stages keeps ~200 KB of copies in flight, above what HBM latency needs.
+  // Block size 8 consumes up to four pages per update, so keeps four stages.
+  const int min_stage = pool.bs == 8 ? 4 : 2;
   int nstage = kDecodeStages;
-  while (nstage > 2 && W * nstage * stage_bytes > 80 * 1024) --nstage;
+  while (nstage > min_stage && W * nstage * stage_bytes > 80 * 1024) --nstage;
   const int smem = round_up(W * nstage * stage_bytes + W * nstage * (8 + 4) + W * 4 + (S + 1) * 4,
                             128);
   if (smem > 227 * 1024) return false;
@@ -94,6 +96,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStrea
   l.smem = plan.smem_bytes;
   l.st = st;
   l.dependent = dependent;
+  if (a.pool.bs == 8)
+    return a.pool.fmt == FMT_INT8_GROUP ? launch_decode_bs8_group(l) : launch_decode_bs8_misc(l);
   switch (a.pool.fmt) {
     case FMT_INT8_GROUP: return launch_decode_int8_group(l);
     case FMT_INT4_GROUP: return launch_decode_int4_group(l);

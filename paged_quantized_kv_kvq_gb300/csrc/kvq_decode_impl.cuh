@@ -167,6 +167,16 @@ __device__ __forceinline__ void v_frag(const uint32_t* w, int mt, uint32_t& a0, 
   }
 }
 
+// The same fragment from the V words of two 8-token pages (block size 8),
+// interleaved per m-tile by load_v8: page A's word gives channels 16mt+g and
+// +8 at tokens 2j, 2j+1, page B's word the same at tokens 8+2j, 8+2j+1.
+template <int FMT>
+__device__ __forceinline__ void v_frag8(const uint32_t* w, int mt, uint32_t& a0, uint32_t& a1,
+                                        uint32_t& a2, uint32_t& a3) {
+  word_to_h2<FMT>(w, 2 * mt, a0, a1);
+  word_to_h2<FMT>(w, 2 * mt + 1, a2, a3);
+}
+
 // Copy a lane's share of a sub-tile from shared memory (16-byte chunks).
 template <int FMT, int D>
 __device__ __forceinline__ void load_lane_words(const char* tile, int lane, uint32_t* words) {
@@ -179,6 +189,40 @@ __device__ __forceinline__ void load_lane_words(const char* tile, int lane, uint
     words[4 * c + 2] = v.z;
     words[4 * c + 3] = v.w;
   }
+}
+
+// A lane's words of one 8-token page (half of lane_words), or zeros when the
+// page is absent.
+template <int FMT, int D>
+__device__ __forceinline__ void load_half_words(const char* page, int lane, uint32_t* words) {
+  constexpr int chunks = lane_words<FMT, D>() / 8;
+#pragma unroll
+  for (int c = 0; c < chunks; ++c) {
+    const uint4 v = page != nullptr ? *reinterpret_cast<const uint4*>(page + c * 512 + lane * 16)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+    words[4 * c + 0] = v.x;
+    words[4 * c + 1] = v.y;
+    words[4 * c + 2] = v.z;
+    words[4 * c + 3] = v.w;
+  }
+}
+
+// V words of a 16-token tile made of two 8-token pages, interleaved per m-tile
+// (A's 4-element group, then B's) for v_frag8.
+template <int FMT, int D>
+__device__ __forceinline__ void load_v8(const char* a, const char* b, int lane, uint32_t* words) {
+  constexpr int HALF = lane_words<FMT, D>() / 2;
+  constexpr int PER = FMT == FMT_FP16 ? 2 : 1;  // 32-bit words per 4-element group
+  uint32_t wa[HALF], wb[HALF];
+  load_half_words<FMT, D>(a, lane, wa);
+  load_half_words<FMT, D>(b, lane, wb);
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int x = 0; x < PER; ++x) {
+      words[2 * PER * mt + x] = wa[PER * mt + x];
+      words[2 * PER * mt + PER + x] = wb[PER * mt + x];
+    }
 }
 
 // Position of a warp in the unit-major page index space.
@@ -199,6 +243,7 @@ struct PairRegs {
   float ks[2][2][NS];  // [tile][row g | g+8][group]
   float vs[2][2][NS];
   const char* vtile[2];  // V codes in shared memory
+  const char* vtile_b[2];  // block size 8: V codes of the tile's second page (or null)
   int rows[2];
 };
 
@@ -232,11 +277,58 @@ __device__ __forceinline__ void load_tile(PairRegs<FMT, D, NG>& r, int t, const 
   r.rows[t] = rows;
 }
 
+// Fill tile t of `r` from two 8-token pages (block size 8): page A gives rows
+// 0..7, page B (null if absent) rows 8..15.  Rows valid: 0 .. rows-1.
+template <int FMT, int D, int NG>
+__device__ __forceinline__ void load_tile8(PairRegs<FMT, D, NG>& r, int t, const char* A,
+                                           const char* B, int rows, const PoolView& pool,
+                                           int lane) {
+  using T = FmtTraits<FMT>;
+  constexpr int NS = PairRegs<FMT, D, NG>::NS;
+  constexpr int HALF = PairRegs<FMT, D, NG>::NU32 / 2;
+  const int g = lane >> 2;
+  uint32_t wa[HALF], wb[HALF];
+  load_half_words<FMT, D>(A, lane, wa);
+  load_half_words<FMT, D>(B, lane, wb);
+#pragma unroll
+  for (int x = 0; x < HALF; ++x) {
+    r.kw[t][x] = wa[x];
+    r.kw[t][HALF + x] = wb[x];
+  }
+  r.vtile[t] = A + pool.code_bytes;
+  r.vtile_b[t] = B != nullptr ? B + pool.code_bytes : nullptr;
+  if constexpr (T::row_scales) {
+    // scales of token g of each page: [bs][NS] per group, [2][bs] per token
+    const int ko = T::group_scales ? 2 * pool.code_bytes : pool.page_bytes;
+    const int vo = T::group_scales ? 8 * NG * 4 : 8 * 4;
+    const float* ka = reinterpret_cast<const float*>(A + ko) + g * NS;
+    const float* va = reinterpret_cast<const float*>(A + ko + vo) + g * NS;
+#pragma unroll
+    for (int gi = 0; gi < NS; ++gi) {
+      r.ks[t][0][gi] = ka[gi];
+      r.vs[t][0][gi] = va[gi];
+    }
+    if (B != nullptr) {
+      const float* kb = reinterpret_cast<const float*>(B + ko) + g * NS;
+      const float* vb = reinterpret_cast<const float*>(B + ko + vo) + g * NS;
+#pragma unroll
+      for (int gi = 0; gi < NS; ++gi) {
+        r.ks[t][1][gi] = kb[gi];
+        r.vs[t][1][gi] = vb[gi];
+      }
+    } else {
+#pragma unroll
+      for (int gi = 0; gi < NS; ++gi) r.ks[t][1][gi] = r.vs[t][1][gi] = 0.f;
+    }
+  }
+  r.rows[t] = rows;
+}
+
 // One online-softmax update over two sub-tiles (32 tokens) for the up-to-8 Q
 // heads of a unit.  Lane (g = lane/4, j = lane%4) holds the scores of tokens g
 // and g+8 of each tile for heads 2j and 2j+1, and O^T rows 16mt+g, 16mt+g+8
 // for the same two heads.  Tile 1 may be empty (rows = 0).
-template <int FMT, int D, int NG>
+template <int FMT, int D, int NG, bool BS8 = false>
 __device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
                                              const uint32_t (&qb)[D / 16][2],
                                              const uint32_t (&ql)[FmtTraits<FMT>::channel ? D / 16 : 1][2],
@@ -380,8 +472,42 @@ __device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
   {
     uint32_t vwp[2][NU32];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) load_lane_words<FMT, D>(r.vtile[t], lane, vwp[t]);
-    if constexpr (T::maybe_nan) {
+    for (int t = 0; t < 2; ++t) {
+      if constexpr (BS8)
+        load_v8<FMT, D>(r.vtile[t], r.vtile_b[t], lane, vwp[t]);
+      else
+        load_lane_words<FMT, D>(r.vtile[t], lane, vwp[t]);
+    }
+    if constexpr (T::maybe_nan && BS8) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int rows = r.rows[t];
+        if (rows < 16) {
+          // page A's words hold tokens 2j, 2j+1 (rows of the tile), page B's
+          // tokens 8+2j, 8+2j+1; zero the ones past the context
+          const int t0 = 2 * j;
+          if constexpr (FMT == FMT_FP16) {
+            const uint32_t mlo = (t0 < rows ? 0xFFFFu : 0u) | (t0 + 1 < rows ? 0xFFFF0000u : 0u);
+            const uint32_t mhi = (t0 + 8 < rows ? 0xFFFFu : 0u) | (t0 + 9 < rows ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              vwp[t][4 * mt] &= mlo;
+              vwp[t][4 * mt + 1] &= mlo;
+              vwp[t][4 * mt + 2] &= mhi;
+              vwp[t][4 * mt + 3] &= mhi;
+            }
+          } else {
+            const uint32_t mlo = (t0 < rows ? 0x00FF00FFu : 0u) | (t0 + 1 < rows ? 0xFF00FF00u : 0u);
+            const uint32_t mhi = (t0 + 8 < rows ? 0x00FF00FFu : 0u) | (t0 + 9 < rows ? 0xFF00FF00u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              vwp[t][2 * mt] &= mlo;
+              vwp[t][2 * mt + 1] &= mhi;
+            }
+          }
+        }
+      }
+    } else if constexpr (T::maybe_nan) {
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int rows = r.rows[t];
@@ -413,7 +539,10 @@ __device__ __forceinline__ void compute_pair(PairRegs<FMT, D, NG>& r, int lane,
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         uint32_t a0, a1, a2, a3;
-        v_frag<FMT>(vwp[t], mt, a0, a1, a2, a3);
+        if constexpr (BS8)
+          v_frag8<FMT>(vwp[t], mt, a0, a1, a2, a3);
+        else
+          v_frag<FMT>(vwp[t], mt, a0, a1, a2, a3);
         mma_16816(o[mt], a0, a1, a2, a3, bh0[t][gi], bh1[t][gi]);
         mma_16816(o[mt], a0, a1, a2, a3, bl0[t][gi], bl1[t][gi]);
       }
@@ -473,7 +602,7 @@ __device__ __forceinline__ void load_q(const DecodeParams& p, int s, int h, int 
   }
 }
 
-template <int FMT, int D, int NG>
+template <int FMT, int D, int NG, bool BS8>
 __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     kvq_decode_kernel(const DecodeParams p) {
   using T = FmtTraits<FMT>;
@@ -787,36 +916,82 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   bool failed = false;
   while (i < n_w) {
     // pages consumed this step: a pair of one-sub-tile pages of the same unit,
-    // or one page of two or more sub-tiles
-    const bool two = bs == 16 && i + 1 < n_w && cc.pi + 1 < cc.Ps;
-    const int npg = two ? 2 : 1;
-    const bool wrap1 = cst + 1 == nstage;
-    const int st0 = cst, st1 = wrap1 ? 0 : cst + 1;
-    if (!wait_stage(st0, cph) || (two && !wait_stage(st1, wrap1 ? cph ^ 1u : cph))) {
-      failed = true;
-      break;
-    }
+    // or one page of two or more sub-tiles; block size 8: up to four pages
+    // (two 16-token tiles of two pages each), all of the same unit
+    int npg;
+    if constexpr (BS8)
+      npg = min(4, min(n_w - i, cc.Ps - cc.pi));
+    else
+      npg = (bs == 16 && i + 1 < n_w && cc.pi + 1 < cc.Ps) ? 2 : 1;
     auto issue_after = [&]() {
       for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
     };
-    if (two) {
-      const int r0 = stage_phys[st0] >= 0 ? min(16, L - cc.pi * 16) : 0;
-      const int r1 = stage_phys[st1] >= 0 ? min(16, L - (cc.pi + 1) * 16) : 0;
-      // an absent page (rows = 0) contributes nothing; keep the valid one in tile 0
-      const int sA = r0 > 0 ? st0 : st1;
-      load_tile<FMT, D, NG>(R, 0, stages + sA * p.stage_bytes, 0, r0 > 0 ? r0 : r1, pool, lane);
-      load_tile<FMT, D, NG>(R, 1, stages + st1 * p.stage_bytes, 0, r0 > 0 ? r1 : 0, pool, lane);
-      compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
+    if constexpr (BS8) {
+      bool ok = true;
+      const char* pg[4];
+      int rp[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pg[k] = nullptr;
+        rp[k] = 0;
+        if (k < npg && ok) {
+          const bool wrap = cst + k >= nstage;  // nstage >= 4 for block size 8
+          const int st = wrap ? cst + k - nstage : cst + k;
+          ok = wait_stage(st, wrap ? cph ^ 1u : cph);
+          pg[k] = stages + st * p.stage_bytes;
+          rp[k] = stage_phys[st] >= 0 ? max(0, min(8, L - (cc.pi + k) * 8)) : 0;
+        }
+      }
+      if (!ok) {
+        failed = true;
+        break;
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const char* A = pg[2 * t];
+        const char* B = pg[2 * t + 1];
+        int ra = rp[2 * t], rb = rp[2 * t + 1];
+        if (ra == 0) {  // an absent page contributes nothing: the tile is page B alone
+          A = B;
+          ra = rb;
+          B = nullptr;
+          rb = 0;
+        }
+        if (ra < 8) {  // a short first page ends its unit: no second page
+          B = nullptr;
+          rb = 0;
+        }
+        if (A == nullptr) A = pg[0];  // an empty tile reads any staged page, all rows masked
+        load_tile8<FMT, D, NG>(R, t, A, B, ra + rb, pool, lane);
+      }
+      compute_pair<FMT, D, NG, true>(R, lane, qb, ql, csc, m, l, E, o);
     } else {
-      const char* stage = stages + st0 * p.stage_bytes;
-      const int nvalid = stage_phys[st0] >= 0 ? min(bs, L - cc.pi * bs) : 0;
-      const int nsub = (nvalid + 15) >> 4;
-      for (int sp = 0; sp < nsub; sp += 2) {
-        const int rA = min(16, nvalid - sp * 16);
-        const int rB = sp + 1 < nsub ? min(16, nvalid - (sp + 1) * 16) : 0;
-        load_tile<FMT, D, NG>(R, 0, stage, sp, rA, pool, lane);
-        load_tile<FMT, D, NG>(R, 1, stage, sp + 1 < nsub ? sp + 1 : sp, rB, pool, lane);
+      const bool two = npg == 2;
+      const bool wrap1 = cst + 1 == nstage;
+      const int st0 = cst, st1 = wrap1 ? 0 : cst + 1;
+      if (!wait_stage(st0, cph) || (two && !wait_stage(st1, wrap1 ? cph ^ 1u : cph))) {
+        failed = true;
+        break;
+      }
+      if (two) {
+        const int r0 = stage_phys[st0] >= 0 ? min(16, L - cc.pi * 16) : 0;
+        const int r1 = stage_phys[st1] >= 0 ? min(16, L - (cc.pi + 1) * 16) : 0;
+        // an absent page (rows = 0) contributes nothing; keep the valid one in tile 0
+        const int sA = r0 > 0 ? st0 : st1;
+        load_tile<FMT, D, NG>(R, 0, stages + sA * p.stage_bytes, 0, r0 > 0 ? r0 : r1, pool, lane);
+        load_tile<FMT, D, NG>(R, 1, stages + st1 * p.stage_bytes, 0, r0 > 0 ? r1 : 0, pool, lane);
         compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
+      } else {
+        const char* stage = stages + st0 * p.stage_bytes;
+        const int nvalid = stage_phys[st0] >= 0 ? min(bs, L - cc.pi * bs) : 0;
+        const int nsub = (nvalid + 15) >> 4;
+        for (int sp = 0; sp < nsub; sp += 2) {
+          const int rA = min(16, nvalid - sp * 16);
+          const int rB = sp + 1 < nsub ? min(16, nvalid - (sp + 1) * 16) : 0;
+          load_tile<FMT, D, NG>(R, 0, stage, sp, rA, pool, lane);
+          load_tile<FMT, D, NG>(R, 1, stage, sp + 1 < nsub ? sp + 1 : sp, rB, pool, lane);
+          compute_pair<FMT, D, NG>(R, lane, qb, ql, csc, m, l, E, o);
+        }
       }
     }
     // every lane is done with the stage(s): hand them back to the copy engine
@@ -958,14 +1133,14 @@ struct DecodeLaunch {
 
 constexpr int kMaxDevices = 64;
 
-template <int FMT, int D, int NG>
+template <int FMT, int D, int NG, bool BS8 = false>
 cudaError_t run_decode(const DecodeLaunch& l) {
   static bool attr_set[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDevices && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kvq_decode_kernel<FMT, D, NG>,
+    e = cudaFuncSetAttribute(kvq_decode_kernel<FMT, D, NG, BS8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -981,7 +1156,7 @@ cudaError_t run_decode(const DecodeLaunch& l) {
     da[0].val.programmaticStreamSerializationAllowed = 1;
     dc.attrs = da;
     dc.numAttrs = l.dependent ? 1 : 0;
-    e = cudaLaunchKernelEx(&dc, kvq_decode_kernel<FMT, D, NG>, l.p);
+    e = cudaLaunchKernelEx(&dc, kvq_decode_kernel<FMT, D, NG, BS8>, l.p);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -997,13 +1172,34 @@ cudaError_t run_decode(const DecodeLaunch& l) {
   return cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D>, l.p);
 }
 
-template <int FMT>
+template <int FMT, bool BS8 = false>
 cudaError_t run_decode_d(const DecodeLaunch& l) {
   switch (l.p.pool.D) {
-    case 64: return run_decode<FMT, 64, 1>(l);
-    case 128: return run_decode<FMT, 128, 1>(l);
+    case 64: return run_decode<FMT, 64, 1, BS8>(l);
+    case 128: return run_decode<FMT, 128, 1, BS8>(l);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Per-group formats: NG = head_dim / group scale groups per head.
+template <int FMT, bool BS8 = false>
+cudaError_t run_decode_group(const DecodeLaunch& l) {
+  const int D = l.p.pool.D, ng = l.p.pool.ng;
+  if (D == 64) {
+    switch (ng) {
+      case 1: return run_decode<FMT, 64, 1, BS8>(l);
+      case 2: return run_decode<FMT, 64, 2, BS8>(l);
+      case 4: return run_decode<FMT, 64, 4, BS8>(l);
+    }
+  } else if (D == 128) {
+    switch (ng) {
+      case 1: return run_decode<FMT, 128, 1, BS8>(l);
+      case 2: return run_decode<FMT, 128, 2, BS8>(l);
+      case 4: return run_decode<FMT, 128, 4, BS8>(l);
+      case 8: return run_decode<FMT, 128, 8, BS8>(l);
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq

@@ -103,5 +103,7 @@ cudaError_t launch_decode_fp16(const DecodeLaunch& l);
 cudaError_t launch_decode_token(const DecodeLaunch& l);
 cudaError_t launch_decode_channel(const DecodeLaunch& l);
 cudaError_t launch_decode_e5m2(const DecodeLaunch& l);
+cudaError_t launch_decode_bs8_group(const DecodeLaunch& l);  // block size 8, INT8 per-group
+cudaError_t launch_decode_bs8_misc(const DecodeLaunch& l);   // block size 8, the other formats
 
 }  // namespace kvq

@@ -42,10 +42,13 @@ HALF_BYTES = {kvq.KVQ_FP16: 4, kvq.KVQ_INT8_PER_TOKEN: 2, kvq.KVQ_INT8_PER_CHANN
                                          (kvq.KVQ_INT8_PER_GROUP, 64), (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0),
                                          (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_INT4_PER_GROUP, 32),
                                          (kvq.KVQ_FP8_E5M2, 0)])
-@pytest.mark.parametrize("nb,bs,hkv,d", [(9103, 16, 8, 128), (64, 16, 1, 64), (100, 32, 32, 128)])
+@pytest.mark.parametrize("nb,bs,hkv,d", [(9103, 16, 8, 128), (64, 16, 1, 64), (100, 32, 32, 128),
+                                         (300, 8, 8, 128), (17, 8, 2, 64)])
 def test_code_bytes_follow_formula(L, dtype, group, nb, bs, hkv, d):
     if dtype in kvq.GROUP_FORMATS and d % group:
         group = d
+    if bs == 8 and dtype == kvq.KVQ_INT4_PER_GROUP:
+        pytest.skip("INT4 takes block sizes that are multiples of 16")
     lay = kvq.kvq_pool_layout_query(nb, bs, hkv, d, dtype, group)
     tokens = nb * bs  # whole blocks
     # the size formula with the element size in half bytes, halved
@@ -76,7 +79,9 @@ def test_layer_stack_matches_formula(L):
     ((8, 16, 8, 100, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_INVALID_ARG),
     ((8, 16, 8, 128, kvq.KVQ_INT8_PER_GROUP, 48), kvq.KVQ_ERR_INVALID_ARG),
     ((8, 16, 8, 128, kvq.KVQ_INT8_PER_GROUP, 8), kvq.KVQ_ERR_UNSUPPORTED),
-    ((8, 8, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
+    ((8, 24, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
+    ((8, 4, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
+    ((8, 8, 8, 128, kvq.KVQ_INT4_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
     ((8, 16, 8, 256, kvq.KVQ_FP16, 0), kvq.KVQ_ERR_UNSUPPORTED),
     ((8, 16, 8, 128, 9, 0), kvq.KVQ_ERR_INVALID_ARG),
 ])

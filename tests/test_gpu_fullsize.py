@@ -114,6 +114,11 @@ def test_gqa_64x2048_full(name):
     _check(name, 0, [0, 31, 63])
 
 
+def test_gqa_64x2048_block8_full():
+    # the same batch in 8-token blocks: every tile pairs two pages
+    _check("gqa_64x2048", 0, [0, 31, 63], bs=8)
+
+
 @pytest.mark.parametrize("name", ["mha_100_fp16", "mha_100_fp8", "mha_100_int8ch",
                                   "mha_100_int8g64"])
 def test_mha_100_full(name):
