@@ -357,21 +357,24 @@ def run_ours(args, rank, world, local_rank):
             kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l], ws,
                                  0, stream)
 
+    def layer_step(l, qq, kk, vv, sl, ln, oo):
+        if fused and P:
+            kvq.kvq_cascade_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln,
+                                        max_ctx, P, sm_scale, oo[l], ws, stream)
+        elif fused:
+            # one call: append at position L-1 (slot from the block table),
+            # then the decode as a programmatic dependent of the append
+            kvq.kvq_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln, max_ctx,
+                                sm_scale, oo[l], ws, stream)
+        else:
+            pools[l].append(kk[l], vv[l], sl, stream)
+            decode_call(l, qq, ln, oo)
+
     # No events between layers inside a step: an event record between two
     # kernels ends the programmatic-dependent overlap of the launches.
     def step(qq, kk, vv, sl, ln, oo):
         for l in range(L):
-            if fused and P:
-                kvq.kvq_cascade_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln,
-                                            max_ctx, P, sm_scale, oo[l], ws, stream)
-            elif fused:
-                # one call: append at position L-1 (slot from the block table),
-                # then the decode as a programmatic dependent of the append
-                kvq.kvq_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln, max_ctx,
-                                    sm_scale, oo[l], ws, stream)
-            else:
-                pools[l].append(kk[l], vv[l], sl, stream)
-                decode_call(l, qq, ln, oo)
+            layer_step(l, qq, kk, vv, sl, ln, oo)
 
     for _ in range(args.warmup):
         step(q, kn, vn, slots, lens, out)
@@ -430,15 +433,51 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(x.numel() * x.element_size() for x in h2d_in)
     d2h = out_h.numel() * out_h.element_size()
 
+    # The copies overlap the layers, as a serving loop would run them: the
+    # inputs go up on one copy stream in two chunks (the first IN0 layers, then
+    # the rest, which lands while those run), the outputs come back on another
+    # in chunks of OUT_CH layers as they complete.  Few chunks, because each
+    # event between two launches ends their programmatic-dependent overlap.
+    # Everything lies between the step's first and last event on the compute
+    # stream: the copy streams start after the first, the compute stream waits
+    # for the last read-back.
+    cp_in, cp_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    IN0, OUT_CH = min(4, L), 8
+    in_chunks = [(0, IN0)] + ([(IN0, L)] if L > IN0 else [])
+
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        kn_d.copy_(kn_h, non_blocking=True)
-        vn_d.copy_(vn_h, non_blocking=True)
-        if not fused:
-            sl_d.copy_(sl_h, non_blocking=True)
-        ln_d.copy_(ln_h, non_blocking=True)
-        step(q_d, kn_d, vn_d, sl_d, ln_d, out)
-        out_h.copy_(out, non_blocking=True)
+        go = torch.cuda.Event()
+        go.record(stream)
+        cp_in.wait_event(go)
+        cp_out.wait_event(go)
+        in_ev = []
+        with torch.cuda.stream(cp_in):
+            ln_d.copy_(ln_h, non_blocking=True)
+            if not fused:
+                sl_d.copy_(sl_h, non_blocking=True)
+            for a, b_ in in_chunks:
+                q_d[a:b_].copy_(q_h[a:b_], non_blocking=True)
+                kn_d[a:b_].copy_(kn_h[a:b_], non_blocking=True)
+                vn_d[a:b_].copy_(vn_h[a:b_], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cp_in)
+                in_ev.append(ev)
+        o0 = 0
+        for l in range(L):
+            for c, (a, _) in enumerate(in_chunks):
+                if l == a:
+                    stream.wait_event(in_ev[c])
+            layer_step(l, q_d, kn_d, vn_d, sl_d, ln_d, out)
+            if (l + 1) % OUT_CH == 0 or l == L - 1:
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                cp_out.wait_event(ev)
+                with torch.cuda.stream(cp_out):
+                    out_h[o0:l + 1].copy_(out[o0:l + 1], non_blocking=True)
+                o0 = l + 1
+        done = torch.cuda.Event()
+        done.record(cp_out)
+        stream.wait_event(done)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -498,7 +537,10 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": "%s hbm_gbs" % peak_kind},
         "e2e": {"value": round(job_gbs(step_total, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": K2},
+                "d2h_bytes_per_step": d2h, "steps": K2,
+                "overlap": "inputs in two chunks (first %d layers, then the rest) and outputs in "
+                           "chunks of %d layers on two copy streams, overlapping the layers"
+                           % (IN0, OUT_CH)},
         "gpu_launches": K * L * launches_per_layer,
         "clocks": clocks,
     }
