@@ -78,6 +78,39 @@ def test_decode_step_workloads(name, kw):
     pool.close()
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (24, 2), (8, 1), (4, 4)])
+def test_decode_step_head_tiles(hq, hkv):
+    # MQA with four head tiles of 8, GQA 12:1 (a ragged tile), 8:1 (one full
+    # tile) and MHA, with the per-token format whose scale spans every kv head
+    # of the token: the oracle's codes and the separate calls' bits.
+    w = synth.workload("gqa_64x2048", S=3, L=130, layers=1)
+    w.Hq, w.Hkv = hq, hkv
+    w.outlier_channels = w.outlier_channels[w.outlier_channels[:, 0] < hkv]
+    fmt, group = kvq.KVQ_INT8_PER_TOKEN, 0
+    w.layer_formats = [(fmt, group)]
+    k, v, slots = layer_tokens(w, 0)
+    S = w.S
+    pool = gpu_pool(w, fmt, group, DEV, k[:-S], v[:-S], slots[:-S])
+    ref, table, remap = oracle_layer(w, fmt, group, k, v, slots, list(range(S)))
+    q = synth.queries(w, 0)
+    out = pool.decode_step(_t(k[-S:]), _t(v[-S:]), _t(q), _t(w.block_table), _t(w.context_lens),
+                           int(w.context_lens.max()))
+    torch.cuda.synchronize()
+    assert pool.error() == kvq.KVQ_OK
+    codes, scales = pool.read_slots(_t(slots[-S:]))
+    rs = oracle_slots(remap, slots[-S:], w.bs)
+    np.testing.assert_array_equal(codes.cpu().numpy().view(np.uint8), ref.codes[rs].view(np.uint8))
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint32), ref.scales[rs].view(np.uint32))
+    got = out.cpu().numpy()
+    np.testing.assert_allclose(got, ref.decode(q, table, w.context_lens), rtol=0, atol=TOL)
+    pool2 = gpu_pool(w, fmt, group, DEV, k, v, slots)
+    sep = pool2.decode(_t(q), _t(w.block_table), _t(w.context_lens), int(w.context_lens.max()))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(sep.cpu().numpy(), got)
+    pool.close()
+    pool2.close()
+
+
 def test_decode_step_edges():
     """L == 0 stores nothing and outputs zeros; L > max_context_len stores
     nothing and is flagged; an unmapped block at L-1 is flagged, not written."""
