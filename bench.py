@@ -349,38 +349,73 @@ def run_ours(args, rank, world, local_rank):
 
     fused = args.step_api == "fused"
 
-    def decode_call(l, qq, ln, oo):
+    def decode_call(l, qq, ln, oo, st=None):
+        st = stream if st is None else st
         if P:
             kvq.kvq_cascade_decode(pools[l].handle, qq[l], table, ln, max_ctx, P, sm_scale, oo[l],
-                                   ws, stream)
+                                   ws, st)
         else:
             kvq.kvq_paged_decode(pools[l].handle, qq[l], table, ln, max_ctx, sm_scale, oo[l], ws,
-                                 0, stream)
+                                 0, st)
 
-    def layer_step(l, qq, kk, vv, sl, ln, oo):
+    def layer_step(l, qq, kk, vv, sl, ln, oo, st=None):
+        st = stream if st is None else st
         if fused and P:
             kvq.kvq_cascade_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln,
-                                        max_ctx, P, sm_scale, oo[l], ws, stream)
+                                        max_ctx, P, sm_scale, oo[l], ws, st)
         elif fused:
             # one call: append at position L-1 (slot from the block table),
             # then the decode as a programmatic dependent of the append
             kvq.kvq_decode_step(pools[l].handle, kk[l], vv[l], qq[l], table, ln, max_ctx,
-                                sm_scale, oo[l], ws, stream)
+                                sm_scale, oo[l], ws, st)
         else:
-            pools[l].append(kk[l], vv[l], sl, stream)
-            decode_call(l, qq, ln, oo)
+            pools[l].append(kk[l], vv[l], sl, st)
+            decode_call(l, qq, ln, oo, st)
 
     # No events between layers inside a step: an event record between two
     # kernels ends the programmatic-dependent overlap of the launches.
-    def step(qq, kk, vv, sl, ln, oo):
+    def step(qq, kk, vv, sl, ln, oo, st=None):
         for l in range(L):
-            layer_step(l, qq, kk, vv, sl, ln, oo)
+            layer_step(l, qq, kk, vv, sl, ln, oo, st)
 
     for _ in range(args.warmup):
         step(q, kn, vn, slots, lens, out)
     torch.cuda.synchronize()
     for p in pools:
         assert p.error() == kvq.KVQ_OK
+
+    # The step as one CUDA graph (the same calls captured once, every kernel
+    # and programmatic edge kept), replayed each timed step, as a serving loop
+    # replays its decode graph; plain stream launches if capture is refused.
+    launch = "stream"
+    graph = None
+    if not args.no_graph:
+        try:
+            cap = torch.cuda.Stream(device=dev)
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                step(q, kn, vn, slots, lens, out, cap)
+            cap.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                step(q, kn, vn, slots, lens, out, cap)
+            torch.cuda.synchronize()
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize()
+            launch = "graph"
+        except Exception as e:  # noqa: BLE001 -- reported in the JSON line
+            graph = None
+            launch = "stream (graph capture refused: %s)" % str(e).splitlines()[0][:120]
+            torch.cuda.synchronize()
+    for p in pools:
+        assert p.error() == kvq.KVQ_OK
+
+    def timed_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step(q, kn, vn, slots, lens, out)
 
     dist = None
     if world > 1:
@@ -400,7 +435,7 @@ def run_ours(args, rank, world, local_rank):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(K):
-        step(q, kn, vn, slots, lens, out)
+        timed_step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -543,6 +578,7 @@ def run_ours(args, rank, world, local_rank):
                            "chunks of %d layers on two copy streams, overlapping the layers"
                            % (IN0, OUT_CH)},
         "gpu_launches": K * L * launches_per_layer,
+        "launch": launch,
         "clocks": clocks,
     }
     del pools
@@ -712,6 +748,8 @@ def main():
                     help="prompts in the prefill batch (--op prefill)")
     ap.add_argument("--block-size", type=int, default=None,
                     help="tokens per block (default: the workload's; 8 or a multiple of 16)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the step as plain stream launches instead of a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers (profiling runs only; the bench line uses all)")
     args = ap.parse_args()
