@@ -480,9 +480,10 @@ def run_ours(args, rank, world, local_rank):
     IN0, OUT_CH = min(4, L), 8
     in_chunks = [(0, IN0)] + ([(IN0, L)] if L > IN0 else [])
 
-    def e2e_step():
+    def e2e_step(st=None):
+        st = stream if st is None else st
         go = torch.cuda.Event()
-        go.record(stream)
+        go.record(st)
         cp_in.wait_event(go)
         cp_out.wait_event(go)
         in_ev = []
@@ -501,28 +502,57 @@ def run_ours(args, rank, world, local_rank):
         for l in range(L):
             for c, (a, _) in enumerate(in_chunks):
                 if l == a:
-                    stream.wait_event(in_ev[c])
-            layer_step(l, q_d, kn_d, vn_d, sl_d, ln_d, out)
+                    st.wait_event(in_ev[c])
+            layer_step(l, q_d, kn_d, vn_d, sl_d, ln_d, out, st)
             if (l + 1) % OUT_CH == 0 or l == L - 1:
                 ev = torch.cuda.Event()
-                ev.record(stream)
+                ev.record(st)
                 cp_out.wait_event(ev)
                 with torch.cuda.stream(cp_out):
                     out_h[o0:l + 1].copy_(out[o0:l + 1], non_blocking=True)
                 o0 = l + 1
         done = torch.cuda.Event()
         done.record(cp_out)
-        stream.wait_event(done)
+        st.wait_event(done)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
+    # the whole end-to-end step (copies on their streams included) as one
+    # graph too, when the step itself was captured
+    e2e_launch = "stream"
+    e2e_graph = None
+    if graph is not None:
+        try:
+            cap2 = torch.cuda.Stream(device=dev)
+            cap2.wait_stream(stream)
+            e2e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graph, stream=cap2):
+                e2e_step(cap2)
+            torch.cuda.synchronize()
+            for _ in range(max(1, args.warmup)):
+                e2e_graph.replay()
+            torch.cuda.synchronize()
+            e2e_launch = "graph"
+        except Exception as e:  # noqa: BLE001 -- reported in the JSON line
+            e2e_graph = None
+            e2e_launch = "stream (graph capture refused: %s)" % str(e).splitlines()[0][:120]
+            torch.cuda.synchronize()
+            # fresh copy streams, in case the failed capture left its mark on them
+            cp_in, cp_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_timed():
+        if e2e_graph is not None:
+            e2e_graph.replay()
+        else:
+            e2e_step()
+
     K2 = max(1, min(K, 50))
     barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(K2):
-        e2e_step()
+        e2e_timed()
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / K2, dist, dev)
@@ -576,7 +606,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h, "steps": K2,
                 "overlap": "inputs in two chunks (first %d layers, then the rest) and outputs in "
                            "chunks of %d layers on two copy streams, overlapping the layers"
-                           % (IN0, OUT_CH)},
+                           % (IN0, OUT_CH), "launch": e2e_launch},
         "gpu_launches": K * L * launches_per_layer,
         "launch": launch,
         "clocks": clocks,
