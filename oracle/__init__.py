@@ -2,7 +2,7 @@
 
 This package is a plain, slow restatement of the method, written to check the
 CUDA library against.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
-CPU-baseline leg of ``bench.py`` may import it.  The product package never
+CPU-baseline leg and ``--impl reference`` arm of ``bench.py`` may import it.  The product package never
 imports it and shares no code with it; the only thing both sides share is the
 seeded input generator module, which holds none of the method's arithmetic.
 
