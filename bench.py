@@ -777,7 +777,7 @@ def main():
     ap.add_argument("--prefill-seqs", type=int, default=8,
                     help="prompts in the prefill batch (--op prefill)")
     ap.add_argument("--block-size", type=int, default=None,
-                    help="tokens per block (default: the workload's; 8 or a multiple of 16)")
+                    help="tokens per block (default: the workload's; 8, 16, 32 or 64)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step as plain stream launches instead of a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,

@@ -97,10 +97,10 @@ size_t kvq_pool_bytes(int64_t num_blocks, int block_size, int kv_heads, int head
  * 16 tokens, reached through a per-request block table; [P312] §三: blocks of
  * 16 or 32 tokens).
  *   num_blocks : physical blocks (>= 1)
- *   block_size : tokens per block: 8, or a multiple of 16 up to 256 ([KVC]
- *                §3.2: 8 for short contexts at high concurrency, 16 or 32 for
- *                long ones).  INT4 pools take multiples of 16 only; pools of
- *                8-token blocks serve append, decode and block copy, while
+ *   block_size : tokens per block: 8, 16, 32 or 64 ([KVC] §3.2: 8 for short
+ *                contexts at high concurrency, 16 or 32 for long ones); other
+ *                sizes return UNSUPPORTED.  INT4 pools take 16 or more; pools
+ *                of 8-token blocks serve append, decode and block copy, while
  *                kvq_prefill and the cascade with prefix_blocks > 0 refuse
  *                them with UNSUPPORTED.
  *   kv_heads   : KV heads (>= 1); head_dim: 64 or 128
@@ -209,7 +209,11 @@ size_t kvq_decode_workspace_bytes(const kvq_pool* pool, int num_seqs, int num_q_
  * out = softmax(q . k^T * sm_scale) v over tokens 0..L-1, with k^, v^ = code * scale.
  * A sequence with L == 0 gets zeros.  Device errors: a block id outside the
  * pool sets OUT_OF_RANGE and that block is skipped; L > max_context_len sets
- * OUT_OF_RANGE and L is clamped. */
+ * OUT_OF_RANGE and L is clamped.  Host errors beyond the argument checks:
+ * UNSUPPORTED when num_seqs > 65535 or when two shared-memory stages of one
+ * (block, kv head) page for each of a CTA's 4 warps exceed 227 KB (FP16
+ * pages of 64-token blocks at head_dim 128); the workspace query then
+ * returns 0. */
 kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs,
                             int num_q_heads, const int32_t* block_table,
                             int max_blocks_per_seq, const int32_t* context_lens,

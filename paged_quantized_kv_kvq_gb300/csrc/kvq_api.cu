@@ -32,9 +32,10 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
   if (num_blocks < 1 || bs < 1 || Hkv < 1 || D < 1 || !valid_dtype(dtype) || lay == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (D % 16 != 0) return KVQ_ERR_INVALID_ARG;
-  // blocks of 8 tokens (half a sub-tile per page) or multiples of 16; INT4's
-  // words pack tokens t and t+8 together and take multiples of 16 only
-  if ((bs % 16 != 0 && bs != 8) || bs > 256) return KVQ_ERR_UNSUPPORTED;
+  // blocks of 8 tokens (half a sub-tile per page), 16, 32 or 64 -- the sizes
+  // the kernels have been run and checked at; INT4's words pack tokens t and
+  // t+8 together and take 16 or more
+  if (bs != 8 && bs != 16 && bs != 32 && bs != 64) return KVQ_ERR_UNSUPPORTED;
   if (bs == 8 && dtype == KVQ_INT4_PER_GROUP) return KVQ_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
   int ng = 1;

@@ -80,6 +80,9 @@ def test_layer_stack_matches_formula(L):
     ((8, 16, 8, 128, kvq.KVQ_INT8_PER_GROUP, 48), kvq.KVQ_ERR_INVALID_ARG),
     ((8, 16, 8, 128, kvq.KVQ_INT8_PER_GROUP, 8), kvq.KVQ_ERR_UNSUPPORTED),
     ((8, 24, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
+    ((8, 48, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
+    ((8, 96, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
+    ((8, 128, 8, 64, kvq.KVQ_FP16, 0), kvq.KVQ_ERR_UNSUPPORTED),
     ((8, 4, 8, 128, kvq.KVQ_INT8_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
     ((8, 8, 8, 128, kvq.KVQ_INT4_PER_GROUP, 128), kvq.KVQ_ERR_UNSUPPORTED),
     ((8, 16, 8, 256, kvq.KVQ_FP16, 0), kvq.KVQ_ERR_UNSUPPORTED),

@@ -128,6 +128,7 @@ def test_tiny_workload_full():
     ("mha_100_fp16", dict(S=5, L=300)), ("mha_100_fp8", dict(S=5, L=300)),
     ("mha_100_int8ch", dict(S=5, L=300)), ("mha_100_int8g64", dict(S=5, L=300)),
     ("long_8x32k", dict(S=1, L=3001, bs=16)), ("long_8x32k", dict(S=1, L=3001, bs=32)),
+    ("long_8x32k", dict(S=2, L=3001, bs=64)),
     ("mixed_256", dict(S=5, L=200, layers=2)), ("gqa_64x2048_int4", dict(S=3, L=500)),
     ("gqa_64x2048_e5m2", dict(S=3, L=500)),
 ])
@@ -247,6 +248,24 @@ def test_device_range_errors_do_not_fault():
     np.testing.assert_array_equal(run_gpu_decode(pool, w, q, DEV), good)
     assert pool.error() == kvq.KVQ_OK
     pool.close()
+
+
+def test_block_size_past_the_shared_memory_stages_is_refused():
+    # head_dim 128, FP16 blocks of 64 tokens: two 32 KB stages for each of 4
+    # warps exceed the shared memory of a CTA, so the decode refuses before
+    # launching anything; INT8 blocks of 64 fit
+    big = kvq.KVPool(8, 64, 2, 128, kvq.KVQ_FP16, 0, device=DEV)
+    assert kvq.kvq_decode_workspace_bytes(big.handle, 1, 2, 64) == 0
+    q = torch.zeros((1, 2, 128), dtype=torch.float16, device=DEV)
+    t = torch.zeros((1, 8), dtype=torch.int32, device=DEV)
+    ln = torch.ones(1, dtype=torch.int32, device=DEV)
+    with pytest.raises(kvq.KVQError) as ei:
+        big.decode(q, t, ln, 64)
+    assert ei.value.status == kvq.KVQ_ERR_UNSUPPORTED
+    big.close()
+    ok = kvq.KVPool(8, 64, 2, 128, kvq.KVQ_INT8_PER_GROUP, 128, device=DEV)
+    assert kvq.kvq_decode_workspace_bytes(ok.handle, 1, 2, 64) > 0
+    ok.close()
 
 
 def test_host_validation():
