@@ -33,8 +33,8 @@ kvq_status layout_for(int64_t num_blocks, int bs, int Hkv, int D, int dtype, int
     return KVQ_ERR_INVALID_ARG;
   if (D % 16 != 0) return KVQ_ERR_INVALID_ARG;
   // blocks of 8 tokens (half a sub-tile per page), 16, 32 or 64 -- the sizes
-  // the kernels have been run and checked at; INT4's words pack tokens t and
-  // t+8 together and take 16 or more
+  // the kernels have been run and checked at (others are refused until they
+  // have); INT4's words pack tokens t and t+8 together and take 16 or more
   if (bs != 8 && bs != 16 && bs != 32 && bs != 64) return KVQ_ERR_UNSUPPORTED;
   if (bs == 8 && dtype == KVQ_INT4_PER_GROUP) return KVQ_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
