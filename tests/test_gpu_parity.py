@@ -128,7 +128,7 @@ def test_tiny_workload_full():
     ("mha_100_fp16", dict(S=5, L=300)), ("mha_100_fp8", dict(S=5, L=300)),
     ("mha_100_int8ch", dict(S=5, L=300)), ("mha_100_int8g64", dict(S=5, L=300)),
     ("long_8x32k", dict(S=1, L=3001, bs=16)), ("long_8x32k", dict(S=1, L=3001, bs=32)),
-    ("long_8x32k", dict(S=2, L=3001, bs=64)),
+    ("long_8x32k", dict(S=1, L=3001, bs=64)),
     ("mixed_256", dict(S=5, L=200, layers=2)), ("gqa_64x2048_int4", dict(S=3, L=500)),
     ("gqa_64x2048_e5m2", dict(S=3, L=500)),
 ])
