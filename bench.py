@@ -184,6 +184,46 @@ def gpu_index(local_rank):
     return local_rank
 
 
+# ----------------------------------------------------------------- kernel breakdown
+def kernel_breakdown(run, reps, layers, ms_step):
+    """Device time of each of this library's kernels over `reps` calls of
+    run() (one decode step each), from a CUPTI trace taken by torch.profiler;
+    launches of a layer overlap through programmatic dependent launch, so the
+    per-layer sum may exceed the step time per layer."""
+    import re
+
+    import torch
+
+    try:
+        from torch.profiler import ProfilerActivity, profile
+    except Exception as e:  # noqa: BLE001 -- reported in the JSON line
+        return {"unavailable": str(e)[:120]}
+    torch.cuda.synchronize()
+    try:
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for _ in range(reps):
+                run()
+            torch.cuda.synchronize()
+        evs = prof.events()
+    except Exception as e:  # noqa: BLE001
+        return {"unavailable": str(e)[:120]}
+    acc = {}
+    for ev in evs:
+        m = re.search(r"(kvq_[a-z0-9_]+_kernel)", ev.name)
+        if m is None or "cuda" not in str(getattr(ev, "device_type", "")).lower():
+            continue
+        d = acc.setdefault(m.group(1), [0, 0.0])
+        d[0] += 1
+        d[1] += ev.time_range.elapsed_us()
+    if not acc:
+        return {"unavailable": "no kernel records in the trace"}
+    out = {k: {"launches": n, "avg_us": round(t / n, 3),
+               "per_layer_us": round(t / (reps * layers), 3)} for k, (n, t) in sorted(acc.items())}
+    return {"kernels": out, "steps_traced": reps,
+            "sum_per_layer_us": round(sum(t for _, t in acc.values()) / (reps * layers), 3),
+            "step_per_layer_us": round(1e3 * ms_step / layers, 3)}
+
+
 # ----------------------------------------------------------------- oracle leg
 def oracle_sample(w, fmt, group, seqs, oracle_mod, synth, kv_heads=None):
     """Set up the oracle's cache for `seqs` of layer 0 (untimed); returns a
@@ -559,6 +599,10 @@ def run_ours(args, rank, world, local_rank):
     for p in pools:
         assert p.error() == kvq.KVQ_OK
 
+    # -- per-kernel device times of a few steps (a CUPTI trace, outside the
+    # timed regions): explains the step time by its kernels
+    kernel_times = kernel_breakdown(timed_step, min(5, K), L, ms)
+
     b = step_bytes(w)
     step_total = b["decode"] + b["append"]
     value = job_gbs(step_total, world, ms)
@@ -578,8 +622,8 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "i8/e4m3 codes x f16 mma -> f32 acc",
         "data": "synthetic (seeded on-device normal draws with the workload's outlier/drift structure)",
-        "config": {
-            **workload_config(w),
+        "config": workload_config(w),
+        "run": {
             "l2": "inputs larger than L2: %d per-layer pools, %.1f GB"
                   % (L, sum(p.buffer.numel() for p in pools) / 1e9),
             "step": ("per layer: kvq_%sdecode_step (append 1 token/seq at L-1, then decode)"
@@ -588,6 +632,7 @@ def run_ours(args, rank, world, local_rank):
                      % ("cascade_decode" if P else "paged_decode")),
             "shared_prefix_blocks_read_once": P,
         },
+        "kernel_times": kernel_times,
         "pct_of_peak": round(100 * value / world / peak, 2),
         "decode_tok_per_s": round(world * w.S / (ms * 1e-3), 1),
         "bytes_per_step": b,
@@ -757,6 +802,53 @@ def run_prefill(args, rank, world, local_rank):
     }
 
 
+def launch_replicas(n, check_gpus=True):
+    """Start n ranks of this script, one per GPU (RANK, LOCAL_RANK, WORLD_SIZE,
+    MASTER_ADDR/PORT set as torchrun would); returns the worst exit code.
+    Rank 0 prints the job's JSON line."""
+    import socket
+
+    if check_gpus:
+        import torch
+
+        have = torch.cuda.device_count()
+        if have < n:
+            print("bench.py: --gpus %d but only %d GPU(s) visible" % (n, have), file=sys.stderr)
+            return 2
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + sys.argv[1:],
+                                      env=env))
+    rcs = [p.wait() for p in procs]
+    return max(rcs, key=abs)
+
+
+def launcher_selftest(rank, world):
+    """Every rank joins a gloo group and reports a step time of rank + 1 ms;
+    rank 0 prints the slowest and how many ranks took part."""
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.init_process_group("gloo")
+    d = dist if world > 1 else None
+    ms = max_over_ranks(1.0 + rank, d, torch.device("cpu"))
+    joined = torch.ones(1)
+    if d is not None:
+        d.all_reduce(joined)
+    if rank == 0:
+        print(json.dumps({"launcher_selftest": True, "n_gpus": world,
+                          "ranks_joined": int(joined.item()), "ms_per_step": ms,
+                          "job_gbs_for_1GB_per_rank": job_gbs(1e9, world, ms)}), flush=True)
+    if d is not None:
+        d.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -782,6 +874,9 @@ def main():
                     help="time the step as plain stream launches instead of a CUDA graph")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers (profiling runs only; the bench line uses all)")
+    ap.add_argument("--launcher-selftest", action="store_true",
+                    help="CPU check of the replica launcher: every rank joins a gloo group, "
+                         "rank 0 prints the max-over-ranks arithmetic; no GPU work")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.steps is None:
@@ -791,8 +886,18 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
+        # the oracle on the host cores: rank 0 alone runs and prints
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not started by torchrun: start the N replica ranks here
+        sys.exit(launch_replicas(args.gpus, check_gpus=not args.launcher_selftest))
+    if args.gpus != world:
+        sys.exit("bench.py: --gpus %d but WORLD_SIZE=%d; launch one rank per GPU"
+                 % (args.gpus, world))
+    if args.launcher_selftest:
+        launcher_selftest(rank, world)
         return
 
     if world > 1:

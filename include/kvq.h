@@ -24,11 +24,18 @@
  *     pool, a context longer than the caller promised, a pipeline wait that
  *     ran out -- set an error word inside the pool; the offending token or
  *     block is skipped and nothing faults.  kvq_get_error() reads and clears it.
+ *     While the error word reports OUT_OF_RANGE or TIMEOUT for a decode, the
+ *     contents of that decode's `out` are undefined (rows of a skipped block
+ *     or of a warp that gave up may be partial, zero or left as they were).
  *   - The library allocates device memory only in kvq_alloc_pool (and only when
  *     the caller passes no buffer).  Decode scratch ("workspace") comes from
  *     the caller.
  *   - Thread safety: calls on different pools may run concurrently; calls on
  *     one pool must be ordered by the caller (one stream, or events).
+ *   - One-time set-up the library remembers (kernel shared-memory opt-ins, the
+ *     address of kvq_paged_decode_noalloc's array) is kept per CUDA context,
+ *     keyed on the context current on the calling thread: after
+ *     cudaDeviceReset, or in another driver context, it is done again.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -246,8 +253,14 @@ kvq_status kvq_paged_decode_ex(const kvq_pool* pool, const kvq_half* q, int num_
  * the same stream.  A sequence with L == 0 stores nothing; L > max_context_len
  * stores nothing and sets OUT_OF_RANGE (the decode clamps as documented); a
  * negative block id at position L-1 sets OUT_OF_RANGE and stores nothing.
- * The decode is launched as a programmatic dependent of the append, so its
- * set-up overlaps the append; it reads the pool only after the append is done.
+ * The append starts once everything before it on the stream has completed,
+ * and the decode is launched as its programmatic dependent: the decode's
+ * set-up and its first page fetches overlap the append, and the one page per
+ * sequence that the append writes (the block holding position L-1) is read
+ * only after the append is done.  So the block receiving a sequence's new
+ * token must be read by no other sequence except as that sequence's own last
+ * block (a block shared further must be copied first, kvq_copy_blocks);
+ * otherwise the other sequence may see the block before or after the write.
  * The caller's k_new/v_new/q buffers must stay valid until the stream reaches
  * this call, as for every other call. */
 kvq_status kvq_decode_step(kvq_pool* pool, const kvq_half* k_new, const kvq_half* v_new,
@@ -326,9 +339,11 @@ kvq_status kvq_cascade_decode_step(kvq_pool* pool, const kvq_half* k_new, const 
  * results are those of kvq_paged_decode_ex; the caller still provides q,
  * the table, the lengths and `out`.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up that device's copy of the array
- *     (cudaGetSymbolAddress), so make that first call before any stream
- *     capture; later calls on the device reuse the address.
+ *   - The first call in a CUDA context looks up that device's copy of the
+ *     array (cudaGetSymbolAddress, with the context current), so make that
+ *     first call before any stream capture; later calls in the same context
+ *     reuse the address, and a new context (after cudaDeviceReset, say) gets a
+ *     fresh lookup on its first call.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose execution
  *     overlaps on the GPU -- on two streams, or from two threads -- race on

@@ -111,6 +111,8 @@ def _declare(L: ctypes.CDLL) -> None:
                                ctypes.c_float, ctypes.c_double)
     L.oracle_num_threads.restype = i32
     L.oracle_num_threads.argtypes = []
+    L.oracle_half_to_float.restype = None
+    L.oracle_half_to_float.argtypes = [P, P, i64]
     L.oracle_set_num_threads.restype = None
     L.oracle_set_num_threads.argtypes = [i32]
     L.oracle_kv_cache_bytes.restype = u64
@@ -144,9 +146,20 @@ def _ptr(a: np.ndarray | None):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def half_to_float(x) -> np.ndarray:
+    """float16 array widened exactly to float32 by the oracle's own routine."""
+    h = np.ascontiguousarray(np.asarray(x, dtype=np.float16))
+    out = np.empty(h.shape, np.float32)
+    lib().oracle_half_to_float(_ptr(h), _ptr(out), h.size)
+    return out
+
+
 def _f32(x) -> np.ndarray:
     """fp16 (or fp32) input widened exactly to a contiguous float32 array."""
-    return np.ascontiguousarray(np.asarray(x), dtype=np.float32)
+    x = np.asarray(x)
+    if x.dtype == np.float16:
+        return half_to_float(x)
+    return np.ascontiguousarray(x, dtype=np.float32)
 
 
 def num_threads() -> int:
@@ -271,6 +284,15 @@ class OracleCache:
         T = slots.size
         assert k.shape == (T, self.Hkv, self.D) and v.shape == k.shape
         assert int(slots.max(initial=-1)) < self.num_slots
+        # Tokens are appended in order, so a repeated slot ends up holding its
+        # last token: keep only that one (the C loop takes distinct slots).
+        live = np.nonzero(slots >= 0)[0]
+        _, last = np.unique(slots[live][::-1], return_index=True)
+        keep = np.sort(live[live.size - 1 - last])
+        if keep.size != T:
+            k, v, slots = (np.ascontiguousarray(k[keep]), np.ascontiguousarray(v[keep]),
+                           np.ascontiguousarray(slots[keep]))
+            T = slots.size
         lib().oracle_append(self.fmt, T, self.Hkv, self.D, self.g or 1, _ptr(k), _ptr(v),
                             _ptr(slots), _ptr(self.chan_scales), _ptr(self.codes),
                             _ptr(self.scales))

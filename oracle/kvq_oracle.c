@@ -170,6 +170,31 @@ uint8_t oracle_e5m2_encode(float x) {
     return (uint8_t)(best | (sign << 7));
 }
 
+/* IEEE binary16 -> binary32, exact: the widening every input goes through
+ * before the fp32 quantizer.  1 sign bit, 5 exponent bits (bias 15), 10
+ * mantissa bits; exponent 0 is zero or subnormal (m * 2^-24), exponent 31 is
+ * infinity (m = 0) or NaN (payload kept in the top mantissa bits), otherwise
+ * (1024 + m) * 2^(e - 25). */
+void oracle_half_to_float(const uint16_t* h, float* f, int64_t n) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < n; ++i) {
+        const uint32_t sign = (uint32_t)(h[i] >> 15);
+        const int e = (h[i] >> 10) & 0x1F;
+        const uint32_t m = h[i] & 0x3FFu;
+        float x;
+        if (e == 31) {
+            const uint32_t bits = (sign << 31) | 0x7F800000u | (m << 13);
+            memcpy(&x, &bits, sizeof x);
+        } else {
+            x = e == 0 ? ldexpf((float)m, -24) : ldexpf((float)(1024u + m), e - 25);
+            if (sign) x = -x;
+        }
+        f[i] = x;
+    }
+}
+
 /* One dynamic-scale INT8 group of n values. */
 void oracle_quant_int8_group(const float* x, int n, int8_t* codes, float* scale) {
     float a = 0.0f;
@@ -285,13 +310,18 @@ static int scales_per_slot(int fmt, int Hkv, int D, int g) {
 /* Append T new tokens ([KVC] §1.1: each decode step appends the new token's
  * K/V to the end of the cache).  k, v: [T][Hkv][D] (fp16 widened to fp32);
  * slots: [T], a negative slot means "skip this token"; chan_scales: [2][Hkv][D]
- * for the per-channel format.  Tokens are processed in order, so a later
- * token overwrites an earlier one at the same slot. */
+ * for the per-channel format.  The non-negative slots must be distinct: each
+ * token then writes only its own slot, and the tokens are taken in parallel.
+ * (OracleCache.append keeps only the last token of a repeated slot, which is
+ * what processing every token in order would leave there.) */
 void oracle_append(int fmt, int64_t T, int Hkv, int D, int g,
                    const float* k, const float* v, const int64_t* slots,
                    const float* chan_scales, void* codes, float* scales) {
     const int per = Hkv * D;
     const int nsc = scales_per_slot(fmt, Hkv, D, g);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t t = 0; t < T; ++t) {
         int64_t slot = slots[t];
         if (slot < 0) continue;

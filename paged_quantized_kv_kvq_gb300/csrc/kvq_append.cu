@@ -81,12 +81,14 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
   const PoolView& pool = p.pool;
   const int64_t t = blockIdx.x;
   const int kv = blockIdx.y;
-  // A decode that depends on this append may launch now: it only reads the
-  // pool after waiting for this grid to complete.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Launched as a programmatic dependent (decode step), wait for the previous
   // kernel's completion before reading anything; otherwise returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Only then may the dependent decode launch: everything before this append
+  // on the stream has completed by now, so the decode may read context
+  // lengths, the block table and every page this append does not write (all
+  // but each sequence's last page) before its own griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int64_t slot;
   if (p.slots != nullptr) {
     slot = p.slots[t];

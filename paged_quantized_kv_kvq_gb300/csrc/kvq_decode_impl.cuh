@@ -43,6 +43,7 @@
 #include <cuda_fp16.h>
 
 #include "kvq_common.cuh"
+#include "kvq_context.h"
 
 namespace kvq {
 
@@ -784,13 +785,23 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     if (++pst == nstage) pst = 0;
   };
   // Everything above reads only inputs (lengths, block table).  When the
-  // decode is a programmatic dependent of the decode-step append, wait here for
-  // the append to complete before the first page is fetched; otherwise this
-  // returns at once.
-  after_wait();
+  // decode is a programmatic dependent of the decode-step append (directly or
+  // through the prefix kernel), that append launched this grid only after
+  // everything before it on the stream had completed, and it writes one page
+  // per sequence: the one holding position L-1, the sequence's last page.  So
+  // the first stages are filled before griddepcontrol.wait up to the first
+  // last page, and the rest after it; without a dependency the wait returns
+  // at once.
   {
     const int npre = min(n_w, nstage);
-    for (int i = 0; i < npre; ++i) issue_next();
+    int k = 0;
+    for (; k < npre; ++k) {
+      const bool last = __shfl_sync(0xffffffffu, ic.pi + 1 == ic.Ps, 0);  // lane 0's cursor
+      if (last) break;
+      issue_next();
+    }
+    after_wait();
+    for (; k < npre; ++k) issue_next();
   }
 
   // Consumer position: page i sits in stage cst; cph is the parity of that
@@ -1013,9 +1024,16 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     }
   }
   if (failed) {
-    // A wait ran out: flag it, then wait (bounded again) for this warp's
-    // copies still in flight so that none lands after the CTA has exited.
+    // A wait ran out: flag it, mark this warp's partial rows empty (m = -inf,
+    // l = 0) so that the merge does not fold in an earlier call's leftovers,
+    // then wait (bounded again) for this warp's copies still in flight so that
+    // none lands after the CTA has exited.
     if (lane == 0) set_error(pool.err, ERR_TIMEOUT);
+    if (lane < 2 * kPartRows) {
+      float* r = p.part + ((int64_t)gw * 2 * kPartRows + lane) * (D + 2);
+      r[0] = kNegInf;
+      r[1] = 0.f;
+    }
     int st = cst;
     uint32_t ph = cph;
     for (int k = i; k < n_issued; ++k) {
@@ -1131,20 +1149,10 @@ struct DecodeLaunch {
   bool dependent;  // launch as a programmatic dependent of the previous kernel
 };
 
-constexpr int kMaxDevices = 64;
-
 template <int FMT, int D, int NG, bool BS8 = false>
 cudaError_t run_decode(const DecodeLaunch& l) {
-  static bool attr_set[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = allow_big_smem<kvq_decode_kernel<FMT, D, NG, BS8>>();
   if (e != cudaSuccess) return e;
-  if (dev < kMaxDevices && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kvq_decode_kernel<FMT, D, NG, BS8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   {
     cudaLaunchConfig_t dc = {};
     dc.gridDim = l.grid;

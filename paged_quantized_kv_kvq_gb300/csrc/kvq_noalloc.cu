@@ -1,36 +1,23 @@
 // kvq_noalloc.cu -- kvq_paged_decode_noalloc: paged decode whose split-K
 // scratch is a fixed device array owned by the library, for callers that
 // cannot allocate device memory (see include/kvq.h).
-#include <mutex>
-
 #include "kvq.h"
+#include "kvq_context.h"
 
 namespace {
 
 // The scratch: one copy per GPU that loads this library, kept until exit.
 static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDev = 64;
-std::mutex g_mu;
-void* g_addr[kMaxDev] = {};
+// Device address of the array in the current CUDA context, looked up on the
+// first call in that context (with it current) and remembered per context, so
+// that a device reset or another driver context gets a fresh lookup.  Host
+// code cannot use the symbol itself: on the host it names a stand-in, not
+// device memory.
+kvq::PerContext<void*> g_addr;
 
-// Device address of the current device's copy of the array, looked up once
-// per device (with that device current).  Host code cannot use the symbol
-// itself: on the host it names a stand-in, not device memory.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
-  return cudaSuccess;
+  return g_addr.get(out, [](void** p) { return cudaGetSymbolAddress(p, g_decode_scratch); });
 }
 
 }  // namespace

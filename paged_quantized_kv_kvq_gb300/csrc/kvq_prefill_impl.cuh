@@ -466,16 +466,8 @@ struct PrefillLaunch {
 
 template <int FMT, int D, int NG>
 cudaError_t run_prefill(const PrefillLaunch& l) {
-  static bool attr_set[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = allow_big_smem<kvq_prefill_kernel<FMT, D, NG>>();
   if (e != cudaSuccess) return e;
-  if (dev < kMaxDevices && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kvq_prefill_kernel<FMT, D, NG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   kvq_prefill_kernel<FMT, D, NG><<<l.grid, kPfThreads, l.smem, l.st>>>(l.p);
   return cudaGetLastError();
 }

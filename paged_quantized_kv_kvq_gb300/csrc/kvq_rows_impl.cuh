@@ -490,16 +490,8 @@ struct RowsLaunch {
 
 template <int FMT, int D, int NG>
 cudaError_t run_rows(const RowsLaunch& l) {
-  static bool attr_set[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = allow_big_smem<kvq_rows_kernel<FMT, D, NG>>();
   if (e != cudaSuccess) return e;
-  if (dev < kMaxDevices && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kvq_rows_kernel<FMT, D, NG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = l.grid;
   cfg.blockDim = dim3(kRowsThreads);

@@ -241,13 +241,25 @@ def kv_tokens(w: Workload, layer: int, seq_pos: np.ndarray) -> tuple[np.ndarray,
     v = np.empty((n, w.Hkv, w.D), np.float16)
     if n == 0:
         return k, v
-    for s in np.unique(seq_pos[:, 0]):
+
+    def one(s):  # sequences fill disjoint rows; numpy draws outside the GIL
         rows = np.nonzero(seq_pos[:, 0] == s)[0]
         pos = seq_pos[rows, 1]
         upto = int(pos.max()) + 1
         kk, vv = _seq_kv(w, layer, int(s), upto)
         k[rows] = kk[pos]
         v[rows] = vv[pos]
+
+    seqs = np.unique(seq_pos[:, 0])
+    if len(seqs) > 1 and n > 4096:
+        import concurrent.futures
+        import os
+
+        with concurrent.futures.ThreadPoolExecutor(min(len(seqs), os.cpu_count() or 1)) as ex:
+            list(ex.map(one, seqs))
+    else:
+        for s in seqs:
+            one(s)
     return k, v
 
 

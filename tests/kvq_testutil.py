@@ -66,7 +66,10 @@ def oracle_layer(w, fmt, group, k, v, slots, seqs, calib=None):
     c = oracle.OracleCache(fmt, max(nb, 1), w.bs, w.Hkv, w.D, group)
     if fmt == oracle.INT8_PER_CHANNEL:
         c.calibrate(*calib)
-    c.append(k[keep], v[keep], new_slots)
+    if keep.all():
+        c.append(k, v, new_slots)
+    else:
+        c.append(k[keep], v[keep], new_slots)
     return c, table, remap
 
 

@@ -38,7 +38,7 @@ def _fetched(w, fmt, group):
                                        (kvq.KVQ_INT8_PER_TOKEN, 0), (kvq.KVQ_INT8_PER_CHANNEL, 0),
                                        (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0), (kvq.KVQ_FP16, 0),
                                        (kvq.KVQ_INT4_PER_GROUP, 128), (kvq.KVQ_FP8_E5M2, 0)])
-@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
 def test_decode_bytes_equal_the_pages_fetched(fmt, group, bs):
     if bs == 8 and fmt == kvq.KVQ_INT4_PER_GROUP:
         pytest.skip("INT4 takes 16-token blocks or larger")

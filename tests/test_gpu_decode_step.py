@@ -148,3 +148,57 @@ def test_decode_step_edges():
                             torch.empty((3, 32, 128), dtype=torch.float32, device=DEV))
     assert e.value.status == kvq.KVQ_ERR_INVALID_ARG
     pool.close()
+
+
+@pytest.fixture(scope="module")
+def late_writer(tmp_path_factory):
+    """ctypes handle of tests/late_writer.cu, compiled for this GPU."""
+    import ctypes
+    import os
+    import shutil
+    import subprocess
+
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "late_writer.cu")
+    so = str(tmp_path_factory.mktemp("late_writer") / "late_writer.so")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
+                    "-Xcompiler", "-fPIC", "-o", so, src], check=True)
+    lib = ctypes.CDLL(so)
+    lib.late_write.restype = ctypes.c_int
+    lib.late_write.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                               ctypes.c_ulonglong, ctypes.c_void_p]
+    return lib
+
+
+def test_decode_step_after_late_length_writer(late_writer):
+    """The kernel just before the step lets its dependents launch early and
+    writes this step's context lengths ~0.2 ms later.  The step must use the
+    written lengths: its append waits for that kernel, and the decode launches
+    only once the append has passed that wait."""
+    w = synth.workload("gqa_64x2048", S=5, L=333, layers=1)
+    fmt, group = w.layer_formats[0]
+    k, v, slots = layer_tokens(w, 0)
+    S = w.S
+    pool = gpu_pool(w, fmt, group, DEV, k[:-S], v[:-S], slots[:-S])
+    ref, table, remap = oracle_layer(w, fmt, group, k, v, slots, list(range(S)))
+    q = synth.queries(w, 0)
+    lens = _t(np.ones(S, np.int32))            # stale lengths, overwritten late
+    truth = _t(w.context_lens)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        lens.fill_(1)
+        torch.cuda.synchronize()
+        assert late_writer.late_write(lens.data_ptr(), truth.data_ptr(), S, 200000,
+                                      stream.cuda_stream) == 0
+        out = pool.decode_step(_t(k[-S:]), _t(v[-S:]), _t(q), _t(w.block_table), lens,
+                               int(w.context_lens.max()))
+        torch.cuda.synchronize()
+        assert pool.error() == kvq.KVQ_OK
+        np.testing.assert_allclose(out.cpu().numpy(), ref.decode(q, table, w.context_lens),
+                                   rtol=0, atol=TOL)
+    codes, _ = pool.read_slots(_t(slots[-S:]))
+    rs = oracle_slots(remap, slots[-S:], w.bs)
+    np.testing.assert_array_equal(codes.cpu().numpy().view(np.uint8), ref.codes[rs].view(np.uint8))
+    pool.close()

@@ -61,13 +61,17 @@ def _sample_tokens(w, layer, seqs):
     return k, v, slots
 
 
-def _check(name, layer, seqs, fmt=None, group=None, cascade=False, **kw):
+def _check(name, layer, seqs, fmt=None, group=None, cascade=False, calib_rows=None, **kw):
+    """calib_rows: per-channel scales from the first calib_rows sampled tokens
+    only (the rest may saturate at +-127), instead of from all of them."""
     w = synth.workload(name, layers=layer + 1, **kw)
     if fmt is None:
         fmt, group = w.layer_formats[layer]
     n = len(seqs)
     k, v, slots = _sample_tokens(w, layer, seqs)
-    calib = (k, v) if fmt == kvq.KVQ_INT8_PER_CHANNEL else None
+    calib = None
+    if fmt == kvq.KVQ_INT8_PER_CHANNEL:
+        calib = (k, v) if calib_rows is None else (k[:calib_rows], v[:calib_rows])
     pool = _full_pool(w, layer, fmt, group, k[:-n], v[:-n], slots[:-n], calib)
     # this step's new tokens: device draws, the sampled sequences' from the host
     gen = torch.Generator(device=DEV)
@@ -108,7 +112,13 @@ def _check(name, layer, seqs, fmt=None, group=None, cascade=False, **kw):
     pool.close()
 
 
-@pytest.mark.parametrize("name", ["gqa_64x2048", "gqa_64x2048_int4", "gqa_64x2048_e5m2"])
+def test_gqa_64x2048_all_sequences_full():
+    # the headline step: every one of the 64 sequences against the oracle, so
+    # every unit the grid's warp ranges cut goes through the split merge
+    _check("gqa_64x2048", 0, list(range(64)))
+
+
+@pytest.mark.parametrize("name", ["gqa_64x2048_int4", "gqa_64x2048_e5m2"])
 def test_gqa_64x2048_full(name):
     # first, middle and last sequence: the last ends the persistent grid's range
     _check(name, 0, [0, 31, 63])
@@ -123,6 +133,12 @@ def test_gqa_64x2048_block8_full():
                                   "mha_100_int8g64"])
 def test_mha_100_full(name):
     _check(name, 0, [0, 57, 99])
+
+
+def test_mha_100_int8ch_saturated_full():
+    # per-channel scales from the first 64 sampled tokens only: the decode
+    # attends codes clipped at +-127 (the append saturates them) at full size
+    _check("mha_100_int8ch", 0, [0, 57, 99], calib_rows=64)
 
 
 @pytest.mark.parametrize("bs", [16, 32])

@@ -110,6 +110,28 @@ def test_decode_small_parity(fmt, group):
     pool.close()
 
 
+def test_per_channel_decode_attends_saturated_codes():
+    """Per-channel scales calibrated on the first 32 cached tokens only: tokens
+    beyond that range append as +-127, and the decode must attend those
+    clipped codes exactly as the oracle's store holds them."""
+    w = synth.workload("mha_100_int8ch", S=5, L=300, layers=1)
+    fmt, group = kvq.KVQ_INT8_PER_CHANNEL, 0
+    k, v, slots = layer_tokens(w, 0)
+    calib = (k[:32], v[:32])
+    pool = gpu_pool(w, fmt, group, DEV, k, v, slots, calib=calib)
+    ref, table, remap = oracle_layer(w, fmt, group, k, v, slots, list(range(w.S)), calib=calib)
+    last = {int(x): i for i, x in enumerate(slots)}
+    uniq = np.array(sorted(last), np.int64)
+    _compare_codes(pool, ref, uniq, oracle_slots(remap, uniq, w.bs))
+    codes = ref.codes[oracle_slots(remap, uniq, w.bs)].view(np.int8)
+    assert np.mean(np.abs(codes.astype(np.int32)) == 127) > 0.005   # many clipped codes
+    q = synth.queries(w, 0)
+    got = run_gpu_decode(pool, w, q, DEV)
+    np.testing.assert_allclose(got, ref.decode(q, table, w.context_lens), rtol=0, atol=TOL)
+    assert pool.error() == kvq.KVQ_OK
+    pool.close()
+
+
 def test_tiny_workload_full():
     w = synth.workload("tiny")
     fmt, g = w.layer_formats[0]

@@ -457,3 +457,18 @@ def test_copy_blocks_then_remap_gives_identical_decode():
     t2 = table.copy()
     t2[2, :3] = free
     np.testing.assert_array_equal(c.decode(q, t2, lens), before)
+
+
+def test_half_to_float_is_exact_on_every_code(oracle_mod):
+    """The oracle's binary16 widening against numpy's on all 65536 codes:
+    every finite value and infinity bit for bit, NaNs as NaN with the sign."""
+    h = np.arange(1 << 16, dtype=np.uint16).view(np.float16)
+    got = oracle_mod.half_to_float(h)
+    ref = h.astype(np.float32)
+    fin = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[fin].view(np.uint32), ref[fin].view(np.uint32))
+    assert np.isnan(got[~fin]).all()
+    np.testing.assert_array_equal(np.signbit(got[~fin]), np.signbit(ref[~fin]))
+    # the extremes by hand: the smallest subnormal, the largest finite value
+    assert oracle_mod.half_to_float(np.array([0x0001], np.uint16).view(np.float16))[0] == 2.0 ** -24
+    assert oracle_mod.half_to_float(np.array([0x7BFF], np.uint16).view(np.float16))[0] == 65504.0
