@@ -187,10 +187,12 @@ def gpu_index(local_rank):
 # ----------------------------------------------------------------- kernel breakdown
 def kernel_breakdown(run, reps, layers, ms_step):
     """Device time of each of this library's kernels over `reps` calls of
-    run() (one decode step each), from a CUPTI trace taken by torch.profiler;
-    launches of a layer overlap through programmatic dependent launch, so the
-    per-layer sum may exceed the step time per layer."""
+    run() (one decode step each), from a CUPTI trace taken by torch.profiler
+    (read back from its Chrome-trace export); launches of a layer overlap
+    through programmatic dependent launch, so the per-layer sum may exceed the
+    step time per layer."""
     import re
+    import tempfile
 
     import torch
 
@@ -200,23 +202,30 @@ def kernel_breakdown(run, reps, layers, ms_step):
         return {"unavailable": str(e)[:120]}
     torch.cuda.synchronize()
     try:
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
             for _ in range(reps):
                 run()
             torch.cuda.synchronize()
-        evs = prof.events()
+        with tempfile.TemporaryDirectory() as d:
+            path = os.path.join(d, "trace.json")
+            prof.export_chrome_trace(path)
+            trace = json.load(open(path))
     except Exception as e:  # noqa: BLE001
         return {"unavailable": str(e)[:120]}
+    evs = trace.get("traceEvents", trace) if isinstance(trace, dict) else trace
     acc = {}
     for ev in evs:
-        m = re.search(r"(kvq_[a-z0-9_]+_kernel)", ev.name)
-        if m is None or "cuda" not in str(getattr(ev, "device_type", "")).lower():
+        if not isinstance(ev, dict) or ev.get("cat") != "kernel":
+            continue
+        m = re.search(r"(kvq_[a-z0-9_]+_kernel)", str(ev.get("name", "")))
+        if m is None:
             continue
         d = acc.setdefault(m.group(1), [0, 0.0])
         d[0] += 1
-        d[1] += ev.time_range.elapsed_us()
+        d[1] += float(ev.get("dur", 0.0))
     if not acc:
-        return {"unavailable": "no kernel records in the trace"}
+        cats = sorted({str(e.get("cat")) for e in evs if isinstance(e, dict)})[:8]
+        return {"unavailable": "no kernel records in the trace (categories: %s)" % ", ".join(cats)}
     out = {k: {"launches": n, "avg_us": round(t / n, 3),
                "per_layer_us": round(t / (reps * layers), 3)} for k, (n, t) in sorted(acc.items())}
     return {"kernels": out, "steps_traced": reps,
@@ -793,7 +802,7 @@ def run_prefill(args, rank, world, local_rank):
         "prompt_tok_per_s": round(world * T / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "kvq_prefill call (mma.sync m16n8k16 f16 -> f32), %d calls timed "
+                     "kernel": "kvq_prefill call (tcgen05.mma kind::f16, fp32 accumulators in TMEM), %d calls timed "
                                "one by one after the step region" % (KR * L),
                      "flop_per_launch": flop_layer, "avg_launch_ms": round(att_ms, 4),
                      "peak_source": "%s bf16_tflops_sustained (f16 has the bf16 rate)" % peak_kind},

@@ -21,7 +21,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_decode_i8g.cu",
            "kvq_decode_misc.cu", "kvq_noalloc.cu", "kvq_rows.cu",
-           "kvq_decode_i4g.cu", "kvq_prefill.cu", "kvq_decode_bs8.cu", "kvq_decode_bs8_misc.cu"]
+           "kvq_decode_i4g.cu", "kvq_prefill.cu", "kvq_decode_bs8.cu", "kvq_decode_bs8_misc.cu", "kvq_prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

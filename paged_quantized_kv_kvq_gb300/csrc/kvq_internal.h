@@ -95,6 +95,15 @@ cudaError_t launch_prefill(const PoolView& pool, const __half* q, int S, int Hq,
                            int max_q_len, const int* table, int max_blocks, const int* lens,
                            int max_ctx, float sm_scale, float* out, cudaStream_t st);
 
+// The same on the 5th-generation tensor cores (kvq_prefill_tc_impl.cuh): for
+// formats with at most one scale per token and K|V (per-group only when the
+// group is the whole head), head_dim 64 or 128, blocks of 16 tokens or more.
+bool prefill_tc_supported(const PoolView& pool);
+cudaError_t launch_prefill_tc(const PoolView& pool, const __half* q, int S, int Hq,
+                              const int* q_start, int max_q_len, const int* table, int max_blocks,
+                              const int* lens, int max_ctx, float sm_scale, float* out,
+                              cudaStream_t st);
+
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;
 cudaError_t launch_decode_int8_group(const DecodeLaunch& l);

@@ -44,6 +44,11 @@ cudaError_t run_prefill_d(const PrefillLaunch& l) {
 cudaError_t launch_prefill(const PoolView& pool, const __half* q, int S, int Hq, const int* q_start,
                            int max_q_len, const int* table, int max_blocks, const int* lens,
                            int max_ctx, float sm_scale, float* out, cudaStream_t st) {
+  // tcgen05 kernel where the format allows; per-group formats with several
+  // scale groups per head take the mma.sync kernel below
+  if (prefill_tc_supported(pool))
+    return launch_prefill_tc(pool, q, S, Hq, q_start, max_q_len, table, max_blocks, lens, max_ctx,
+                             sm_scale, out, st);
   const bool tok = pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN;
   const int stage_bytes = round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
   int nstage = 4;

@@ -38,9 +38,13 @@ def _expand(table, lens, nq):
     return np.array(rows, np.int32), np.array(L, np.int32)
 
 
-def _case(fmt, group, name="gqa_64x2048", S=3, L=300, nq=(50, 17, 64), lens=None, seed=0, **kw):
+def _case(fmt, group, name="gqa_64x2048", S=3, L=300, nq=(50, 17, 64), lens=None, seed=0,
+          heads=None, **kw):
     w = synth.workload(name, S=S, L=L, layers=1, **kw)
     w.layer_formats = [(fmt, group)]
+    if heads is not None:
+        w.Hq, w.Hkv = heads
+        w.outlier_channels = w.outlier_channels[w.outlier_channels[:, 0] < w.Hkv]
     k, v, slots = layer_tokens(w, 0)
     calib = (k, v) if fmt == kvq.KVQ_INT8_PER_CHANNEL else None
     pool = gpu_pool(w, fmt, group, DEV, k, v, slots, calib=calib)
@@ -111,4 +115,31 @@ def test_prefill_edges():
     assert pool.error() == kvq.KVQ_ERR_OUT_OF_RANGE
     assert not got[:10].any()          # positions before the start of the context
     np.testing.assert_allclose(got[10:], exp[10:], rtol=0, atol=TOL)
+    pool.close()
+
+
+@pytest.mark.parametrize("fmt,group,kw,nq", [
+    (kvq.KVQ_INT8_PER_GROUP, 128, dict(S=2, L=700, bs=32), (700, 129)),
+    (kvq.KVQ_INT8_PER_TOKEN, 0, dict(S=2, L=700, bs=64), (333, 700)),
+    (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0, dict(S=2, L=515, bs=32), (64, 515)),
+    (kvq.KVQ_INT4_PER_GROUP, 128, dict(S=2, L=640, bs=64), (640, 65)),
+])
+def test_prefill_block_sizes(fmt, group, kw, nq):
+    """Blocks of 32 and 64 tokens: a 64-token key step spans two pages or one;
+    ragged ends of the context and of the chunk."""
+    pool, got, exp, _ = _case(fmt, group, nq=nq, **kw)
+    assert pool.error() == kvq.KVQ_OK
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    pool.close()
+
+
+@pytest.mark.parametrize("heads,nq", [((32, 32), (300, 1, 129)), ((32, 4), (100, 37, 16)),
+                                      ((32, 1), (40, 3, 1)), ((24, 2), (77, 50, 9))])
+def test_prefill_head_groups(heads, nq):
+    """MHA (one Q head per kv head: 128 query tokens per tile), GQA 8:1, MQA
+    (32 heads: 4 query tokens per tile) and GQA 12:1 (tiles that split a
+    token's heads), with the per-token format whose scale spans all heads."""
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_TOKEN, 0, S=3, L=300, nq=nq, heads=heads)
+    assert pool.error() == kvq.KVQ_OK
+    np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     pool.close()
