@@ -46,9 +46,11 @@ cudaError_t launch_prefill(const PoolView& pool, const __half* q, int S, int Hq,
                            int max_ctx, float sm_scale, float* out, cudaStream_t st) {
   // tcgen05 kernel where the format allows; per-group formats with several
   // scale groups per head take the mma.sync kernel below
-  if (prefill_tc_supported(pool))
-    return launch_prefill_tc(pool, q, S, Hq, q_start, max_q_len, table, max_blocks, lens, max_ctx,
-                             sm_scale, out, st);
+  if (prefill_tc_supported(pool)) {
+    const cudaError_t e = launch_prefill_tc(pool, q, S, Hq, q_start, max_q_len, table, max_blocks,
+                                            lens, max_ctx, sm_scale, out, st);
+    if (e != cudaErrorInvalidValue) return e;  // else: no room for its tiles, use the kernel below
+  }
   const bool tok = pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN;
   const int stage_bytes = round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
   int nstage = 4;

@@ -34,6 +34,36 @@ cudaError_t launch_prefill_tc(const PoolView& pool, const __half* q, int S, int 
   if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   PrefillTcLaunch l;
   PrefillTcParams& p = l.p;
+  // shared-memory plan: Q (hi, and lo for per-channel), the K tile, the V^T
+  // tile, the weight tiles (the low part reuses the K tile when it is as
+  // large), the raw page stage of one key step, the misc block
+  const bool ch = pool.fmt == FMT_INT8_CHANNEL;
+  const bool tok = pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN;
+  const int D = pool.D;
+  const int qb = kTcThreads * D * 2, kb = kTcStep * D * 2, vb = D * kTcStep * 2,
+            pb = kTcThreads * kTcStep * 2;
+  p.off_qlo = qb;
+  p.off_kh = ch ? 2 * qb : qb;
+  p.off_vt = p.off_kh + kb;
+  p.off_phi = p.off_vt + vb;
+  int next = p.off_phi + pb;
+  if (kb >= pb) {
+    p.off_plo = p.off_kh;
+  } else {
+    p.off_plo = next;
+    next += pb;
+  }
+  p.npg = kTcStep / pool.bs;
+  p.tok_bytes = tok ? 2 * pool.bs * 4 : 0;
+  p.pstride = (pool.page_bytes + p.tok_bytes + 127) / 128 * 128;
+  p.off_raw = next;
+  next += p.npg * p.pstride;
+  p.off_misc = (next + 127) / 128 * 128;
+  // 1024 bytes of alignment slack; at least 80 KB so that no more than two
+  // CTAs (2 x 256 TMEM columns) share an SM
+  l.smem = p.off_misc + kMiscBytes + 1024;
+  if (l.smem < 80 * 1024) l.smem = 80 * 1024;
+  if (l.smem > 227 * 1024) return cudaErrorInvalidValue;
   p.pool = pool;
   p.q = q;
   p.table = table;
