@@ -8,30 +8,33 @@
 // position L - n + i.  K/V are read from the block-paged cache (§2.2) in their
 // stored format (§2.3, §3.3) and dequantized inside the kernel (§4.3).
 //
-// GB300 design.  A CTA takes one (sequence, kv head) and 128 Q rows -- the
-// (query token, Q head of the group) pairs, 32 query tokens x 4 heads for GQA
-// 4:1 -- and walks the keys in steps of 64 tokens:
-//   1. the step's pages, brought into a shared-memory stage by bulk copies
-//      issued one step ahead, are turned by the 128 threads into exact fp16
-//      values: K as a 64 x D tile, V transposed as a D x 64 tile, both K-major
-//      with the 128-byte swizzle; the step's per-token scales go to shared
-//      memory;
-//   2. one thread issues S = Q.K^T (M 128, N 64, K = D) into tensor memory;
-//   3. each thread owns one row: it reads its 64 scores from TMEM, applies
-//      the K scales, the causal limit and the online softmax (base 2), and
-//      writes the weights p * s_V * 2^E as an fp16 high part and an fp16 low
-//      part (one K-major 128 x 64 tile each; the low part reuses the K tile,
-//      which S no longer needs); its exponent reference moves only when a
-//      score passes it by more than 2^8, and only then (or when E drops) is
-//      its row of the output accumulator in TMEM rescaled;
-//   4. one thread issues O += P_hi.V + P_lo.V (M 128, N D, K 64) into TMEM.
-// Codes are exact in fp16, so dequantization is a scale outside the
-// contraction, as in the decode kernel; the hi + lo split keeps the weights
-// exact to ~2^-22.  The output row is normalised once at the end.  Two CTAs
-// share an SM (at most ~113 KB of shared memory and 256 TMEM columns each),
-// so one CTA's tensor work overlaps the other's conversion and softmax.  Every
-// wait on the MMA barrier is bounded; a wait that runs out sets the pool's
-// timeout bit, waits (bounded) for the MMAs in flight and frees TMEM.
+// GB300 design.  A CTA of 12 warps takes one (sequence, kv head) and two
+// tiles of 128 Q rows -- the (query token, Q head of the group) pairs, 32
+// query tokens x 4 heads per tile for GQA 4:1 -- and walks the keys in steps
+// of 64 tokens, with the work split by role:
+//   * 4 converter warps load the next step's code pages into registers while
+//     the current step is being used, then turn them into exact fp16 values
+//     in shared memory -- K as a 64 x D tile, V transposed as a D x 64 tile,
+//     both K-major with the 128-byte swizzle, two buffers -- and publish the
+//     step's per-token scales and valid-token mask;
+//   * each tile's 4 softmax warps own its 128 rows (one row per thread, one
+//     TMEM lane each): they read the row's 64 scores S = Q.K^T from tensor
+//     memory, apply the K scales, the causal limit and the online softmax
+//     (base 2), and write the weights p * s_V * 2^E as an fp16 high part and
+//     an fp16 low part (K-major 128 x 64 tiles); the row's exponent reference
+//     moves only when a score passes it by more than 2^8, and only then (or
+//     when E drops) is its row of the output accumulator in TMEM rescaled;
+//   * one thread of each tile issues that tile's tensor-core work: O +=
+//     P_hi.V + P_lo.V (M 128, N D, K 64), then, once the next step is
+//     converted, S = Q.K^T (M 128, N 64, K D), both tcgen05.mma kind::f16
+//     with fp32 accumulators in TMEM.
+// While one tile runs its softmax the tensor cores run the other tile's
+// products, and the conversion of a step is shared by both tiles.  Codes are
+// exact in fp16, so dequantization is a scale outside the contraction, as in
+// the decode kernel; the hi + lo split keeps the weights exact to ~2^-22.
+// Every wait is bounded and gives up early once another role has given up;
+// the CTA then flags a timeout in the pool's error word, waits (bounded) for
+// its MMAs in flight and frees TMEM.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -41,11 +44,10 @@
 
 namespace kvq {
 
-constexpr int kTcThreads = 128;   // = Q rows per CTA = TMEM lanes
+constexpr int kTcRows = 128;      // Q rows per tile = TMEM lanes
 constexpr int kTcStep = 64;       // key tokens per step
-constexpr int kTcCols = 256;      // TMEM columns: O at [0, D), S at [128, 192)
-constexpr int kTcSCol = 128;
 constexpr int kTcSlack = 8;       // log2 of how far a row may exceed its reference maximum
+constexpr int kTcConv = 128;      // converter threads
 
 struct PrefillTcParams {
   PoolView pool;
@@ -56,19 +58,32 @@ struct PrefillTcParams {
   float* out;           // [Tq][Hq][D]
   int S, Hq, G, max_blocks, max_ctx;
   int ntiles;           // 128-row tiles per (sequence, kv head)
+  int ngroups;          // CTAs per (sequence, kv head): ceil(ntiles / NT)
   float sm_scale_log2;
-  // shared-memory plan (byte offsets from a 1024-byte aligned base)
-  int off_qlo, off_kh, off_vt, off_phi, off_plo, off_raw, off_misc;
-  int npg;              // pages per key step (64 / block size)
-  int pstride;          // bytes of one page slot of the raw stage
-  int tok_bytes;        // per-token scale bytes copied after each page (0 otherwise)
 };
 
-// The misc block: float ks[64], vs[64], vmax[2]; uint32 tmask[2]; float
-// red[4]; int stage_ok[4]; uint64 bar_mma, bar_raw; uint32 tslot.
-constexpr int kMiscKs = 0, kMiscVs = 256, kMiscVmax = 512, kMiscMask = 520, kMiscRed = 528,
-              kMiscOk = 544, kMiscBarMma = 560, kMiscBarRaw = 568, kMiscSlot = 576,
-              kMiscBytes = 640;
+// Shared-memory plan of a CTA with NT tiles (byte offsets from a 1024-byte
+// aligned base): Q tiles (and their low parts for per-channel pools), the two
+// K and V^T buffers, each tile's weight tiles, the misc block.
+template <int D, int NT, bool CH>
+struct TcPlan {
+  static constexpr int QB = kTcRows * D * 2, KB = kTcStep * D * 2, VB = D * kTcStep * 2,
+                       PB = kTcRows * kTcStep * 2;
+  static constexpr int q = 0;                              // [NT][QB] (+ [NT][QB] low parts)
+  static constexpr int kh = NT * QB * (CH ? 2 : 1);        // [2][KB]
+  static constexpr int vt = kh + 2 * KB;                   // [2][VB]
+  static constexpr int pw = vt + 2 * VB;                   // [NT][hi, lo][PB]
+  static constexpr int misc = pw + NT * 2 * PB;
+  // misc: float ks[2][64], vs[2][64]; float vmax[2][2]; uint32 mask[2][2];
+  // int abort; uint64 kv_full[2], kv_empty[2], s_full[NT], o_full[NT], drain[NT]; uint32 tslot
+  static constexpr int ks = misc, vs = misc + 512, vmax = misc + 1024, mask = misc + 1040,
+                       abort = misc + 1056, bars = misc + 1064, tslot = bars + 8 * (4 + 3 * NT);
+  static constexpr int bytes = tslot + 16;
+  static constexpr int request = bytes + 1024;             // alignment slack
+  static constexpr int threads = kTcRows * NT + kTcConv;
+  static constexpr int cols = NT == 2 ? 512 : 256;          // TMEM: O at 128X, S at 256 + 64X (NT 2)
+  static constexpr int s_col(int x) { return NT == 2 ? 256 + 64 * x : 128; }
+};
 
 template <int FMT>
 __device__ __forceinline__ void tc_word_to_h2(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -138,11 +153,27 @@ __device__ __forceinline__ void tc_convert_chunk(uint4 raw, int L, int c, bool i
   }
 }
 
-// Bounded wait on an mbarrier by every thread; CTA-uniform result.
-__device__ __forceinline__ bool tc_wait_bar(uint64_t* bar, uint32_t parity) {
-  bool ok = false;
-  for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(bar, parity);
-  return !__syncthreads_or(!ok);
+// Bounded wait that gives up early once another role has set *abort; a wait
+// that runs out sets it.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (int tries = 0; tries < kWaitTries; ++tries) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+// Named barrier over `count` threads with an OR of `pred`.
+__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Split two fp32 weights into fp16 high and low pairs: (a, b) ~= hi + lo.
@@ -156,10 +187,22 @@ __device__ __forceinline__ void tc_split2(float a, float b, uint32_t& hi, uint32
   lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int FMT, int D>
-__global__ void __launch_bounds__(kTcThreads, 2) kvq_prefill_tc_kernel(const PrefillTcParams p) {
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+template <int FMT, int D, int NT>
+__global__ void __launch_bounds__(TcPlan<D, NT, FmtTraits<FMT>::channel>::threads, 1)
+    kvq_prefill_tc_kernel(const PrefillTcParams p) {
   using T = FmtTraits<FMT>;
   constexpr bool CH = T::channel;
+  using PL = TcPlan<D, NT, CH>;
+  constexpr int ES = FMT == FMT_FP16 ? 2 : 1;
+  constexpr int SUB_BYTES = FMT == FMT_INT4_GROUP ? 8 * D : 16 * D * ES;
+  constexpr int CPS = SUB_BYTES / 16;                 // 16-byte chunks per K (or V) sub-tile
+  constexpr int NCH = (CPS + kTcConv - 1) / kTcConv;  // chunks per converter thread and sub-tile
   const float kNegInf = __int_as_float(0xff800000u);
 
   extern __shared__ __align__(1024) char smem_raw[];
@@ -168,436 +211,458 @@ __global__ void __launch_bounds__(kTcThreads, 2) kvq_prefill_tc_kernel(const Pre
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PoolView& pool = p.pool;
   const int bs = pool.bs;
-  // heaviest tiles (longest causal ranges) first
-  const int per_tile = p.S * pool.Hkv;
-  const int tile = p.ntiles - 1 - static_cast<int>(blockIdx.x / per_tile);
-  const int seq = static_cast<int>(blockIdx.x % per_tile) % p.S;
-  const int h = static_cast<int>(blockIdx.x % per_tile) / p.S;
+  // heaviest tile groups (longest causal ranges) first
+  const int per = p.S * pool.Hkv;
+  const int grp = p.ngroups - 1 - static_cast<int>(blockIdx.x / per);
+  const int seq = static_cast<int>(blockIdx.x % per) % p.S;
+  const int h = static_cast<int>(blockIdx.x % per) / p.S;
 
   const int qbase = p.q_start[seq];
   const int nq = p.q_start[seq + 1] - qbase;
   int ctx = p.lens[seq];
   if (ctx > p.max_ctx || ctx < nq) {
-    if (tile == 0 && h == 0 && tid == 0) set_error(pool.err, ERR_RANGE);
+    if (grp == 0 && h == 0 && tid == 0) set_error(pool.err, ERR_RANGE);
     ctx = min(ctx, p.max_ctx);
   }
   const int rows_total = nq * p.G;
-  if (tile * kTcThreads >= rows_total) return;  // CTA-uniform
-
-  // ---- this thread's row and the CTA's key range
-  const int rr = tile * kTcThreads + tid;
-  const bool row_ok = rr < rows_total;
-  const int lim = row_ok ? max(0, ctx - nq + rr / p.G + 1) : 0;
-  int64_t orow = -1;
-  if (row_ok) orow = (int64_t)(qbase + rr / p.G) * p.Hq + h * p.G + rr % p.G;
-  const int last = min(rows_total, (tile + 1) * kTcThreads) - 1;
+  const int row0 = grp * NT * kTcRows;  // first row of the CTA
+  if (row0 >= rows_total) return;       // CTA-uniform
+  const int last = min(rows_total, row0 + NT * kTcRows) - 1;
   const int kv_end = max(0, min(ctx, ctx - nq + last / p.G + 1));
   const int nsteps = (kv_end + kTcStep - 1) / kTcStep;
+
+  // softmax threads: tile X, row r (= TMEM lane)
+  const bool is_sm = tid < NT * kTcRows;
+  const int X = is_sm ? warp >> 2 : 0;
+  const int r = (warp & 3) * 32 + lane;
+  const int rr = row0 + X * kTcRows + r;
+  const bool row_ok = is_sm && rr < rows_total;
+  const int lim = row_ok ? max(0, ctx - nq + rr / p.G + 1) : 0;
+  const int64_t orow = row_ok ? (int64_t)(qbase + rr / p.G) * p.Hq + h * p.G + rr % p.G : -1;
   if (nsteps == 0) {  // nothing to attend: zeros (CTA-uniform)
     if (row_ok)
       for (int d = 0; d < D; ++d) p.out[orow * D + d] = 0.f;
     return;
   }
 
-  char* q_hi = sm;
-  char* q_lo = sm + p.off_qlo;
-  char* kh = sm + p.off_kh;
-  char* vt = sm + p.off_vt;
-  char* p_hi = sm + p.off_phi;
-  char* p_lo = sm + p.off_plo;  // may be the K tile: free once S is computed
-  char* raw = sm + p.off_raw;
-  char* misc = sm + p.off_misc;
-  float* ks_s = reinterpret_cast<float*>(misc + kMiscKs);
-  float* vs_s = reinterpret_cast<float*>(misc + kMiscVs);
-  float* vmax_s = reinterpret_cast<float*>(misc + kMiscVmax);
-  uint32_t* tmask_s = reinterpret_cast<uint32_t*>(misc + kMiscMask);
-  float* red = reinterpret_cast<float*>(misc + kMiscRed);
-  int* stage_ok = reinterpret_cast<int*>(misc + kMiscOk);
-  uint64_t* bar_mma = reinterpret_cast<uint64_t*>(misc + kMiscBarMma);
-  uint64_t* bar_raw = reinterpret_cast<uint64_t*>(misc + kMiscBarRaw);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + kMiscSlot);
-  const int* trow = p.table + (int64_t)seq * p.max_blocks;
+  float* ks_s = reinterpret_cast<float*>(sm + PL::ks);      // [2][64]
+  float* vs_s = reinterpret_cast<float*>(sm + PL::vs);      // [2][64]
+  float* vmax_s = reinterpret_cast<float*>(sm + PL::vmax);  // [2][2]
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(sm + PL::mask);  // [2][2]
+  volatile int* abort_f = reinterpret_cast<volatile int*>(sm + PL::abort);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL::bars);
+  uint64_t* kv_full = bars;           // [2]: converted K/V of a step (128 arrivals)
+  uint64_t* kv_empty = bars + 2;      // [2]: every tile's MMAs of that step done (NT commits)
+  uint64_t* s_full = bars + 4;        // [NT]: S of the tile's current step
+  uint64_t* o_full = bars + 4 + NT;   // [NT]: the tile's last P.V done
+  uint64_t* drain = bars + 4 + 2 * NT;  // [NT]: clean-up
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PL::tslot);
 
-  // Thread 0: bulk-copy the pages of key step j into the raw stage, one
-  // transaction count on bar_raw (a plain arrival when no page is present).
-  auto issue_step = [&](int j) {
-    uint32_t total = 0;
-    int phys[4];
-    for (int pg = 0; pg < p.npg; ++pg) {
-      const int tb = j * kTcStep + pg * bs;
-      const int n = tb / bs;
-      phys[pg] = (tb < kv_end && n < p.max_blocks) ? trow[n] : -1;
-      const bool ok = phys[pg] >= 0 && (int64_t)phys[pg] < pool.num_blocks;
-      if (tb < kv_end && !ok) set_error(pool.err, ERR_RANGE);
-      if (!ok) phys[pg] = -1;
-      stage_ok[pg] = ok ? 1 : 0;
-      if (ok) total += pool.page_bytes + p.tok_bytes;
-    }
-    if (total == 0) {
-      mbar_arrive(bar_raw);
-      return;
-    }
-    mbar_arrive_expect_tx(bar_raw, total);
-    for (int pg = 0; pg < p.npg; ++pg) {
-      if (phys[pg] < 0) continue;
-      char* dst = raw + pg * p.pstride;
-      bulk_g2s(dst, pool.pages + ((int64_t)phys[pg] * pool.Hkv + h) * pool.page_bytes,
-               pool.page_bytes, bar_raw);
-      if (p.tok_bytes)
-        bulk_g2s(dst + pool.page_bytes, pool.tok_scales + (int64_t)phys[pg] * 2 * bs, p.tok_bytes,
-                 bar_raw);
-    }
-  };
-
-  // ---- barriers, the first step's pages, TMEM (warp 0 allocates)
   if (tid == 0) {
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_raw, 1);
+    mbar_init(&kv_full[0], kTcConv);
+    mbar_init(&kv_full[1], kTcConv);
+    mbar_init(&kv_empty[0], NT);
+    mbar_init(&kv_empty[1], NT);
+    for (int x = 0; x < NT; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&o_full[x], 1);
+      mbar_init(&drain[x], 1);
+    }
+    *abort_f = 0;
     fence_barrier_init();
-    issue_step(0);
   }
-  if (warp == 0) tc_alloc(tslot, kTcCols);
+  if (warp == 0) tc_alloc(tslot, PL::cols);
 
-  // ---- Q tile (rows of this CTA, zero past the chunk), K-major swizzled
+  // ---- softmax threads: their own Q row into the tile (K-major, swizzled)
   float csc = p.sm_scale_log2;
-  auto q_row_ptr = [&](int r) -> const __half* {
-    const int x = tile * kTcThreads + r;
-    if (x >= rows_total) return nullptr;
-    return p.q + ((int64_t)(qbase + x / p.G) * p.Hq + h * p.G + x % p.G) * D;
-  };
-  if constexpr (!CH) {
-    for (int it = tid; it < kTcThreads * (D / 8); it += kTcThreads) {
-      const int r = it / (D / 8), c = it % (D / 8);
-      const __half* src = q_row_ptr(r);
-      const uint4 v = src ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(q_hi + sw128_offset(r, 8 * c, kTcThreads)) = v;
-    }
-  } else {
-    // fold the K channel scale into q, scale the tile by 2^eq so that its
-    // largest magnitude lies in [2^13, 2^14), split into fp16 hi + lo
-    const float* ksc = pool.chan_scales + (int64_t)h * D;
-    float amax = 0.f;
-    for (int it = tid; it < kTcThreads * (D / 8); it += kTcThreads) {
-      const int r = it / (D / 8), c = it % (D / 8);
-      const __half* src = q_row_ptr(r);
-      if (src == nullptr) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * c);
-      const __half* hv = reinterpret_cast<const __half*>(&v);
+  if (is_sm) {
+    const __half* src = row_ok ? p.q + orow * D : nullptr;
+    char* qx = sm + PL::q + X * PL::QB;
+    if constexpr (!CH) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(__half2float(hv[e]) * ksc[8 * c + e]));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) red[warp] = amax;
-    __syncthreads();
-    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
-    const float up = ldexpf(1.f, eq);
-    csc = ldexpf(csc, -eq);
-    for (int it = tid; it < kTcThreads * (D / 8); it += kTcThreads) {
-      const int r = it / (D / 8), c = it % (D / 8);
-      const __half* src = q_row_ptr(r);
-      uint4 hv4 = make_uint4(0, 0, 0, 0), lv4 = make_uint4(0, 0, 0, 0);
-      if (src != nullptr) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * c);
-        const __half* hv = reinterpret_cast<const __half*>(&v);
-        uint32_t* ho = reinterpret_cast<uint32_t*>(&hv4);
-        uint32_t* lo = reinterpret_cast<uint32_t*>(&lv4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          split_h2(__half2float(hv[2 * e]) * ksc[8 * c + 2 * e] * up,
-                   __half2float(hv[2 * e + 1]) * ksc[8 * c + 2 * e + 1] * up, ho[e], lo[e]);
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = src ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = v;
       }
-      *reinterpret_cast<uint4*>(q_hi + sw128_offset(r, 8 * c, kTcThreads)) = hv4;
-      *reinterpret_cast<uint4*>(q_lo + sw128_offset(r, 8 * c, kTcThreads)) = lv4;
+    } else {
+      // fold the K channel scale into the row, scale it by 2^eq so that its
+      // largest magnitude lies in [2^13, 2^14), split into fp16 hi + lo
+      const float* ksc = pool.chan_scales + (int64_t)h * D;
+      char* ql = sm + PL::q + (NT + X) * PL::QB;
+      float amax = 0.f;
+      if (src)
+        for (int d = 0; d < D; ++d) amax = fmaxf(amax, fabsf(__half2float(src[d]) * ksc[d]));
+      const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
+      const float up = ldexpf(1.f, eq);
+      csc = ldexpf(csc, -eq);
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 hv4 = make_uint4(0, 0, 0, 0), lv4 = make_uint4(0, 0, 0, 0);
+        if (src) {
+          uint32_t* ho = reinterpret_cast<uint32_t*>(&hv4);
+          uint32_t* lo = reinterpret_cast<uint32_t*>(&lv4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = 8 * c + 2 * e;
+            split_h2(__half2float(src[d]) * ksc[d] * up, __half2float(src[d + 1]) * ksc[d + 1] * up,
+                     ho[e], lo[e]);
+          }
+        }
+        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = hv4;
+        *reinterpret_cast<uint4*>(ql + sw128_offset(r, 8 * c, kTcRows)) = lv4;
+      }
     }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tO = tmem, tS = tmem + kTcSCol;
-  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+  const int* trow = p.table + (int64_t)seq * p.max_blocks;
 
-  const uint32_t qhi_a = smem_u32(q_hi), qlo_a = smem_u32(q_lo), kh_a = smem_u32(kh),
-                 vt_a = smem_u32(vt), phi_a = smem_u32(p_hi), plo_a = smem_u32(p_lo);
-  constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
-  constexpr uint32_t id_o = tc_idesc_f16(128, D);
-
-  float m = kNegInf, l = 0.f;
-  int E = T::row_scales ? 100 : 14 - kTcSlack;
-  uint32_t ph_mma = 0, ph_raw = 0;
-  bool failed = false;
-
-  for (int jstep = 0; jstep < nsteps; ++jstep) {
-    const int t0 = jstep * kTcStep;
-    // ---- 1. this step's pages have landed: codes -> fp16 tiles, scales
-    if (!tc_wait_bar(bar_raw, ph_raw)) {
-      failed = true;
-      break;
-    }
-    ph_raw ^= 1u;
-    if (tid < kTcStep) {
-      const int t = t0 + tid;
-      const int pg = tid / bs, off = tid - pg * bs;
-      const bool ok = stage_ok[pg] != 0 && t < kv_end;
-      const char* page = raw + pg * p.pstride;
-      float k_s = 1.f, v_s = 1.f;
-      if constexpr (T::group_scales) {
-        const float* sc = reinterpret_cast<const float*>(page + 2 * pool.code_bytes);
-        k_s = ok ? sc[off] : 0.f;
-        v_s = ok ? sc[bs + off] : 0.f;
-      } else if constexpr (T::token_scales) {
-        const float* sc = reinterpret_cast<const float*>(page + pool.page_bytes);
-        k_s = ok ? sc[off] : 0.f;
-        v_s = ok ? sc[bs + off] : 0.f;
-      } else {
-        v_s = ok ? 1.f : 0.f;
-      }
-      ks_s[tid] = k_s * csc;
-      vs_s[tid] = v_s;
-      const uint32_t bits = __ballot_sync(0xffffffffu, ok);
-      float vm = v_s;
+  if (!is_sm) {
+    // ======================= converters =======================
+    const int cid = tid - NT * kTcRows;
+    const int npg = kTcStep / bs;
+    // raw codes of one step: [sub-tile][K|V][chunk] for this thread's chunks
+    uint4 rv[4][2][NCH];
+    float sk = 0.f, sv = 0.f;  // this thread's token scales (cid < 64)
+    bool tok_ok = false;       // and whether that token is present
+    int tphys[4];              // block ids of the step being loaded
+    auto load_table = [&](int j, int (&ph)[4]) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-      if (lane == 0) {
-        tmask_s[warp] = bits;
-        vmax_s[warp] = vm;
+      for (int pg = 0; pg < 4; ++pg) {
+        const int tb = j * kTcStep + pg * bs;
+        const int n = tb / bs;
+        ph[pg] = (pg < npg && tb < kv_end && n < p.max_blocks) ? trow[n] : -1;
       }
-    }
-    {
-      constexpr int ES = FMT == FMT_FP16 ? 2 : 1;
-      constexpr int SUB_BYTES = FMT == FMT_INT4_GROUP ? 8 * D : 16 * D * ES;
-      constexpr int CPS = SUB_BYTES / 16;  // 16-byte chunks per K (or V) sub-tile
-      for (int it = tid; it < 8 * CPS; it += kTcThreads) {
-        const int s = it / (2 * CPS), rem = it - s * (2 * CPS);
-        const bool isv = rem >= CPS;
-        const int ch = isv ? rem - CPS : rem;
+    };
+    auto page_of = [&](int phys) -> const char* {
+      return pool.pages + ((int64_t)phys * pool.Hkv + h) * pool.page_bytes;
+    };
+    auto phys_ok = [&](int phys) { return phys >= 0 && (int64_t)phys < pool.num_blocks; };
+    auto load_step = [&](int j, const int (&ph)[4]) {
+      const int t0 = j * kTcStep;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
         const int pg = (16 * s) / bs, sub = ((16 * s) % bs) >> 4;
+        const bool ok = phys_ok(ph[pg]) && t0 + 16 * s < kv_end;
+        const char* base = ok ? page_of(ph[pg]) + sub * SUB_BYTES : nullptr;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            const int ch = cid + i * kTcConv;
+            rv[s][kv][i] = (ok && ch < CPS)
+                               ? *reinterpret_cast<const uint4*>(base + (kv ? pool.code_bytes : 0) +
+                                                                 (ch >> 5) * 512 + (ch & 31) * 16)
+                               : make_uint4(0, 0, 0, 0);
+          }
+      }
+      if (cid < kTcStep) {
+        const int pg = cid / bs, off = cid - (cid / bs) * bs;
+        const bool ok = phys_ok(ph[pg]) && t0 + cid < kv_end;
+        tok_ok = ok;
+        sk = 0.f;
+        sv = ok ? 1.f : 0.f;
+        if constexpr (T::group_scales) {
+          if (ok) {
+            const float* sc = reinterpret_cast<const float*>(page_of(ph[pg]) + 2 * pool.code_bytes);
+            sk = sc[off];
+            sv = sc[bs + off];
+          }
+        } else if constexpr (T::token_scales) {
+          if (ok) {
+            sk = pool.tok_scales[((int64_t)ph[pg] * 2) * bs + off];
+            sv = pool.tok_scales[((int64_t)ph[pg] * 2 + 1) * bs + off];
+          }
+        }
+      }
+    };
+    load_table(0, tphys);
+    load_step(0, tphys);
+    load_table(1, tphys);
+    for (int j = 0; j < nsteps; ++j) {
+      const int b = j & 1;
+      if (j >= 2 && !tc_wait(&kv_empty[b], ((j >> 1) - 1) & 1, abort_f)) break;
+      const int t0 = j * kTcStep;
+      char* khb = sm + PL::kh + b * PL::KB;
+      char* vtb = sm + PL::vt + b * PL::VB;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
         const int nvalid = min(max(kv_end - (t0 + 16 * s), 0), 16);
-        const bool ok = stage_ok[pg] != 0 && nvalid > 0;
-        uint4 rv = make_uint4(0, 0, 0, 0);
-        if (ok)
-          rv = *reinterpret_cast<const uint4*>(raw + pg * p.pstride + (isv ? pool.code_bytes : 0) +
-                                               sub * SUB_BYTES + (ch >> 5) * 512 + (ch & 31) * 16);
-        tc_convert_chunk<FMT, D>(rv, ch & 31, ch >> 5, isv, s, ok ? nvalid : 0, kh, vt);
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            const int ch = cid + i * kTcConv;
+            if (ch < CPS) tc_convert_chunk<FMT, D>(rv[s][kv][i], ch & 31, ch >> 5, kv == 1, s,
+                                                   nvalid, khb, vtb);
+          }
+      }
+      if (cid < kTcStep) {
+        // token t0 + cid: its K and V scale (0 for a token that is absent or
+        // past the end), and its bit of the step's valid-token mask
+        ks_s[b * 64 + cid] = sk;
+        vs_s[b * 64 + cid] = sv;
+        const uint32_t bits = __ballot_sync(0xffffffffu, tok_ok);
+        float vm = sv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+        if (lane == 0) {
+          mask_s[b * 2 + (cid >> 5)] = bits;
+          vmax_s[b * 2 + (cid >> 5)] = vm;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&kv_full[b]);
+      if (j + 1 < nsteps) {
+        int nx[4];
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) nx[pg] = tphys[pg];
+        load_step(j + 1, nx);
+        load_table(j + 2, tphys);
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- 2. the raw stage is free: fetch the next step; S = Q K^T
-    if (tid == 0) {
-      tc_fence_after();
+  } else {
+    // ======================= softmax + MMA issue, tile X =======================
+    const uint32_t tO = tmem + X * 128, tS = tmem + PL::s_col(X);
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t qa = smem_u32(sm + PL::q + X * PL::QB);
+    const uint32_t qla = smem_u32(sm + PL::q + (NT + X) * PL::QB);
+    const uint32_t pha = smem_u32(sm + PL::pw + X * 2 * PL::PB);
+    const uint32_t pla = pha + PL::PB;
+    char* p_hi = sm + PL::pw + X * 2 * PL::PB;
+    char* p_lo = p_hi + PL::PB;
+    constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
+    constexpr uint32_t id_o = tc_idesc_f16(128, D);
+    const bool issuer = r == 0;  // thread 0 of the tile
+    const int bar_id = 1 + X;
+    auto issue_s = [&](int j) {  // S = Q K^T of step j (issuer)
+      const uint32_t kha = smem_u32(sm + PL::kh + (j & 1) * PL::KB);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = (kk >> 2) * (kTcStep * 128) + (kk & 3) * 32;
-        const uint32_t qo = (kk >> 2) * (kTcThreads * 128) + (kk & 3) * 32;
-        tc_mma_f16(tS, sw128_desc(qhi_a + qo), sw128_desc(kh_a + ko), id_s, kk > 0);
-        if constexpr (CH) tc_mma_f16(tS, sw128_desc(qlo_a + qo), sw128_desc(kh_a + ko), id_s, 1);
+        const uint32_t qo = (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
+        tc_mma_f16(tS, sw128_desc(qa + qo), sw128_desc(kha + ko), id_s, kk > 0);
+        if constexpr (CH) tc_mma_f16(tS, sw128_desc(qla + qo), sw128_desc(kha + ko), id_s, 1);
       }
-      tc_commit(bar_mma);
-      if (jstep + 1 < nsteps) issue_step(jstep + 1);
-    }
-    if (!tc_wait_bar(bar_mma, ph_mma)) {
-      failed = true;
-      break;
-    }
-    ph_mma ^= 1u;
-    tc_fence_after();
-
-    // ---- 3. online softmax of this thread's row (base 2); the weights carry
-    // the V scale and 2^E, which is folded into the exponent
-    float z[kTcStep];
-    {
-      float a[32];
-      tc_ld32(tS + lane_base, a);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = a[i];
-      tc_ld32(tS + lane_base + 32, a);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
-    }
-    const uint32_t mk0 = tmask_s[0], mk1 = tmask_s[1];
-    const int lr = lim - t0;  // tokens [0, lr) of this step are attended by this row
-    float mx = kNegInf;
-    if (lr >= kTcStep && (mk0 & mk1) == 0xffffffffu) {
-#pragma unroll
-      for (int t = 0; t < kTcStep; t += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(ks_s + t);
-        float a0, a1, a2, a3;
-        f2_unpack(f2_mul(f2_pack(z[t], z[t + 1]), f2_pack(k4.x, k4.y)), a0, a1);
-        f2_unpack(f2_mul(f2_pack(z[t + 2], z[t + 3]), f2_pack(k4.z, k4.w)), a2, a3);
-        z[t] = a0;
-        z[t + 1] = a1;
-        z[t + 2] = a2;
-        z[t + 3] = a3;
-        mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < kTcStep; ++t) {
-        const bool ok = t < lr && (((t < 32 ? mk0 : mk1) >> (t & 31)) & 1u);
-        z[t] = ok ? z[t] * ks_s[t] : kNegInf;
-        mx = fmaxf(mx, z[t]);
+      tc_commit(&s_full[X]);
+    };
+    bool failed = false;
+    if (issuer) {
+      if (tc_wait(&kv_full[0], 0, abort_f)) {
+        tc_fence_after();
+        issue_s(0);
       }
     }
-    // The row's reference maximum m moves only when the step's maximum passes
-    // it by more than kTcSlack (weights then stay below 2^kTcSlack, and the
-    // 2^E prescale leaves that much headroom below the fp16 range), so the
-    // accumulator in TMEM is rescaled only on such a jump or when E drops.
-    const float mn = (m == kNegInf || mx > m + kTcSlack) ? mx : m;
-    const float ms = mn == kNegInf ? 0.f : mn;
-    int dE = 0;
-    if constexpr (T::row_scales) {
-      const float vmax = fmaxf(vmax_s[0], vmax_s[1]);
-      if (vmax > 0.f) {
-        const int En = min(E, 13 - kTcSlack - exponent_of(vmax));
-        dE = En - E;
-        E = En;
+    float m = kNegInf, l = 0.f;
+    int E = T::row_scales ? 100 : 14 - kTcSlack;
+    for (int j = 0; j < nsteps; ++j) {
+      const int b = j & 1;
+      bool ok = tc_wait(&s_full[X], j & 1, abort_f);
+      // the step's scales and mask were published with kv_full (already
+      // complete: S of this step was computed from them)
+      ok = ok && tc_wait(&kv_full[b], (j >> 1) & 1, abort_f);
+      if (bar_or(bar_id, kTcRows, !ok)) {
+        failed = true;
+        break;
       }
-    }
-    // p' = 2^(z - ms + E): the weights before the V scale
-    const float bias = ms - static_cast<float>(E);
-    uint64_t rs2 = f2_pack(0.f, 0.f);
-    {
-      const uint64_t b2 = f2_pack(bias, bias);
+      tc_fence_after();
+      const int t0 = j * kTcStep;
+      float z[kTcStep];
+      {
+        float a[32];
+        tc_ld32(tS + lane_base, a);
 #pragma unroll
-      for (int t = 0; t < kTcStep; t += 2) {
-        float a0, a1;
-        f2_unpack(f2_sub(f2_pack(z[t], z[t + 1]), b2), a0, a1);
-        z[t] = fast_exp2(a0);  // 0 for masked tokens
-        z[t + 1] = fast_exp2(a1);
-        rs2 = f2_add(rs2, f2_pack(z[t], z[t + 1]));
+        for (int i = 0; i < 32; ++i) z[i] = a[i];
+        tc_ld32(tS + lane_base + 32, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
       }
+      const float* ksb = ks_s + b * 64;
+      const float* vsb = vs_s + b * 64;
+      const uint32_t mk0 = mask_s[b * 2], mk1 = mask_s[b * 2 + 1];
+      const int lr = lim - t0;  // tokens [0, lr) of this step are attended by this row
+      float mx = kNegInf;
+      if (lr >= kTcStep && (mk0 & mk1) == 0xffffffffu) {
+#pragma unroll
+        for (int t = 0; t < kTcStep; t += 4) {
+          float a0 = z[t], a1 = z[t + 1], a2 = z[t + 2], a3 = z[t + 3];
+          if constexpr (T::row_scales) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ksb + t);
+            f2_unpack(f2_mul(f2_pack(a0, a1), f2_pack(k4.x, k4.y)), a0, a1);
+            f2_unpack(f2_mul(f2_pack(a2, a3), f2_pack(k4.z, k4.w)), a2, a3);
+          }
+          z[t] = a0;
+          z[t + 1] = a1;
+          z[t + 2] = a2;
+          z[t + 3] = a3;
+          mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < kTcStep; ++t) {
+          const bool okt = t < lr && (((t < 32 ? mk0 : mk1) >> (t & 31)) & 1u);
+          z[t] = okt ? (T::row_scales ? z[t] * ksb[t] : z[t]) : kNegInf;
+          mx = fmaxf(mx, z[t]);
+        }
+      }
+      // scores in log2 units are z * csc (csc > 0).  The reference maximum m
+      // moves only when the step's maximum passes it by more than kTcSlack,
+      // so the TMEM accumulator is rescaled only then (or when E drops).
+      const float mxz = mx == kNegInf ? kNegInf : mx * csc;
+      const float mn = (m == kNegInf || mxz > m + kTcSlack) ? mxz : m;
+      const float ms = mn == kNegInf ? 0.f : mn;
+      int dE = 0;
+      if constexpr (T::row_scales) {
+        const float vmax = fmaxf(vmax_s[b * 2], vmax_s[b * 2 + 1]);
+        if (vmax > 0.f) {
+          const int En = min(E, 13 - kTcSlack - exponent_of(vmax));
+          dE = En - E;
+          E = En;
+        }
+      }
+      // p' = 2^(z csc - ms + E), the weight before the V scale
+      const float nbias = static_cast<float>(E) - ms;
+      uint64_t rs2 = f2_pack(0.f, 0.f);
+      {
+        const uint64_t c2 = f2_pack(csc, csc), b2 = f2_pack(nbias, nbias);
+#pragma unroll
+        for (int t = 0; t < kTcStep; t += 2) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(z[t], z[t + 1]), c2, b2), a0, a1);
+          z[t] = fast_exp2(a0);  // 0 for masked tokens
+          z[t + 1] = fast_exp2(a1);
+          rs2 = f2_add(rs2, f2_pack(z[t], z[t + 1]));
+        }
+      }
+      float rsa, rsb;
+      f2_unpack(rs2, rsa, rsb);
+      const float alpha = fast_exp2(m - ms);
+      l = fmaf(l, alpha, (rsa + rsb) * pow2f(-E));
+      m = mn;
+      if (j > 0) {
+        // O holds steps 0..j-1: the P.V of step j-1 completed before S of
+        // step j (one issuing thread, in order)
+        const float f = alpha * pow2f(dE);
+        if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc_ld32(tO + lane_base + 32 * c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tc_st32(tO + lane_base + 32 * c, o);
+          }
+          tc_wait_st();
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kTcStep / 8; ++c) {
+        uint32_t hv[4], lv[4];
+        float vv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if constexpr (T::row_scales) {
+          const float4 v0 = *reinterpret_cast<const float4*>(vsb + 8 * c);
+          const float4 v1 = *reinterpret_cast<const float4*>(vsb + 8 * c + 4);
+          vv[0] = v0.x, vv[1] = v0.y, vv[2] = v0.z, vv[3] = v0.w;
+          vv[4] = v1.x, vv[5] = v1.y, vv[6] = v1.z, vv[7] = v1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float w0 = z[8 * c + 2 * e], w1 = z[8 * c + 2 * e + 1];
+          // masked tokens (absent, past the end, or causally later) have p' = 0;
+          // their V scale is 0 too
+          if constexpr (T::row_scales)
+            f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(vv[2 * e], vv[2 * e + 1])), w0, w1);
+          tc_split2(w0, w1, hv[e], lv[e]);
+        }
+        const uint32_t o = sw128_offset(r, 8 * c, kTcRows);
+        *reinterpret_cast<uint4*>(p_hi + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(p_lo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      bar_or(bar_id, kTcRows, false);  // the tile's weights are written, S is read
+      if (issuer) {
+        tc_fence_after();
+        const uint32_t vta = smem_u32(sm + PL::vt + b * PL::VB);
+#pragma unroll
+        for (int kk = 0; kk < kTcStep / 16; ++kk)
+          tc_mma_f16(tO, sw128_desc(pha + kk * 32), sw128_desc(vta + kk * 32), id_o,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTcStep / 16; ++kk)
+          tc_mma_f16(tO, sw128_desc(pla + kk * 32), sw128_desc(vta + kk * 32), id_o, 1u);
+        tc_commit(&kv_empty[b]);
+        if (j + 1 < nsteps) {
+          if (tc_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_f)) {
+            tc_fence_after();
+            issue_s(j + 1);
+          }
+        } else {
+          tc_commit(&o_full[X]);
+        }
+      }
+      __syncwarp();
     }
-    float rsa, rsb;
-    f2_unpack(rs2, rsa, rsb);
-    const float alpha = fast_exp2(m - ms);
-    l = fmaf(l, alpha, (rsa + rsb) * pow2f(-E));
-    m = mn;
-    if (jstep > 0) {
-      const float f = alpha * pow2f(dE);
-      if (__any_sync(0xffffffffu, f != 1.f)) {
+    if (!failed) {
+      // ---- normalised output rows once the tile's last P.V is done
+      bool ok = tc_wait(&o_full[X], 0, abort_f);
+      if (bar_or(bar_id, kTcRows, !ok)) {
+        failed = true;
+      } else {
+        tc_fence_after();
+        const float f = l > 0.f ? pow2f(-E) / l : 0.f;
+        const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           tc_ld32(tO + lane_base + 32 * c, o);
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(p.out + orow * D + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tc_st32(tO + lane_base + 32 * c, o);
-        }
-        tc_wait_st();
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < kTcStep / 8; ++c) {
-      uint32_t hv[4], lv[4];
-      if constexpr (T::row_scales) {
-        const float4 v0 = *reinterpret_cast<const float4*>(vs_s + 8 * c);
-        const float4 v1 = *reinterpret_cast<const float4*>(vs_s + 8 * c + 4);
-        const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float w0, w1;
-          f2_unpack(f2_mul(f2_pack(z[8 * c + 2 * e], z[8 * c + 2 * e + 1]),
-                           f2_pack(vv[2 * e], vv[2 * e + 1])), w0, w1);
-          tc_split2(w0, w1, hv[e], lv[e]);
-        }
-      } else {
-        // no V scale: masked tokens already have p' = 0; a token of an absent
-        // page has vs = 0
-        const float4 v0 = *reinterpret_cast<const float4*>(vs_s + 8 * c);
-        const float4 v1 = *reinterpret_cast<const float4*>(vs_s + 8 * c + 4);
-        const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          tc_split2(vv[2 * e] != 0.f ? z[8 * c + 2 * e] : 0.f,
-                    vv[2 * e + 1] != 0.f ? z[8 * c + 2 * e + 1] : 0.f, hv[e], lv[e]);
-      }
-      const uint32_t o = sw128_offset(tid, 8 * c, kTcThreads);
-      *reinterpret_cast<uint4*>(p_hi + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-      *reinterpret_cast<uint4*>(p_lo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- 4. O += P_hi V + P_lo V
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTcStep / 16; ++kk)
-        tc_mma_f16(tO, sw128_desc(phi_a + kk * 32), sw128_desc(vt_a + kk * 32), id_o,
-                   (jstep > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < kTcStep / 16; ++kk)
-        tc_mma_f16(tO, sw128_desc(plo_a + kk * 32), sw128_desc(vt_a + kk * 32), id_o, 1u);
-      tc_commit(bar_mma);
-    }
-    if (!tc_wait_bar(bar_mma, ph_mma)) {
-      failed = true;
-      break;
-    }
-    ph_mma ^= 1u;
-    tc_fence_after();
-  }
-
-  if (failed) {
-    // a wait ran out: flag it, wait (bounded) for the MMAs and copies in
-    // flight, free TMEM
-    if (tid == 0) set_error(pool.err, ERR_TIMEOUT);
-    tc_wait_bar(bar_mma, ph_mma);
-    tc_wait_bar(bar_raw, ph_raw);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, kTcCols);
-    return;
-  }
-
-  // ---- normalised output row
-  {
-    const float f = l > 0.f ? pow2f(-E) / l : 0.f;
-    const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      float o[32];
-      tc_ld32(tO + lane_base + 32 * c, o);
-      if (row_ok) {
-        float4* dst = reinterpret_cast<float4*>(p.out + orow * D + 32 * c);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float4 v = make_float4(o[4 * i] * f, o[4 * i + 1] * f, o[4 * i + 2] * f, o[4 * i + 3] * f);
-          if constexpr (CH) {
-            const float* cs = vch + 32 * c + 4 * i;
-            v.x *= cs[0];
-            v.y *= cs[1];
-            v.z *= cs[2];
-            v.w *= cs[3];
+            for (int i = 0; i < 8; ++i) {
+              float4 v = make_float4(o[4 * i] * f, o[4 * i + 1] * f, o[4 * i + 2] * f,
+                                     o[4 * i + 3] * f);
+              if constexpr (CH) {
+                const float* cs = vch + 32 * c + 4 * i;
+                v.x *= cs[0];
+                v.y *= cs[1];
+                v.z *= cs[2];
+                v.w *= cs[3];
+              }
+              dst[i] = v;
+            }
           }
-          dst[i] = v;
         }
       }
+    }
+    if (issuer) {
+      // every MMA this thread issued has completed before TMEM is freed
+      tc_commit(&drain[X]);
+      bool ok = false;
+      for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(&drain[X], 0);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc_dealloc(tmem, kTcCols);
+  if (tid == 0 && *abort_f) set_error(pool.err, ERR_TIMEOUT);
+  if (warp == 0) tc_dealloc(tmem, PL::cols);
 }
 
 struct PrefillTcLaunch {
   PrefillTcParams p;
   dim3 grid;
-  int smem;
   cudaStream_t st;
 };
 
-template <int FMT, int D>
+template <int FMT, int D, int NT>
 cudaError_t run_prefill_tc(const PrefillTcLaunch& l) {
-  cudaError_t e = allow_big_smem<kvq_prefill_tc_kernel<FMT, D>>();
+  using PL = TcPlan<D, NT, FmtTraits<FMT>::channel>;
+  static_assert(PL::request <= 227 * 1024, "shared memory plan too large");
+  cudaError_t e = allow_big_smem<kvq_prefill_tc_kernel<FMT, D, NT>>();
   if (e != cudaSuccess) return e;
-  kvq_prefill_tc_kernel<FMT, D><<<l.grid, kTcThreads, l.smem, l.st>>>(l.p);
+  kvq_prefill_tc_kernel<FMT, D, NT><<<l.grid, PL::threads, PL::request, l.st>>>(l.p);
   return cudaGetLastError();
 }
 
