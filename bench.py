@@ -739,11 +739,23 @@ def run_prefill(args, rank, world, local_rank):
     out = torch.empty((T, w.Hq, w.D), dtype=torch.float32, device=dev)
     mq = int(lens.max())
     sm_scale = w.D ** -0.5
+    # --prefill-api ex: two passes (the key steps staged once as fp16 tiles
+    # in a workspace, then attention); plain: kvq_prefill, one pass
+    ex = args.prefill_api == "ex"
+    ws_n = max(kvq.kvq_prefill_workspace_bytes(p.handle, w.S, mq) for p in pools) if ex else 0
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev) if ws_n else None
+
+    def attend(l):
+        if ex:
+            kvq.kvq_prefill_ex(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, out, ws,
+                               stream)
+        else:
+            kvq.kvq_prefill(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, out, stream)
 
     def step():
         for l in range(L):
             kvq.kvq_append(pools[l].handle, kin[l], vin[l], slots, stream)
-            kvq.kvq_prefill(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, out, stream)
+            attend(l)
 
     for _ in range(args.warmup):
         step()
@@ -775,7 +787,7 @@ def run_prefill(args, rank, world, local_rank):
     for i in range(KR):
         for l in range(L):
             evs[i * L + l][0].record(stream)
-            kvq.kvq_prefill(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, out, stream)
+            attend(l)
             evs[i * L + l][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -798,15 +810,19 @@ def run_prefill(args, rank, world, local_rank):
                    "head_dim": w.D, "block_size": w.bs,
                    "kv_format": sorted({"%s%s" % (FORMAT_NAME[f], (" %d" % g) if f in GROUPED else "")
                                         for f, g in w.layer_formats}),
-                   "step": "per layer: kvq_append (every prompt token) then kvq_prefill"},
+                   "step": "per layer: kvq_append (every prompt token) then kvq_prefill%s"
+                           % ("_ex" if ex else "")},
         "prompt_tok_per_s": round(world * T / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "kvq_prefill call (tcgen05.mma kind::f16, fp32 accumulators in TMEM), %d calls timed "
+                     "kernel": ("kvq_prefill_ex call (staging of the key steps as fp16 tiles, then "
+                                "tcgen05.mma kind::f16 attention" if ex else
+                                "kvq_prefill call (tcgen05.mma kind::f16 attention, codes converted "
+                                "in the kernel") + ", fp32 accumulators in TMEM), %d calls timed "
                                "one by one after the step region" % (KR * L),
                      "flop_per_launch": flop_layer, "avg_launch_ms": round(att_ms, 4),
                      "peak_source": "%s bf16_tflops_sustained (f16 has the bf16 rate)" % peak_kind},
-        "gpu_launches": K * L * 2,
+        "gpu_launches": K * L * (3 if ex else 2),  # append, (staging,) attention
         "clocks": clocks,
     }
 
@@ -877,6 +893,9 @@ def main():
                     help="decode: the decode step (default); prefill: prompt prefill")
     ap.add_argument("--prefill-seqs", type=int, default=8,
                     help="prompts in the prefill batch (--op prefill)")
+    ap.add_argument("--prefill-api", default="plain", choices=["plain", "ex"],
+                    help="--op prefill: kvq_prefill (one pass) or kvq_prefill_ex (key steps "
+                         "staged once in a workspace, then attention)")
     ap.add_argument("--block-size", type=int, default=None,
                     help="tokens per block (default: the workload's; 8, 16, 32 or 64)")
     ap.add_argument("--no-graph", action="store_true",

@@ -315,6 +315,27 @@ kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, in
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                        float sm_scale, float* out, cudaStream_t stream);
 
+/* kvq_prefill in two passes through a caller workspace (same arguments and
+ * results, [KVC] §1.1).  Every 64-token key step of a sequence's cache is
+ * read by all the thread blocks whose query rows come after it; here a first
+ * pass turns each step's codes into exact fp16 once, with its per-token scales
+ * beside them, and the attention pass reads those instead of converting the
+ * codes again in every block.  The arithmetic is the same as kvq_prefill's
+ * (codes exact in fp16, scales applied outside the contraction).
+ *   workspace : >= kvq_prefill_workspace_bytes(pool, num_seqs, max_context_len)
+ *               bytes, 256-byte aligned, owned by the caller; its contents are
+ *               scratch (written and read by this call only)
+ * kvq_prefill_workspace_bytes returns 0 for the formats this path does not take
+ * (per-group formats with more than one group per head, 8-token blocks); for
+ * them kvq_prefill_ex ignores the workspace and runs kvq_prefill.  Returns
+ * KVQ_ERR_WORKSPACE when the workspace is missing or too small. */
+size_t kvq_prefill_workspace_bytes(const kvq_pool* pool, int num_seqs, int max_context_len);
+kvq_status kvq_prefill_ex(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
+                          const int32_t* q_start, int max_q_len, const int32_t* block_table,
+                          int max_blocks_per_seq, const int32_t* context_lens,
+                          int max_context_len, float sm_scale, float* out, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream);
+
 /* kvq_decode_step with the cascade decode: the new token of sequence s goes to
  * position context_lens[s]-1, which must lie past the shared prefix (a token
  * written into a shared block would change every sequence's prefix). */

@@ -101,6 +101,8 @@ def _declare(L):
         "kvq_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, f32, P, P, sz, P]),
         "kvq_cascade_workspace_bytes": (sz, [P, i32, i32, i32]),
         "kvq_prefill": (i32, [P, P, i32, i32, P, i32, P, i32, P, i32, f32, P, P]),
+        "kvq_prefill_workspace_bytes": (sz, [P, i32, i32]),
+        "kvq_prefill_ex": (i32, [P, P, i32, i32, P, i32, P, i32, P, i32, f32, P, P, sz, P]),
         "kvq_selftest_decode_timeout": (i32, [P, P, i32, i32, P, i32, P, i32, P, P, sz, i32, P]),
         "kvq_cascade_decode": (i32, [P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz, P]),
         "kvq_cascade_decode_step": (i32, [P, P, P, P, i32, i32, P, i32, P, i32, i32, f32, P, P, sz,
@@ -337,6 +339,28 @@ def kvq_prefill(pool, q, q_start, max_q_len, block_table, context_lens, max_cont
         int(max_q_len), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
         _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len), float(sm_scale),
         _ptr(out, torch.float32, "out"), _stream(stream)), "kvq_prefill")
+
+
+def kvq_prefill_workspace_bytes(pool, num_seqs, max_context_len) -> int:
+    return int(lib().kvq_prefill_workspace_bytes(pool, int(num_seqs), int(max_context_len)))
+
+
+def kvq_prefill_ex(pool, q, q_start, max_q_len, block_table, context_lens, max_context_len,
+                   sm_scale, out, workspace, stream=None) -> None:
+    """kvq_prefill in two passes through a caller workspace (kvq_prefill_ex in
+    include/kvq.h); workspace: uint8 device tensor of at least
+    kvq_prefill_workspace_bytes(...) bytes, or None when that is 0."""
+    import torch
+
+    Tq, Hq, _ = q.shape
+    S = q_start.numel() - 1
+    ws = None if workspace is None else _ptr(workspace, torch.uint8, "workspace")
+    nbytes = 0 if workspace is None else workspace.numel()
+    _check(lib().kvq_prefill_ex(
+        pool, _ptr(q, torch.float16, "q"), S, Hq, _ptr(q_start, torch.int32, "q_start"),
+        int(max_q_len), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(context_lens, torch.int32, "context_lens"), int(max_context_len), float(sm_scale),
+        _ptr(out, torch.float32, "out"), ws, nbytes, _stream(stream)), "kvq_prefill_ex")
 
 
 def kvq_selftest_decode_timeout(pool, q, block_table, context_lens, max_context_len, out,

@@ -491,6 +491,41 @@ kvq_status kvq_prefill(const kvq_pool* pool, const kvq_half* q, int num_seqs, in
   return e == cudaErrorInvalidValue ? KVQ_ERR_UNSUPPORTED : from_cuda(e);
 }
 
+size_t kvq_prefill_workspace_bytes(const kvq_pool* pool, int num_seqs, int max_context_len) {
+  if (pool == nullptr || num_seqs < 1 || max_context_len < 1) return 0;
+  return kvq::prefill_ws_bytes(pool->view, num_seqs, max_context_len);
+}
+
+kvq_status kvq_prefill_ex(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
+                          const int32_t* q_start, int max_q_len, const int32_t* block_table,
+                          int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                          float sm_scale, float* out, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream) {
+  if (pool == nullptr) return KVQ_ERR_INVALID_ARG;
+  const size_t need = kvq_prefill_workspace_bytes(pool, num_seqs, max_context_len);
+  if (need == 0)  // a format or geometry the two-pass path does not take
+    return kvq_prefill(pool, q, num_seqs, num_q_heads, q_start, max_q_len, block_table,
+                       max_blocks_per_seq, context_lens, max_context_len, sm_scale, out, stream);
+  if (num_seqs < 0 || num_q_heads < 1 || max_q_len < 0 || max_blocks_per_seq < 1 ||
+      max_context_len < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_q_len == 0) return KVQ_OK;
+  if (q == nullptr || q_start == nullptr || block_table == nullptr || context_lens == nullptr ||
+      out == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % pool->view.Hkv != 0) return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * pool->view.bs) return KVQ_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) & 15) return KVQ_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return KVQ_ERR_INVALID_ARG;
+  const cudaError_t e = kvq::launch_prefill_ws(
+      pool->view, reinterpret_cast<const __half*>(q), num_seqs, num_q_heads, q_start, max_q_len,
+      block_table, max_blocks_per_seq, context_lens, max_context_len, sm_scale, out, workspace,
+      stream);
+  return e == cudaErrorInvalidValue ? KVQ_ERR_UNSUPPORTED : from_cuda(e);
+}
+
 kvq_status kvq_paged_decode(const kvq_pool* pool, const kvq_half* q, int num_seqs, int num_q_heads,
                             const int32_t* block_table, int max_blocks_per_seq,
                             const int32_t* context_lens, int max_context_len, float sm_scale,

@@ -104,6 +104,15 @@ cudaError_t launch_prefill_tc(const PoolView& pool, const __half* q, int S, int 
                               const int* lens, int max_ctx, float sm_scale, float* out,
                               cudaStream_t st);
 
+// Prefill in two passes through a workspace (kvq_prefill_ws_impl.cuh): the
+// codes of every 64-token key step staged once as fp16 tiles, then the
+// attention pass.  Same formats as launch_prefill_tc; 0 bytes otherwise.
+size_t prefill_ws_bytes(const PoolView& pool, int S, int max_ctx);
+cudaError_t launch_prefill_ws(const PoolView& pool, const __half* q, int S, int Hq,
+                              const int* q_start, int max_q_len, const int* table, int max_blocks,
+                              const int* lens, int max_ctx, float sm_scale, float* out, void* ws,
+                              cudaStream_t st);
+
 // Per-format kernel launchers (one translation unit each, compiled in parallel).
 struct DecodeLaunch;
 cudaError_t launch_decode_int8_group(const DecodeLaunch& l);

@@ -164,16 +164,26 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
-// Named barrier over `count` threads with an OR of `pred`.
-__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+// Named barrier ID over `count` threads with an OR of `pred` (the id is an
+// immediate: a barrier id held in a register makes the compiler reserve all
+// sixteen barriers and lowers the register budget of the kernel).
+template <int ID>
+__device__ __forceinline__ bool bar_or_n(int count, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
       "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "r"(static_cast<uint32_t>(pred)), "n"(ID), "r"(count)
       : "memory");
   return r != 0;
+}
+__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+  switch (id) {
+    case 1: return bar_or_n<1>(count, pred);
+    case 2: return bar_or_n<2>(count, pred);
+    default: return bar_or_n<3>(count, pred);
+  }
 }
 
 // Split two fp32 weights into fp16 high and low pairs: (a, b) ~= hi + lo.

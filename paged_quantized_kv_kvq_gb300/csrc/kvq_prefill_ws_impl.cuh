@@ -1,0 +1,594 @@
+// kvq_prefill_ws_impl.cuh -- prefill / chunked-prefill attention over a
+// quantized paged KV pool in two passes through a caller workspace, on the
+// 5th-generation tensor cores.
+//
+// Method ("KV Cache优化实战：大模型推理显存占用与加速方案详解",
+// 0539edu.com/news/5800990, §1.1): query token i of a chunk of n tokens of a
+// sequence whose cache holds L tokens (the chunk included) sits at position
+// L - n + i and attends to positions 0 .. L - n + i of the block-paged cache
+// (§2.2), whose K/V are stored as codes with scales (§2.3, §3.3).
+//
+// Why two passes.  Every 64-token key step of a (sequence, kv head) is read
+// by every CTA whose query rows come after it -- 16 of them on average for a
+// 2048-token prompt -- and in the one-pass kernel each of those CTAs turns
+// the codes into fp16 again, on the same SM issue slots the softmax needs.
+// Here a staging pass does that once per step: it writes the step's codes as
+// exact fp16 values, already in the layout the tensor core reads from shared
+// memory (K as a 64 x D tile, V transposed as a D x 64 tile, both K-major
+// with the 128-byte swizzle), plus the step's per-token K and V scales, its
+// valid-token mask and its largest V scale, into one record of the
+// workspace.  The scales stay outside the contraction exactly as in the
+// one-pass kernel, so the arithmetic is the same; only where the fp16 copy
+// of the codes is made differs.
+//
+// The attention pass: a CTA takes one (sequence, kv head) and two tiles of
+// 128 Q rows (one tile for per-channel pools, whose Q has a low part too).
+// Tile 0's issuing thread also bulk-copies each step's record into one of
+// two shared-memory stages, as soon as a stage is free; each tile's four
+// softmax warps own its 128 rows (one row
+// per thread, one TMEM lane each) and run the online softmax (base 2) on the
+// row's 64 scores from TMEM, writing the weights p * s_V * 2^E as fp16 high
+// and low tiles; one thread of each tile issues its tcgen05.mma work: the
+// next step's S = Q.K^T into the other of its two S buffers in TMEM as soon
+// as that step has landed (overlapping the current softmax), and O +=
+// P_hi.V + P_lo.V once the weights are written.  The exponent reference of a
+// row moves only when a score passes it by more than 2^8, so the TMEM
+// accumulator is rescaled rarely.  Every wait is bounded and gives up early
+// once another role has given up; the CTA then flags a timeout, waits
+// (bounded) for its copies and MMAs in flight, and frees TMEM.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "kvq_prefill_tc_impl.cuh"
+
+namespace kvq {
+
+// One staged key step of one (sequence, kv head) in the workspace.
+template <int D>
+struct StepRec {
+  static constexpr int KB = kTcStep * D * 2, VB = D * kTcStep * 2;
+  static constexpr int kh = 0, vt = KB;             // fp16 tiles, swizzled K-major
+  static constexpr int ks = KB + VB;                // float[64] K scales (0: absent token)
+  static constexpr int vs = ks + 256;               // float[64] V scales (0: absent token)
+  static constexpr int mask = vs + 256;             // uint32[2] valid tokens
+  static constexpr int vmax = mask + 8;             // float[2] largest V scale per half
+  static constexpr int copy = vmax + 8;             // bytes the attention pass copies
+  static constexpr int bytes = (copy + 1023) / 1024 * 1024;  // record stride
+};
+
+struct StageParams {
+  PoolView pool;
+  const int* table;  // [S][max_blocks]
+  const int* lens;   // [S]
+  char* ws;          // records [S][max_steps][Hkv]
+  int S, max_blocks, max_ctx, max_steps;
+};
+
+// Staging pass: one CTA of 128 threads per (sequence, key step, kv head).
+template <int FMT, int D>
+__global__ void __launch_bounds__(128) kvq_prefill_stage_kernel(const StageParams p) {
+  using T = FmtTraits<FMT>;
+  using R = StepRec<D>;
+  constexpr int SUB_BYTES = FMT == FMT_INT4_GROUP ? 8 * D : 16 * D * (FMT == FMT_FP16 ? 2 : 1);
+  constexpr int CPS = SUB_BYTES / 16;
+  const PoolView& pool = p.pool;
+  const int bs = pool.bs;
+  const int h = blockIdx.x % pool.Hkv;
+  const int j = (blockIdx.x / pool.Hkv) % p.max_steps;
+  const int s = blockIdx.x / (pool.Hkv * p.max_steps);
+  const int ctx = min(p.lens[s], p.max_ctx);
+  const int t0 = j * kTcStep;
+  if (t0 >= ctx) return;
+  char* rec = p.ws + ((int64_t)(s * p.max_steps + j) * pool.Hkv + h) * R::bytes;
+  const int* trow = p.table + (int64_t)s * p.max_blocks;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto page_of = [&](int t, int& off) -> const char* {  // the page of token t, or null
+    const int n = t / bs;
+    off = t - n * bs;
+    const int phys = n < p.max_blocks ? trow[n] : -1;
+    if (phys < 0 || (int64_t)phys >= pool.num_blocks) return nullptr;
+    return pool.pages + ((int64_t)phys * pool.Hkv + h) * pool.page_bytes;
+  };
+  // codes -> fp16 tiles
+  for (int it = tid; it < 8 * CPS; it += 128) {
+    const int s4 = it / (2 * CPS), rem = it - s4 * (2 * CPS);
+    const bool isv = rem >= CPS;
+    const int ch = isv ? rem - CPS : rem;
+    int off;
+    const char* page = page_of(t0 + 16 * s4, off);
+    const int nvalid = page ? min(max(ctx - (t0 + 16 * s4), 0), 16) : 0;
+    uint4 rv = make_uint4(0, 0, 0, 0);
+    if (nvalid > 0)
+      rv = *reinterpret_cast<const uint4*>(page + (isv ? pool.code_bytes : 0) + (off >> 4) * SUB_BYTES +
+                                           (ch >> 5) * 512 + (ch & 31) * 16);
+    tc_convert_chunk<FMT, D>(rv, ch & 31, ch >> 5, isv, s4, nvalid, rec + R::kh, rec + R::vt);
+  }
+  // per-token scales, the valid-token mask, the largest V scale
+  if (tid < kTcStep) {
+    const int t = t0 + tid;
+    int off;
+    const char* page = t < ctx ? page_of(t, off) : nullptr;
+    if (t < ctx && page == nullptr && (off == 0 || tid == 0)) set_error(pool.err, ERR_RANGE);
+    const bool ok = page != nullptr;
+    float sk = 0.f, sv = ok ? 1.f : 0.f;
+    if (ok) {
+      if constexpr (T::group_scales) {
+        const float* sc = reinterpret_cast<const float*>(page + 2 * pool.code_bytes);
+        sk = sc[off];
+        sv = sc[bs + off];
+      } else if constexpr (T::token_scales) {
+        const int64_t blk = (page - pool.pages) / ((int64_t)pool.Hkv * pool.page_bytes);
+        sk = pool.tok_scales[(blk * 2) * bs + off];
+        sv = pool.tok_scales[(blk * 2 + 1) * bs + off];
+      }
+    }
+    reinterpret_cast<float*>(rec + R::ks)[tid] = sk;
+    reinterpret_cast<float*>(rec + R::vs)[tid] = sv;
+    const uint32_t bits = __ballot_sync(0xffffffffu, ok);
+    float vm = sv;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+    if (lane == 0) {
+      reinterpret_cast<uint32_t*>(rec + R::mask)[warp] = bits;
+      reinterpret_cast<float*>(rec + R::vmax)[warp] = vm;
+    }
+  }
+}
+
+struct PrefillWsParams {
+  PoolView pool;
+  const __half* q;      // [Tq][Hq][D]
+  const int* lens;      // [S]
+  const int* q_start;   // [S + 1]
+  float* out;           // [Tq][Hq][D]
+  const char* ws;       // staged records
+  int S, Hq, G, max_ctx, max_steps;
+  int ngroups;          // CTAs per (sequence, kv head): ceil(tiles / NT)
+  float sm_scale_log2;
+};
+
+// Shared-memory plan of the attention pass (offsets from a 1024-byte aligned
+// base): Q tiles (and low parts), two record stages, weight tiles, misc.
+template <int D, int NT, bool CH>
+struct WsPlan {
+  using R = StepRec<D>;
+  static constexpr int QB = kTcRows * D * 2, PB = kTcRows * kTcStep * 2;
+  static constexpr int q = 0;
+  static constexpr int stage = NT * QB * (CH ? 2 : 1);     // [2][R::bytes]
+  static constexpr int pw = stage + 2 * R::bytes;          // [NT][hi, lo][PB]
+  static constexpr int misc = pw + NT * 2 * PB;
+  // misc: int abort; uint64 kv_full[2], kv_empty[2], s_full[NT], pv_done[NT],
+  // o_full[NT], drain[NT]; uint32 tslot
+  static constexpr int abort = misc, bars = misc + 8, tslot = bars + 8 * (4 + 4 * NT);
+  static constexpr int request = tslot + 16 + 1024;        // + alignment slack
+  // the softmax warps only: two per SM sub-partition keeps the full register
+  // budget (a ninth warp would put three on one sub-partition and cap every
+  // thread at 168 registers); tile 0's issuing thread also copies the records
+  static constexpr int threads = kTcRows * NT;
+  // TMEM: O at 128x, S double-buffered at 256 + 128x + 64k (NT 2) / 128 + 64k (NT 1)
+  static constexpr int cols = NT == 2 ? 512 : 256;
+  static constexpr int s_col(int x, int k) { return NT == 2 ? 256 + 128 * x + 64 * k : 128 + 64 * k; }
+};
+
+template <int FMT>
+struct WsShape {
+  static constexpr int NT = FMT == FMT_INT8_CHANNEL ? 1 : 2;
+};
+
+// Wait on an mbarrier phase with one lane of the warp spinning (bounded, see
+// tc_wait); the other lanes then observe the completed phase with one
+// non-blocking test each.  Warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_test_wait(bar, parity);
+  return ok;
+}
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::channel>::threads, 1)
+    kvq_prefill_ws_kernel(const PrefillWsParams p) {
+  using T = FmtTraits<FMT>;
+  constexpr bool CH = T::channel;
+  constexpr int NT = WsShape<FMT>::NT;
+  using PL = WsPlan<D, NT, CH>;
+  using R = StepRec<D>;
+  const float kNegInf = __int_as_float(0xff800000u);
+
+  extern __shared__ __align__(1024) char smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  char* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PoolView& pool = p.pool;
+  // heaviest tile groups (longest causal ranges) first
+  const int per = p.S * pool.Hkv;
+  const int grp = p.ngroups - 1 - static_cast<int>(blockIdx.x / per);
+  const int seq = static_cast<int>(blockIdx.x % per) % p.S;
+  const int h = static_cast<int>(blockIdx.x % per) / p.S;
+
+  const int qbase = p.q_start[seq];
+  const int nq = p.q_start[seq + 1] - qbase;
+  int ctx = p.lens[seq];
+  if (ctx > p.max_ctx || ctx < nq) {
+    if (grp == 0 && h == 0 && tid == 0) set_error(pool.err, ERR_RANGE);
+    ctx = min(ctx, p.max_ctx);
+  }
+  const int rows_total = nq * p.G;
+  const int row0 = grp * NT * kTcRows;
+  if (row0 >= rows_total) return;  // CTA-uniform
+  const int last = min(rows_total, row0 + NT * kTcRows) - 1;
+  const int kv_end = max(0, min(ctx, ctx - nq + last / p.G + 1));
+  const int nsteps = (kv_end + kTcStep - 1) / kTcStep;
+
+  const bool is_sm = tid < NT * kTcRows;
+  const int X = is_sm ? warp >> 2 : 0;
+  const int r = (warp & 3) * 32 + lane;
+  const int rr = row0 + X * kTcRows + r;
+  const bool row_ok = is_sm && rr < rows_total;
+  const int lim = row_ok ? max(0, ctx - nq + rr / p.G + 1) : 0;
+  const int64_t orow = row_ok ? (int64_t)(qbase + rr / p.G) * p.Hq + h * p.G + rr % p.G : -1;
+  if (nsteps == 0) {  // nothing to attend: zeros (CTA-uniform)
+    if (row_ok)
+      for (int d = 0; d < D; ++d) p.out[orow * D + d] = 0.f;
+    return;
+  }
+
+  volatile int* abort_f = reinterpret_cast<volatile int*>(sm + PL::abort);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL::bars);
+  uint64_t* kv_full = bars;              // [2]: the step's record landed
+  uint64_t* kv_empty = bars + 2;         // [2]: every tile's MMAs of that step done
+  uint64_t* s_full = bars + 4;           // [NT]: S of the tile's next step
+  uint64_t* pv_done = bars + 4 + NT;     // [NT]: the tile's last issued P.V done
+  uint64_t* o_full = bars + 4 + 2 * NT;  // [NT]: the tile's final P.V done
+  uint64_t* drain = bars + 4 + 3 * NT;   // [NT]: clean-up
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PL::tslot);
+  const bool copier = tid == 0;          // tile 0's issuer also copies the records
+  if (tid == 0) {
+    mbar_init(&kv_full[0], 1);
+    mbar_init(&kv_full[1], 1);
+    mbar_init(&kv_empty[0], NT);
+    mbar_init(&kv_empty[1], NT);
+    for (int x = 0; x < NT; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&pv_done[x], 1);
+      mbar_init(&o_full[x], 1);
+      mbar_init(&drain[x], 1);
+    }
+    *abort_f = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tc_alloc(tslot, PL::cols);
+  const char* recs = p.ws + ((int64_t)seq * p.max_steps * pool.Hkv + h) * R::bytes;
+  auto rec_of = [&](int j) { return recs + (int64_t)j * pool.Hkv * R::bytes; };
+  int copied = 0;  // copier: records whose copy has been issued
+  auto copy_rec = [&](int j) {
+    mbar_arrive_expect_tx(&kv_full[j & 1], R::copy);
+    bulk_g2s(sm + PL::stage + (j & 1) * R::bytes, rec_of(j), R::copy, &kv_full[j & 1]);
+    copied = j + 1;
+  };
+  // copier: issue every record copy whose stage is already free (non-blocking)
+  auto pump = [&]() {
+    while (copied < nsteps &&
+           (copied < 2 || mbar_test_wait(&kv_empty[copied & 1], ((copied >> 1) - 1) & 1)))
+      copy_rec(copied);
+  };
+  // copier: make sure record j's copy is issued, waiting for its stage if needed
+  auto ensure = [&](int j) -> bool {
+    while (copied <= j && copied < nsteps) {
+      if (copied >= 2 && !tc_wait(&kv_empty[copied & 1], ((copied >> 1) - 1) & 1, abort_f))
+        return false;
+      copy_rec(copied);
+    }
+    return true;
+  };
+
+  // ---- softmax threads: their own Q row into the tile (K-major, swizzled)
+  float csc = p.sm_scale_log2;
+  if (is_sm) {
+    const __half* src = row_ok ? p.q + orow * D : nullptr;
+    char* qx = sm + PL::q + X * PL::QB;
+    if constexpr (!CH) {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = src ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = v;
+      }
+    } else {
+      // fold the K channel scale into the row, scale it by 2^eq so that its
+      // largest magnitude lies in [2^13, 2^14), split into fp16 hi + lo
+      const float* ksc = pool.chan_scales + (int64_t)h * D;
+      char* ql = sm + PL::q + (NT + X) * PL::QB;
+      float amax = 0.f;
+      if (src)
+        for (int d = 0; d < D; ++d) amax = fmaxf(amax, fabsf(__half2float(src[d]) * ksc[d]));
+      const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
+      const float up = ldexpf(1.f, eq);
+      csc = ldexpf(csc, -eq);
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 hv4 = make_uint4(0, 0, 0, 0), lv4 = make_uint4(0, 0, 0, 0);
+        if (src) {
+          uint32_t* ho = reinterpret_cast<uint32_t*>(&hv4);
+          uint32_t* lo = reinterpret_cast<uint32_t*>(&lv4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = 8 * c + 2 * e;
+            split_h2(__half2float(src[d]) * ksc[d] * up, __half2float(src[d + 1]) * ksc[d + 1] * up,
+                     ho[e], lo[e]);
+          }
+        }
+        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = hv4;
+        *reinterpret_cast<uint4*>(ql + sw128_offset(r, 8 * c, kTcRows)) = lv4;
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  {
+    // ======================= softmax + MMA issue, tile X =======================
+    const uint32_t tO = tmem + X * 128;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t qa = smem_u32(sm + PL::q + X * PL::QB);
+    const uint32_t qla = smem_u32(sm + PL::q + (NT + X) * PL::QB);
+    const uint32_t pha = smem_u32(sm + PL::pw + X * 2 * PL::PB);
+    const uint32_t pla = pha + PL::PB;
+    char* p_hi = sm + PL::pw + X * 2 * PL::PB;
+    char* p_lo = p_hi + PL::PB;
+    constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
+    constexpr uint32_t id_o = tc_idesc_f16(128, D);
+    const bool issuer = r == 0;  // thread 0 of the tile
+    const int bar_id = 1 + X;
+    auto stage_of = [&](int j) { return sm + PL::stage + (j & 1) * R::bytes; };
+    auto issue_s = [&](int j) {  // S = Q K^T of step j into its S buffer (issuer)
+      const uint32_t kha = smem_u32(stage_of(j) + R::kh);
+      const uint32_t ts = tmem + PL::s_col(X, j & 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ko = (kk >> 2) * (kTcStep * 128) + (kk & 3) * 32;
+        const uint32_t qo = (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
+        tc_mma_f16(ts, sw128_desc(qa + qo), sw128_desc(kha + ko), id_s, kk > 0);
+        if constexpr (CH) tc_mma_f16(ts, sw128_desc(qla + qo), sw128_desc(kha + ko), id_s, 1);
+      }
+      tc_commit(&s_full[X]);
+    };
+    bool failed = false;
+    if (copier) pump();  // records 0 and 1
+    if (issuer && tc_wait(&kv_full[0], 0, abort_f)) {
+      tc_fence_after();
+      issue_s(0);
+    }
+    __syncwarp();
+    float m = kNegInf, l = 0.f;
+    int E = T::row_scales ? 100 : 14 - kTcSlack;
+    int next_s = 1;  // issuer: the next step whose S is not yet issued
+    for (int j = 0; j < nsteps; ++j) {
+      const int b = j & 1;
+      const char* st = stage_of(j);
+      bool ok = warp_wait(&s_full[X], j & 1, abort_f);
+      // the record's scales and mask landed with kv_full (already complete:
+      // S of this step was computed from its K tile)
+      ok = ok && warp_wait(&kv_full[b], (j >> 1) & 1, abort_f);
+      if (bar_or(bar_id, kTcRows, !ok)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      // the next step's S goes into the other S buffer now if its record has
+      // landed (the softmax of step j-1, which read that buffer, is complete)
+      if (copier) pump();
+      if (issuer && next_s == j + 1 && j + 1 < nsteps &&
+          mbar_test_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
+        issue_s(j + 1);
+        next_s = j + 2;
+      }
+      __syncwarp();
+      const int t0 = j * kTcStep;
+      float z[kTcStep];
+      {
+        const uint32_t ts = tmem + PL::s_col(X, b) + lane_base;
+        float a[32];
+        tc_ld32(ts, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = a[i];
+        tc_ld32(ts + 32, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
+      }
+      const float* ksb = reinterpret_cast<const float*>(st + R::ks);
+      const float* vsb = reinterpret_cast<const float*>(st + R::vs);
+      const uint32_t mk0 = reinterpret_cast<const uint32_t*>(st + R::mask)[0];
+      const uint32_t mk1 = reinterpret_cast<const uint32_t*>(st + R::mask)[1];
+      const int lr = lim - t0;  // tokens [0, lr) of this step are attended by this row
+      float mx = kNegInf;
+      if (lr >= kTcStep && (mk0 & mk1) == 0xffffffffu) {
+#pragma unroll
+        for (int t = 0; t < kTcStep; t += 4) {
+          float a0 = z[t], a1 = z[t + 1], a2 = z[t + 2], a3 = z[t + 3];
+          if constexpr (T::row_scales) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ksb + t);
+            f2_unpack(f2_mul(f2_pack(a0, a1), f2_pack(k4.x, k4.y)), a0, a1);
+            f2_unpack(f2_mul(f2_pack(a2, a3), f2_pack(k4.z, k4.w)), a2, a3);
+          }
+          z[t] = a0;
+          z[t + 1] = a1;
+          z[t + 2] = a2;
+          z[t + 3] = a3;
+          mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < kTcStep; ++t) {
+          const bool okt = t < lr && (((t < 32 ? mk0 : mk1) >> (t & 31)) & 1u);
+          z[t] = okt ? (T::row_scales ? z[t] * ksb[t] : z[t]) : kNegInf;
+          mx = fmaxf(mx, z[t]);
+        }
+      }
+      // scores in log2 units are z * csc (csc > 0); the reference maximum m
+      // moves only when the step's maximum passes it by more than kTcSlack
+      const float mxz = mx == kNegInf ? kNegInf : mx * csc;
+      const float mn = (m == kNegInf || mxz > m + kTcSlack) ? mxz : m;
+      const float ms = mn == kNegInf ? 0.f : mn;
+      int dE = 0;
+      if constexpr (T::row_scales) {
+        const float* vm = reinterpret_cast<const float*>(st + R::vmax);
+        const float vmax = fmaxf(vm[0], vm[1]);
+        if (vmax > 0.f) {
+          const int En = min(E, 13 - kTcSlack - exponent_of(vmax));
+          dE = En - E;
+          E = En;
+        }
+      }
+      // p' = 2^(z csc - ms + E), the weight before the V scale
+      const float nbias = static_cast<float>(E) - ms;
+      uint64_t rs2 = f2_pack(0.f, 0.f);
+      {
+        const uint64_t c2 = f2_pack(csc, csc), b2 = f2_pack(nbias, nbias);
+#pragma unroll
+        for (int t = 0; t < kTcStep; t += 2) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(z[t], z[t + 1]), c2, b2), a0, a1);
+          z[t] = fast_exp2(a0);  // 0 for masked tokens
+          z[t + 1] = fast_exp2(a1);
+          rs2 = f2_add(rs2, f2_pack(z[t], z[t + 1]));
+        }
+      }
+      float rsa, rsb;
+      f2_unpack(rs2, rsa, rsb);
+      const float alpha = fast_exp2(m - ms);
+      l = fmaf(l, alpha, (rsa + rsb) * pow2f(-E));
+      m = mn;
+      if (j > 0) {
+        // the previous step's P.V must be done before O is rescaled and the
+        // weight tiles are overwritten
+        const bool okp = warp_wait(&pv_done[X], (j - 1) & 1, abort_f);
+        if (bar_or(bar_id, kTcRows, !okp)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const float f = alpha * pow2f(dE);
+        if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc_ld32(tO + lane_base + 32 * c, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tc_st32(tO + lane_base + 32 * c, o);
+          }
+          tc_wait_st();
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kTcStep / 8; ++c) {
+        uint32_t hv[4], lv[4];
+        float vv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if constexpr (T::row_scales) {
+          const float4 v0 = *reinterpret_cast<const float4*>(vsb + 8 * c);
+          const float4 v1 = *reinterpret_cast<const float4*>(vsb + 8 * c + 4);
+          vv[0] = v0.x, vv[1] = v0.y, vv[2] = v0.z, vv[3] = v0.w;
+          vv[4] = v1.x, vv[5] = v1.y, vv[6] = v1.z, vv[7] = v1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float w0 = z[8 * c + 2 * e], w1 = z[8 * c + 2 * e + 1];
+          // masked tokens (absent, past the end, or causally later) have p' = 0;
+          // an absent token's V scale is 0 too
+          if constexpr (T::row_scales)
+            f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(vv[2 * e], vv[2 * e + 1])), w0, w1);
+          tc_split2(w0, w1, hv[e], lv[e]);
+        }
+        const uint32_t o = sw128_offset(r, 8 * c, kTcRows);
+        *reinterpret_cast<uint4*>(p_hi + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(p_lo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      bar_or(bar_id, kTcRows, false);  // the tile's weights are written, S is read
+      if (issuer) {
+        tc_fence_after();
+        const uint32_t vta = smem_u32(st + R::vt);
+#pragma unroll
+        for (int kk = 0; kk < kTcStep / 16; ++kk)
+          tc_mma_f16(tO, sw128_desc(pha + kk * 32), sw128_desc(vta + kk * 32), id_o,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTcStep / 16; ++kk)
+          tc_mma_f16(tO, sw128_desc(pla + kk * 32), sw128_desc(vta + kk * 32), id_o, 1u);
+        tc_commit(&kv_empty[b]);
+        tc_commit(&pv_done[X]);
+        if (j + 1 == nsteps) tc_commit(&o_full[X]);
+        if (copier) pump();
+        if (next_s == j + 1 && j + 1 < nsteps) {
+          // its record had not landed earlier: wait for it now (issuing its
+          // copy first if the stage only just became free)
+          if ((!copier || ensure(j + 1)) &&
+              tc_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_f)) {
+            tc_fence_after();
+            issue_s(j + 1);
+          }
+          next_s = j + 2;
+        }
+      }
+      __syncwarp();
+    }
+    if (!failed) {
+      // ---- normalised output rows once the tile's last P.V is done
+      const bool ok = warp_wait(&o_full[X], 0, abort_f);
+      if (bar_or(bar_id, kTcRows, !ok)) {
+        failed = true;
+      } else {
+        tc_fence_after();
+        const float f = l > 0.f ? pow2f(-E) / l : 0.f;
+        const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc_ld32(tO + lane_base + 32 * c, o);
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(p.out + orow * D + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 v = make_float4(o[4 * i] * f, o[4 * i + 1] * f, o[4 * i + 2] * f,
+                                     o[4 * i + 3] * f);
+              if constexpr (CH) {
+                const float* cs = vch + 32 * c + 4 * i;
+                v.x *= cs[0];
+                v.y *= cs[1];
+                v.z *= cs[2];
+                v.w *= cs[3];
+              }
+              dst[i] = v;
+            }
+          }
+        }
+      }
+    }
+    if (issuer) {
+      // every MMA this thread issued has completed before TMEM is freed
+      tc_commit(&drain[X]);
+      bool ok = false;
+      for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(&drain[X], 0);
+    }
+    if (copier) {
+      // every record copy issued has landed before the CTA exits (all of them
+      // were consumed unless a wait gave up)
+      for (int j = copied >= 2 ? copied - 2 : 0; j < copied; ++j) {
+        bool ok = false;
+        for (int tries = 0; tries < kWaitTries && !ok; ++tries)
+          ok = mbar_try_wait(&kv_full[j & 1], (j >> 1) & 1);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_f) set_error(pool.err, ERR_TIMEOUT);
+  if (warp == 0) tc_dealloc(tmem, PL::cols);
+}
+
+}  // namespace kvq

@@ -160,7 +160,7 @@ def test_shared4k_256_cascade_full():
 def test_prefill_8x2048_full():
     """Prompt prefill at the size the bench times: 8 prompts of 2048 tokens of
     the 64x2048 layout (INT8 per-group 128), each whole prompt one chunk, all
-    in one kvq_prefill call; sampled query rows of the first and last prompt
+    in one kvq_prefill_ex call; sampled query rows of the first and last prompt
     (the first rows, the sub-tile and page edges, the middle and the end),
     each against the oracle's decode over its causal length."""
     w = synth.workload("gqa_64x2048", S=8, layers=1)
@@ -179,8 +179,12 @@ def test_prefill_8x2048_full():
     for s in seqs:
         q[int(qs[s]):int(qs[s + 1])] = _t(qh[s])
     out = torch.empty((T, w.Hq, w.D), dtype=torch.float32, device=DEV)
-    kvq.kvq_prefill(pool.handle, q, _t(qs), int(lens.max()), _t(w.block_table), _t(w.context_lens),
-                    int(lens.max()), w.D ** -0.5, out)
+    mc = int(lens.max())
+    # through kvq_prefill_ex, as the bench times it (key steps staged once)
+    ws = torch.empty(kvq.kvq_prefill_workspace_bytes(pool.handle, w.S, mc), dtype=torch.uint8,
+                     device=DEV)
+    kvq.kvq_prefill_ex(pool.handle, q, _t(qs), mc, _t(w.block_table), _t(w.context_lens), mc,
+                       w.D ** -0.5, out, ws)
     torch.cuda.synchronize()
     assert pool.error() == kvq.KVQ_OK
     ref, rtable, _ = oracle_layer(w, fmt, group, k, v, slots, seqs)

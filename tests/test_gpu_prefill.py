@@ -38,8 +38,23 @@ def _expand(table, lens, nq):
     return np.array(rows, np.int32), np.array(L, np.int32)
 
 
+def _prefill(api, pool, q, qs, mq, table, lens, mc, sm, out):
+    """One prefill call: "one_pass" = kvq_prefill, "two_pass" = kvq_prefill_ex
+    with its workspace (the staged fp16 key steps)."""
+    if api == "one_pass":
+        kvq.kvq_prefill(pool.handle, q, qs, mq, table, lens, mc, sm, out)
+        return
+    S = qs.numel() - 1
+    nb = kvq.kvq_prefill_workspace_bytes(pool.handle, S, mc)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=DEV) if nb else None
+    kvq.kvq_prefill_ex(pool.handle, q, qs, mq, table, lens, mc, sm, out, ws)
+
+
+APIS = ["one_pass", "two_pass"]
+
+
 def _case(fmt, group, name="gqa_64x2048", S=3, L=300, nq=(50, 17, 64), lens=None, seed=0,
-          heads=None, **kw):
+          heads=None, api="one_pass", **kw):
     w = synth.workload(name, S=S, L=L, layers=1, **kw)
     w.layer_formats = [(fmt, group)]
     if heads is not None:
@@ -54,34 +69,37 @@ def _case(fmt, group, name="gqa_64x2048", S=3, L=300, nq=(50, 17, 64), lens=None
     qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
     q = _queries(int(qs[-1]), w.Hq, w.D, seed)
     out = torch.empty((int(qs[-1]), w.Hq, w.D), dtype=torch.float32, device=DEV)
-    kvq.kvq_prefill(pool.handle, _t(q), _t(qs), int(nq.max()), _t(w.block_table), _t(lens),
-                    int(max(lens.max(), 1)), w.D ** -0.5, out)
+    _prefill(api, pool, _t(q), _t(qs), int(nq.max()), _t(w.block_table), _t(lens),
+             int(max(lens.max(), 1)), w.D ** -0.5, out)
     torch.cuda.synchronize()
     t_exp, l_exp = _expand(table, lens, nq)
     exp = ref.decode(q, t_exp, l_exp)
     return pool, out.cpu().numpy(), exp, l_exp
 
 
+@pytest.mark.parametrize("api", APIS)
 @pytest.mark.parametrize("fmt,group", FORMATS)
-def test_prefill_parity(fmt, group):
-    pool, got, exp, _ = _case(fmt, group)
+def test_prefill_parity(fmt, group, api):
+    pool, got, exp, _ = _case(fmt, group, api=api)
     assert pool.error() == kvq.KVQ_OK
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     pool.close()
 
 
-def test_prefill_whole_prompt_and_long_context():
+@pytest.mark.parametrize("api", APIS)
+def test_prefill_whole_prompt_and_long_context(api):
     """A fresh prompt (chunk = whole context) and a chunk deep into a long
     context, MHA with head_dim 128, and GQA 4:1 with D 64 (tiny)."""
-    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 128, S=2, L=1300, nq=(1300, 300))
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 128, S=2, L=1300, nq=(1300, 300), api=api)
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     assert pool.error() == kvq.KVQ_OK
     pool.close()
     pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 64, name="mha_100_int8g64", S=2, L=400,
-                              nq=(33, 1))
+                              nq=(33, 1), api=api)
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     pool.close()
-    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 64, name="tiny", S=4, L=None, nq=(17, 5, 64, 3))
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_GROUP, 64, name="tiny", S=4, L=None, nq=(17, 5, 64, 3),
+                              api=api)
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     pool.close()
 
@@ -103,15 +121,17 @@ def test_prefill_one_token_chunks_equal_decode():
     pool.close()
 
 
-def test_prefill_edges():
+@pytest.mark.parametrize("api", APIS)
+def test_prefill_edges(api):
     """Ragged tiles, a grid wider than the chunks, an empty chunk, and a
     context shorter than its chunk (flagged; the rows left without a position
     get zeros)."""
-    pool, got, exp, l_exp = _case(kvq.KVQ_FP16, 0, nq=(5, 0, 1))
+    pool, got, exp, l_exp = _case(kvq.KVQ_FP16, 0, nq=(5, 0, 1), api=api)
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     assert pool.error() == kvq.KVQ_OK
     pool.close()
-    pool, got, exp, l_exp = _case(kvq.KVQ_INT8_PER_GROUP, 128, nq=(20, 3, 7), lens=(10, 300, 300))
+    pool, got, exp, l_exp = _case(kvq.KVQ_INT8_PER_GROUP, 128, nq=(20, 3, 7), lens=(10, 300, 300),
+                                  api=api)
     assert pool.error() == kvq.KVQ_ERR_OUT_OF_RANGE
     assert not got[:10].any()          # positions before the start of the context
     np.testing.assert_allclose(got[10:], exp[10:], rtol=0, atol=TOL)
@@ -124,10 +144,11 @@ def test_prefill_edges():
     (kvq.KVQ_FP8_E4M3_PER_TOKEN, 0, dict(S=2, L=515, bs=32), (64, 515)),
     (kvq.KVQ_INT4_PER_GROUP, 128, dict(S=2, L=640, bs=64), (640, 65)),
 ])
-def test_prefill_block_sizes(fmt, group, kw, nq):
+@pytest.mark.parametrize("api", APIS)
+def test_prefill_block_sizes(fmt, group, kw, nq, api):
     """Blocks of 32 and 64 tokens: a 64-token key step spans two pages or one;
     ragged ends of the context and of the chunk."""
-    pool, got, exp, _ = _case(fmt, group, nq=nq, **kw)
+    pool, got, exp, _ = _case(fmt, group, nq=nq, api=api, **kw)
     assert pool.error() == kvq.KVQ_OK
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     pool.close()
@@ -135,11 +156,39 @@ def test_prefill_block_sizes(fmt, group, kw, nq):
 
 @pytest.mark.parametrize("heads,nq", [((32, 32), (300, 1, 129)), ((32, 4), (100, 37, 16)),
                                       ((32, 1), (40, 3, 1)), ((24, 2), (77, 50, 9))])
-def test_prefill_head_groups(heads, nq):
+@pytest.mark.parametrize("api", APIS)
+def test_prefill_head_groups(heads, nq, api):
     """MHA (one Q head per kv head: 128 query tokens per tile), GQA 8:1, MQA
     (32 heads: 4 query tokens per tile) and GQA 12:1 (tiles that split a
     token's heads), with the per-token format whose scale spans all heads."""
-    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_TOKEN, 0, S=3, L=300, nq=nq, heads=heads)
+    pool, got, exp, _ = _case(kvq.KVQ_INT8_PER_TOKEN, 0, S=3, L=300, nq=nq, heads=heads, api=api)
     assert pool.error() == kvq.KVQ_OK
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
     pool.close()
+
+
+def test_prefill_ex_workspace_rules():
+    """kvq_prefill_ex refuses a missing or short workspace for the formats it
+    stages, and needs none (runs kvq_prefill) for per-group formats with
+    several groups per head."""
+    w = synth.workload("gqa_64x2048", S=2, L=100, layers=1)
+    for fmt, group in [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_INT8_PER_GROUP, 32)]:
+        pool = kvq.KVPool(w.num_blocks, w.bs, w.Hkv, w.D, fmt, group, device=DEV)
+        nb = kvq.kvq_prefill_workspace_bytes(pool.handle, w.S, 100)
+        q = torch.zeros((10, w.Hq, w.D), dtype=torch.float16, device=DEV)
+        qs = _t(np.array([0, 5, 10], np.int32))
+        out = torch.empty((10, w.Hq, w.D), dtype=torch.float32, device=DEV)
+        args = (pool.handle, q, qs, 5, _t(w.block_table), _t(w.context_lens), 100, 0.1, out)
+        if group == 128:
+            assert nb == w.S * 2 * w.Hkv * 33792     # two 64-token steps per sequence
+            with pytest.raises(kvq.KVQError) as e:
+                kvq.kvq_prefill_ex(*args, None)
+            assert e.value.status == kvq.KVQ_ERR_WORKSPACE
+            with pytest.raises(kvq.KVQError) as e:
+                kvq.kvq_prefill_ex(*args, torch.empty(nb - 256, dtype=torch.uint8, device=DEV))
+            assert e.value.status == kvq.KVQ_ERR_WORKSPACE
+        else:
+            assert nb == 0
+            kvq.kvq_prefill_ex(*args, None)
+        torch.cuda.synchronize()
+        pool.close()
