@@ -893,7 +893,7 @@ def main():
                     help="decode: the decode step (default); prefill: prompt prefill")
     ap.add_argument("--prefill-seqs", type=int, default=8,
                     help="prompts in the prefill batch (--op prefill)")
-    ap.add_argument("--prefill-api", default="plain", choices=["plain", "ex"],
+    ap.add_argument("--prefill-api", default="ex", choices=["plain", "ex"],
                     help="--op prefill: kvq_prefill (one pass) or kvq_prefill_ex (key steps "
                          "staged once in a workspace, then attention)")
     ap.add_argument("--block-size", type=int, default=None,

@@ -193,6 +193,21 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Polls of the spinning phase of a bounded wait (non-blocking tests, each
+// well under a microsecond) before it falls back to suspending tries.
+constexpr int kSpinPolls = 20000;
+
+// Bounded wait for the phase with this parity: first spin on non-blocking
+// tests (a suspended thread is not always resumed the moment the phase
+// completes), then up to `tries` suspending tries of <= 1 ms each.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int tries) {
+  for (int i = 0; i < kSpinPolls; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  for (int i = 0; i < tries; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
 // Bulk (TMA, non-tensor) copy global -> shared, completion counted in bytes on
 // the mbarrier.  Addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,

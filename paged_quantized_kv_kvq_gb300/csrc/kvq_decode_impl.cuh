@@ -809,8 +809,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   int cst = 0;
   uint32_t cph = 0;
   auto wait_stage = [&](int st, uint32_t parity) -> bool {
-    bool ok = false;
-    for (int tries = 0; tries < p.wait_tries && !ok; ++tries) ok = mbar_try_wait(&bars[st], parity);
+    const bool ok = mbar_wait_bounded(&bars[st], parity, p.wait_tries);
     return __all_sync(0xffffffffu, ok);
   };
 

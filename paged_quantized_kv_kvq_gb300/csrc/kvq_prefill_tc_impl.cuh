@@ -156,6 +156,12 @@ __device__ __forceinline__ void tc_convert_chunk(uint4 raw, int L, int c, bool i
 // Bounded wait that gives up early once another role has set *abort; a wait
 // that runs out sets it.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  // spin first: a suspended thread is not always resumed the moment the
+  // phase completes, and these waits are on the critical path
+  for (int i = 0; i < kSpinPolls; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+  }
   for (int tries = 0; tries < kWaitTries; ++tries) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;

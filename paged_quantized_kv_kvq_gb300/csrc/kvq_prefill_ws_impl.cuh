@@ -23,19 +23,26 @@
 //
 // The attention pass: a CTA takes one (sequence, kv head) and two tiles of
 // 128 Q rows (one tile for per-channel pools, whose Q has a low part too).
-// Tile 0's issuing thread also bulk-copies each step's record into one of
-// two shared-memory stages, as soon as a stage is free; each tile's four
-// softmax warps own its 128 rows (one row
-// per thread, one TMEM lane each) and run the online softmax (base 2) on the
-// row's 64 scores from TMEM, writing the weights p * s_V * 2^E as fp16 high
-// and low tiles; one thread of each tile issues its tcgen05.mma work: the
-// next step's S = Q.K^T into the other of its two S buffers in TMEM as soon
-// as that step has landed (overlapping the current softmax), and O +=
-// P_hi.V + P_lo.V once the weights are written.  The exponent reference of a
-// row moves only when a score passes it by more than 2^8, so the TMEM
-// accumulator is rescaled rarely.  Every wait is bounded and gives up early
-// once another role has given up; the CTA then flags a timeout, waits
-// (bounded) for its copies and MMAs in flight, and frees TMEM.
+// Its eight softmax warps own the rows (one row per thread, one TMEM lane
+// each); one control thread bulk-copies the step records into four shared
+// memory stages and issues every tcgen05.mma.  Per tile, tensor memory holds
+// the output accumulator O, the step's scores S and the step's weights P:
+//   * the control thread issues S = Q.K^T (M 128, N 64, K D, A and B from
+//     shared memory) for every tile once the step's record has landed and the
+//     tile has read its previous S;
+//   * each softmax thread reads its row of S, signals that S may be
+//     overwritten, applies the K scales, the causal limit and the online
+//     softmax (base 2), and writes the weights p * s_V * 2^E as fp16 high and
+//     low parts into P with tcgen05.st; the row's exponent reference moves
+//     only when a score passes it by more than 2^8, and only then (or when E
+//     drops) is its row of O rescaled;
+//   * the control thread then issues O += P_hi.V + P_lo.V (M 128, N D, K 64,
+//     A from tensor memory, V^T from shared memory).
+// So the next step's S is computed while the softmax of the current one runs,
+// and the two tiles' softmax and tensor work interleave.  The threads meet
+// only at mbarriers; every wait is bounded and gives up early once another
+// role has given up; the CTA then flags a timeout, waits (bounded) for its
+// copies and MMAs in flight, and frees TMEM.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -148,28 +155,7 @@ struct PrefillWsParams {
   float sm_scale_log2;
 };
 
-// Shared-memory plan of the attention pass (offsets from a 1024-byte aligned
-// base): Q tiles (and low parts), two record stages, weight tiles, misc.
-template <int D, int NT, bool CH>
-struct WsPlan {
-  using R = StepRec<D>;
-  static constexpr int QB = kTcRows * D * 2, PB = kTcRows * kTcStep * 2;
-  static constexpr int q = 0;
-  static constexpr int stage = NT * QB * (CH ? 2 : 1);     // [2][R::bytes]
-  static constexpr int pw = stage + 2 * R::bytes;          // [NT][hi, lo][PB]
-  static constexpr int misc = pw + NT * 2 * PB;
-  // misc: int abort; uint64 kv_full[2], kv_empty[2], s_full[NT], pv_done[NT],
-  // o_full[NT], drain[NT]; uint32 tslot
-  static constexpr int abort = misc, bars = misc + 8, tslot = bars + 8 * (4 + 4 * NT);
-  static constexpr int request = tslot + 16 + 1024;        // + alignment slack
-  // the softmax warps only: two per SM sub-partition keeps the full register
-  // budget (a ninth warp would put three on one sub-partition and cap every
-  // thread at 168 registers); tile 0's issuing thread also copies the records
-  static constexpr int threads = kTcRows * NT;
-  // TMEM: O at 128x, S double-buffered at 256 + 128x + 64k (NT 2) / 128 + 64k (NT 1)
-  static constexpr int cols = NT == 2 ? 512 : 256;
-  static constexpr int s_col(int x, int k) { return NT == 2 ? 256 + 128 * x + 64 * k : 128 + 64 * k; }
-};
+constexpr int kWsStages = 4;  // record stages in shared memory
 
 template <int FMT>
 struct WsShape {
@@ -187,12 +173,38 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+// Shared-memory plan of the attention pass (offsets from a 1024-byte aligned
+// base): Q tiles (and low parts), kWsStages record stages, misc.
+template <int D, int NT, bool CH>
+struct WsPlan {
+  using R = StepRec<D>;
+  static constexpr int QB = kTcRows * D * 2;
+  static constexpr int q = 0;
+  static constexpr int stage = NT * QB * (CH ? 2 : 1);     // [kWsStages][R::bytes]
+  static constexpr int misc = stage + kWsStages * R::bytes;
+  // misc: int abort; uint64 kv_full[S], kv_empty[S], s_full[NT], s_read[NT],
+  // p_full[NT], pv_done[NT], o_full[NT], drain; uint32 tslot
+  static constexpr int abort = misc, bars = misc + 8;
+  static constexpr int nbars = 2 * kWsStages + 5 * NT + 1;
+  static constexpr int tslot = bars + 8 * nbars;
+  static constexpr int request = tslot + 16 + 1024;        // + alignment slack
+  // the softmax warps plus one control warp per tile (its lane 0 issues that
+  // tile's MMAs; tile 0's also issues the record copies)
+  static constexpr int threads = kTcRows * NT + 32 * NT;
+  // TMEM: per tile x, O at 128x (D columns), S at 256 + 128x (64), P at S + 64
+  // (32 columns of fp16 pairs for the high part, 32 for the low part); one
+  // tile: O 0, S 128, P 192
+  static constexpr int cols = NT == 2 ? 512 : 256;
+  static constexpr int s_col(int x) { return NT == 2 ? 256 + 128 * x : 128; }
+};
+
 template <int FMT, int D>
 __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::channel>::threads, 1)
     kvq_prefill_ws_kernel(const PrefillWsParams p) {
   using T = FmtTraits<FMT>;
   constexpr bool CH = T::channel;
   constexpr int NT = WsShape<FMT>::NT;
+  constexpr int NS = kWsStages;
   using PL = WsPlan<D, NT, CH>;
   using R = StepRec<D>;
   const float kNegInf = __int_as_float(0xff800000u);
@@ -237,52 +249,32 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
 
   volatile int* abort_f = reinterpret_cast<volatile int*>(sm + PL::abort);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL::bars);
-  uint64_t* kv_full = bars;              // [2]: the step's record landed
-  uint64_t* kv_empty = bars + 2;         // [2]: every tile's MMAs of that step done
-  uint64_t* s_full = bars + 4;           // [NT]: S of the tile's next step
-  uint64_t* pv_done = bars + 4 + NT;     // [NT]: the tile's last issued P.V done
-  uint64_t* o_full = bars + 4 + 2 * NT;  // [NT]: the tile's final P.V done
-  uint64_t* drain = bars + 4 + 3 * NT;   // [NT]: clean-up
+  uint64_t* kv_full = bars;                // [NS]: the step's record landed
+  uint64_t* kv_empty = bars + NS;          // [NS]: the MMAs of the step in that stage done
+  uint64_t* s_full = bars + 2 * NS;        // [NT]: S of the tile's current step
+  uint64_t* s_read = s_full + NT;          // [NT]: the tile's 128 rows have read S
+  uint64_t* p_full = s_read + NT;          // [NT]: the tile's 128 rows have written P
+  uint64_t* pv_done = p_full + NT;         // [NT]: the tile's last issued P.V done
+  uint64_t* o_full = pv_done + NT;         // [NT]: the tile's final P.V done
+  uint64_t* drain = o_full + NT;           // clean-up
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PL::tslot);
-  const bool copier = tid == 0;          // tile 0's issuer also copies the records
   if (tid == 0) {
-    mbar_init(&kv_full[0], 1);
-    mbar_init(&kv_full[1], 1);
-    mbar_init(&kv_empty[0], NT);
-    mbar_init(&kv_empty[1], NT);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], NT);  // every tile's MMAs of the step done
+    }
     for (int x = 0; x < NT; ++x) {
       mbar_init(&s_full[x], 1);
+      mbar_init(&s_read[x], kTcRows);
+      mbar_init(&p_full[x], kTcRows);
       mbar_init(&pv_done[x], 1);
       mbar_init(&o_full[x], 1);
-      mbar_init(&drain[x], 1);
     }
+    mbar_init(drain, NT);
     *abort_f = 0;
     fence_barrier_init();
   }
   if (warp == 0) tc_alloc(tslot, PL::cols);
-  const char* recs = p.ws + ((int64_t)seq * p.max_steps * pool.Hkv + h) * R::bytes;
-  auto rec_of = [&](int j) { return recs + (int64_t)j * pool.Hkv * R::bytes; };
-  int copied = 0;  // copier: records whose copy has been issued
-  auto copy_rec = [&](int j) {
-    mbar_arrive_expect_tx(&kv_full[j & 1], R::copy);
-    bulk_g2s(sm + PL::stage + (j & 1) * R::bytes, rec_of(j), R::copy, &kv_full[j & 1]);
-    copied = j + 1;
-  };
-  // copier: issue every record copy whose stage is already free (non-blocking)
-  auto pump = [&]() {
-    while (copied < nsteps &&
-           (copied < 2 || mbar_test_wait(&kv_empty[copied & 1], ((copied >> 1) - 1) & 1)))
-      copy_rec(copied);
-  };
-  // copier: make sure record j's copy is issued, waiting for its stage if needed
-  auto ensure = [&](int j) -> bool {
-    while (copied <= j && copied < nsteps) {
-      if (copied >= 2 && !tc_wait(&kv_empty[copied & 1], ((copied >> 1) - 1) & 1, abort_f))
-        return false;
-      copy_rec(copied);
-    }
-    return true;
-  };
 
   // ---- softmax threads: their own Q row into the tile (K-major, swizzled)
   float csc = p.sm_scale_log2;
@@ -328,77 +320,124 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  auto stage_of = [&](int j) { return sm + PL::stage + (j % NS) * R::bytes; };
 
-  {
-    // ======================= softmax + MMA issue, tile X =======================
+  if (!is_sm) {
+    // ======================= control: tile C's MMAs (tile 0's: the copies too) =======================
+    const int C = warp - 4 * NT;
+    if (lane == 0) {
+      const char* recs = p.ws + ((int64_t)seq * p.max_steps * pool.Hkv + h) * R::bytes;
+      int copied = 0;
+      auto copy_rec = [&](int j) {
+        mbar_arrive_expect_tx(&kv_full[j % NS], R::copy);
+        bulk_g2s(stage_of(j), recs + (int64_t)j * pool.Hkv * R::bytes, R::copy, &kv_full[j % NS]);
+        copied = j + 1;
+      };
+      // issue every copy whose stage is free (non-blocking; tile 0's thread)
+      auto pump = [&]() {
+        while (C == 0 && copied < nsteps &&
+               (copied < NS || mbar_test_wait(&kv_empty[copied % NS], ((copied / NS) - 1) & 1)))
+          copy_rec(copied);
+      };
+      // make sure record j's copy is issued, waiting for its stage if needed
+      // (tile 0's thread; the others only wait for the record to land)
+      auto ensure = [&](int j) -> bool {
+        while (C == 0 && copied <= j) {
+          if (copied >= NS && !tc_wait(&kv_empty[copied % NS], ((copied / NS) - 1) & 1, abort_f))
+            return false;
+          copy_rec(copied);
+        }
+        return true;
+      };
+      constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
+      constexpr uint32_t id_o = tc_idesc_f16(128, D);
+      auto issue_s = [&](int x, int j) {  // S_x = Q_x K^T of step j
+        const uint32_t qa = smem_u32(sm + PL::q + x * PL::QB);
+        const uint32_t qla = smem_u32(sm + PL::q + (NT + x) * PL::QB);
+        const uint32_t kha = smem_u32(stage_of(j) + R::kh);
+        const uint32_t ts = tmem + PL::s_col(x);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kTcStep * 128) + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
+          tc_mma_f16(ts, sw128_desc(qa + qo), sw128_desc(kha + ko), id_s, kk > 0);
+          if constexpr (CH) tc_mma_f16(ts, sw128_desc(qla + qo), sw128_desc(kha + ko), id_s, 1);
+        }
+        tc_commit(&s_full[x]);
+      };
+      auto issue_pv = [&](int x, int j) {  // O_x += P_x V of step j (P in TMEM)
+        const uint32_t vta = smem_u32(stage_of(j) + R::vt);
+        const uint32_t tp = tmem + PL::s_col(x) + 64;
+        const uint32_t to = tmem + x * 128;
+#pragma unroll
+        for (int kk = 0; kk < kTcStep / 16; ++kk)
+          tc_mma_f16_ts(to, tp + 8 * kk, sw128_desc(vta + kk * 32), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTcStep / 16; ++kk)
+          tc_mma_f16_ts(to, tp + 32 + 8 * kk, sw128_desc(vta + kk * 32), id_o, 1u);
+        tc_commit(&pv_done[x]);
+      };
+      pump();
+      for (int j = 0; j <= nsteps && !*abort_f; ++j) {
+        if (j < nsteps) {
+          // S of step j, once its record has landed and the tile has read its
+          // previous S
+          if (!ensure(j) || !tc_wait(&kv_full[j % NS], (j / NS) & 1, abort_f)) break;
+          if (j > 0 && !tc_wait(&s_read[C], (j - 1) & 1, abort_f)) break;
+          tc_fence_after();
+          issue_s(C, j);
+        }
+        if (j > 0) {
+          // P.V of step j-1, once the tile's weights are written
+          if (!tc_wait(&p_full[C], (j - 1) & 1, abort_f)) break;
+          tc_fence_after();
+          issue_pv(C, j - 1);
+          if (j == nsteps) tc_commit(&o_full[C]);
+          tc_commit(&kv_empty[(j - 1) % NS]);  // this tile's MMAs reading that stage are issued
+        }
+        pump();
+      }
+      // every MMA has completed and every copy has landed before the CTA exits
+      tc_commit(drain);
+      bool ok = false;
+      for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(drain, 0);
+      for (int j = copied > NS ? copied - NS : 0; j < copied; ++j) {
+        ok = false;
+        for (int tries = 0; tries < kWaitTries && !ok; ++tries)
+          ok = mbar_try_wait(&kv_full[j % NS], (j / NS) & 1);
+      }
+    }
+  } else {
+    // ======================= softmax rows, tile X =======================
     const uint32_t tO = tmem + X * 128;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t qa = smem_u32(sm + PL::q + X * PL::QB);
-    const uint32_t qla = smem_u32(sm + PL::q + (NT + X) * PL::QB);
-    const uint32_t pha = smem_u32(sm + PL::pw + X * 2 * PL::PB);
-    const uint32_t pla = pha + PL::PB;
-    char* p_hi = sm + PL::pw + X * 2 * PL::PB;
-    char* p_lo = p_hi + PL::PB;
-    constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
-    constexpr uint32_t id_o = tc_idesc_f16(128, D);
-    const bool issuer = r == 0;  // thread 0 of the tile
-    const int bar_id = 1 + X;
-    auto stage_of = [&](int j) { return sm + PL::stage + (j & 1) * R::bytes; };
-    auto issue_s = [&](int j) {  // S = Q K^T of step j into its S buffer (issuer)
-      const uint32_t kha = smem_u32(stage_of(j) + R::kh);
-      const uint32_t ts = tmem + PL::s_col(X, j & 1);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ko = (kk >> 2) * (kTcStep * 128) + (kk & 3) * 32;
-        const uint32_t qo = (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32;
-        tc_mma_f16(ts, sw128_desc(qa + qo), sw128_desc(kha + ko), id_s, kk > 0);
-        if constexpr (CH) tc_mma_f16(ts, sw128_desc(qla + qo), sw128_desc(kha + ko), id_s, 1);
-      }
-      tc_commit(&s_full[X]);
-    };
+    const uint32_t tS = tmem + PL::s_col(X) + lane_base;
+    const uint32_t tP = tS + 64;
     bool failed = false;
-    if (copier) pump();  // records 0 and 1
-    if (issuer && tc_wait(&kv_full[0], 0, abort_f)) {
-      tc_fence_after();
-      issue_s(0);
-    }
-    __syncwarp();
     float m = kNegInf, l = 0.f;
     int E = T::row_scales ? 100 : 14 - kTcSlack;
-    int next_s = 1;  // issuer: the next step whose S is not yet issued
     for (int j = 0; j < nsteps; ++j) {
-      const int b = j & 1;
       const char* st = stage_of(j);
-      bool ok = warp_wait(&s_full[X], j & 1, abort_f);
-      // the record's scales and mask landed with kv_full (already complete:
-      // S of this step was computed from its K tile)
-      ok = ok && warp_wait(&kv_full[b], (j >> 1) & 1, abort_f);
-      if (bar_or(bar_id, kTcRows, !ok)) {
+      // S of this step (its record's scales and mask landed before it)
+      if (!warp_wait(&s_full[X], j & 1, abort_f) ||
+          !warp_wait(&kv_full[j % NS], (j / NS) & 1, abort_f)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      // the next step's S goes into the other S buffer now if its record has
-      // landed (the softmax of step j-1, which read that buffer, is complete)
-      if (copier) pump();
-      if (issuer && next_s == j + 1 && j + 1 < nsteps &&
-          mbar_test_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
-        issue_s(j + 1);
-        next_s = j + 2;
-      }
-      __syncwarp();
       const int t0 = j * kTcStep;
       float z[kTcStep];
       {
-        const uint32_t ts = tmem + PL::s_col(X, b) + lane_base;
         float a[32];
-        tc_ld32(ts, a);
+        tc_ld32(tS, a);
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = a[i];
-        tc_ld32(ts + 32, a);
+        tc_ld32(tS + 32, a);
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
       }
+      tc_fence_before();
+      mbar_arrive(&s_read[X]);  // the next S may go into this buffer
       const float* ksb = reinterpret_cast<const float*>(st + R::ks);
       const float* vsb = reinterpret_cast<const float*>(st + R::vs);
       const uint32_t mk0 = reinterpret_cast<const uint32_t*>(st + R::mask)[0];
@@ -463,10 +502,9 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
       l = fmaf(l, alpha, (rsa + rsb) * pow2f(-E));
       m = mn;
       if (j > 0) {
-        // the previous step's P.V must be done before O is rescaled and the
-        // weight tiles are overwritten
-        const bool okp = warp_wait(&pv_done[X], (j - 1) & 1, abort_f);
-        if (bar_or(bar_id, kTcRows, !okp)) {
+        // the previous step's P.V must be done before O is rescaled and P
+        // is overwritten
+        if (!warp_wait(&pv_done[X], (j - 1) & 1, abort_f)) {
           failed = true;
           break;
         }
@@ -481,68 +519,35 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
             for (int i = 0; i < 32; ++i) o[i] *= f;
             tc_st32(tO + lane_base + 32 * c, o);
           }
-          tc_wait_st();
         }
       }
+      // the weights w = p' * s_V as fp16 hi + lo pairs into P (two halves of
+      // 32 tokens: 16 columns of the high part, 16 of the low part each)
 #pragma unroll
-      for (int c = 0; c < kTcStep / 8; ++c) {
-        uint32_t hv[4], lv[4];
-        float vv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-        if constexpr (T::row_scales) {
-          const float4 v0 = *reinterpret_cast<const float4*>(vsb + 8 * c);
-          const float4 v1 = *reinterpret_cast<const float4*>(vsb + 8 * c + 4);
-          vv[0] = v0.x, vv[1] = v0.y, vv[2] = v0.z, vv[3] = v0.w;
-          vv[4] = v1.x, vv[5] = v1.y, vv[6] = v1.z, vv[7] = v1.w;
-        }
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t hv[16], lv[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float w0 = z[8 * c + 2 * e], w1 = z[8 * c + 2 * e + 1];
+        for (int c = 0; c < 16; ++c) {
+          const int t = 32 * hf + 2 * c;
+          float w0 = z[t], w1 = z[t + 1];
           // masked tokens (absent, past the end, or causally later) have p' = 0;
           // an absent token's V scale is 0 too
-          if constexpr (T::row_scales)
-            f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(vv[2 * e], vv[2 * e + 1])), w0, w1);
-          tc_split2(w0, w1, hv[e], lv[e]);
-        }
-        const uint32_t o = sw128_offset(r, 8 * c, kTcRows);
-        *reinterpret_cast<uint4*>(p_hi + o) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4*>(p_lo + o) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      bar_or(bar_id, kTcRows, false);  // the tile's weights are written, S is read
-      if (issuer) {
-        tc_fence_after();
-        const uint32_t vta = smem_u32(st + R::vt);
-#pragma unroll
-        for (int kk = 0; kk < kTcStep / 16; ++kk)
-          tc_mma_f16(tO, sw128_desc(pha + kk * 32), sw128_desc(vta + kk * 32), id_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kTcStep / 16; ++kk)
-          tc_mma_f16(tO, sw128_desc(pla + kk * 32), sw128_desc(vta + kk * 32), id_o, 1u);
-        tc_commit(&kv_empty[b]);
-        tc_commit(&pv_done[X]);
-        if (j + 1 == nsteps) tc_commit(&o_full[X]);
-        if (copier) pump();
-        if (next_s == j + 1 && j + 1 < nsteps) {
-          // its record had not landed earlier: wait for it now (issuing its
-          // copy first if the stage only just became free)
-          if ((!copier || ensure(j + 1)) &&
-              tc_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_f)) {
-            tc_fence_after();
-            issue_s(j + 1);
+          if constexpr (T::row_scales) {
+            const float2 v2 = *reinterpret_cast<const float2*>(vsb + t);
+            f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(v2.x, v2.y)), w0, w1);
           }
-          next_s = j + 2;
+          tc_split2(w0, w1, hv[c], lv[c]);
         }
+        tc_st16(tP + 16 * hf, hv);
+        tc_st16(tP + 32 + 16 * hf, lv);
       }
-      __syncwarp();
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[X]);
     }
     if (!failed) {
       // ---- normalised output rows once the tile's last P.V is done
-      const bool ok = warp_wait(&o_full[X], 0, abort_f);
-      if (bar_or(bar_id, kTcRows, !ok)) {
-        failed = true;
-      } else {
+      if (warp_wait(&o_full[X], 0, abort_f)) {
         tc_fence_after();
         const float f = l > 0.f ? pow2f(-E) / l : 0.f;
         const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
@@ -567,21 +572,6 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
             }
           }
         }
-      }
-    }
-    if (issuer) {
-      // every MMA this thread issued has completed before TMEM is freed
-      tc_commit(&drain[X]);
-      bool ok = false;
-      for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(&drain[X], 0);
-    }
-    if (copier) {
-      // every record copy issued has landed before the CTA exits (all of them
-      // were consumed unless a wait gave up)
-      for (int j = copied >= 2 ? copied - 2 : 0; j < copied; ++j) {
-        bool ok = false;
-        for (int tries = 0; tries < kWaitTries && !ok; ++tries)
-          ok = mbar_try_wait(&kv_full[j & 1], (j >> 1) & 1);
       }
     }
   }
