@@ -89,9 +89,16 @@ cudaError_t run_ws(const StageParams& sp, const PrefillWsParams& ap, int64_t nti
   if (e != cudaSuccess) return e;
   PrefillWsParams a = ap;
   const int64_t ngroups = (ntiles + NT - 1) / NT;
-  const int64_t grid = ngroups * a.S * a.pool.Hkv;
-  if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int64_t items = ngroups * a.S * a.pool.Hkv;
+  if (items < 1 || items > 0x7fffffffLL) return cudaErrorInvalidValue;
   a.ngroups = static_cast<int>(ngroups);
+  // persistent: one CTA per SM (its shared memory allows no more), each
+  // taking every grid-th item
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 152;
+  const int64_t grid = items < sms ? items : sms;
   e = allow_big_smem<kvq_prefill_ws_kernel<FMT, D>>();
   if (e != cudaSuccess) return e;
   kvq_prefill_ws_kernel<FMT, D><<<static_cast<unsigned>(grid), PL::threads, PL::request, st>>>(a);

@@ -183,9 +183,9 @@ struct WsPlan {
   static constexpr int stage = NT * QB * (CH ? 2 : 1);     // [kWsStages][R::bytes]
   static constexpr int misc = stage + kWsStages * R::bytes;
   // misc: int abort; uint64 kv_full[S], kv_empty[S], s_full[NT], s_read[NT],
-  // p_full[NT], pv_done[NT], o_full[NT], drain; uint32 tslot
+  // p_full[NT], pv_done[NT], o_full[NT], q_full[NT], drain; uint32 tslot
   static constexpr int abort = misc, bars = misc + 8;
-  static constexpr int nbars = 2 * kWsStages + 5 * NT + 1;
+  static constexpr int nbars = 2 * kWsStages + 6 * NT + 1;
   static constexpr int tslot = bars + 8 * nbars;
   static constexpr int request = tslot + 16 + 1024;        // + alignment slack
   // the softmax warps plus one control warp per tile (its lane 0 issues that
@@ -197,6 +197,38 @@ struct WsPlan {
   static constexpr int cols = NT == 2 ? 512 : 256;
   static constexpr int s_col(int x) { return NT == 2 ? 256 + 128 * x : 128; }
 };
+
+// One work item of the attention pass: NT tiles of 128 Q rows of one
+// (sequence, kv head).  Items are numbered heaviest (longest causal range)
+// first; a CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+struct WsItem {
+  int seq, h, qbase, nq, ctx, rows_total, row0, kv_end, nsteps;
+  bool bad_ctx;
+};
+
+template <int NT>
+__device__ __forceinline__ WsItem ws_item(const PrefillWsParams& p, int i) {
+  const int per = p.S * p.pool.Hkv;
+  WsItem it;
+  const int grp = p.ngroups - 1 - i / per;
+  it.seq = (i % per) % p.S;
+  it.h = (i % per) / p.S;
+  it.qbase = p.q_start[it.seq];
+  it.nq = p.q_start[it.seq + 1] - it.qbase;
+  int ctx = p.lens[it.seq];
+  it.bad_ctx = ctx > p.max_ctx || ctx < it.nq;
+  it.ctx = min(ctx, p.max_ctx);
+  it.rows_total = it.nq * p.G;
+  it.row0 = grp * NT * kTcRows;
+  if (it.row0 >= it.rows_total) {
+    it.kv_end = it.nsteps = -1;  // nothing in this item
+    return it;
+  }
+  const int last = min(it.rows_total, it.row0 + NT * kTcRows) - 1;
+  it.kv_end = max(0, min(it.ctx, it.ctx - it.nq + last / p.G + 1));
+  it.nsteps = (it.kv_end + kTcStep - 1) / kTcStep;
+  return it;
+}
 
 template <int FMT, int D>
 __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::channel>::threads, 1)
@@ -214,54 +246,24 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
   char* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PoolView& pool = p.pool;
-  // heaviest tile groups (longest causal ranges) first
-  const int per = p.S * pool.Hkv;
-  const int grp = p.ngroups - 1 - static_cast<int>(blockIdx.x / per);
-  const int seq = static_cast<int>(blockIdx.x % per) % p.S;
-  const int h = static_cast<int>(blockIdx.x % per) / p.S;
-
-  const int qbase = p.q_start[seq];
-  const int nq = p.q_start[seq + 1] - qbase;
-  int ctx = p.lens[seq];
-  if (ctx > p.max_ctx || ctx < nq) {
-    if (grp == 0 && h == 0 && tid == 0) set_error(pool.err, ERR_RANGE);
-    ctx = min(ctx, p.max_ctx);
-  }
-  const int rows_total = nq * p.G;
-  const int row0 = grp * NT * kTcRows;
-  if (row0 >= rows_total) return;  // CTA-uniform
-  const int last = min(rows_total, row0 + NT * kTcRows) - 1;
-  const int kv_end = max(0, min(ctx, ctx - nq + last / p.G + 1));
-  const int nsteps = (kv_end + kTcStep - 1) / kTcStep;
-
-  const bool is_sm = tid < NT * kTcRows;
-  const int X = is_sm ? warp >> 2 : 0;
-  const int r = (warp & 3) * 32 + lane;
-  const int rr = row0 + X * kTcRows + r;
-  const bool row_ok = is_sm && rr < rows_total;
-  const int lim = row_ok ? max(0, ctx - nq + rr / p.G + 1) : 0;
-  const int64_t orow = row_ok ? (int64_t)(qbase + rr / p.G) * p.Hq + h * p.G + rr % p.G : -1;
-  if (nsteps == 0) {  // nothing to attend: zeros (CTA-uniform)
-    if (row_ok)
-      for (int d = 0; d < D; ++d) p.out[orow * D + d] = 0.f;
-    return;
-  }
+  const int n_items = p.ngroups * p.S * pool.Hkv;
 
   volatile int* abort_f = reinterpret_cast<volatile int*>(sm + PL::abort);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL::bars);
   uint64_t* kv_full = bars;                // [NS]: the step's record landed
-  uint64_t* kv_empty = bars + NS;          // [NS]: the MMAs of the step in that stage done
+  uint64_t* kv_empty = bars + NS;          // [NS]: every tile's MMAs of the step in that stage done
   uint64_t* s_full = bars + 2 * NS;        // [NT]: S of the tile's current step
   uint64_t* s_read = s_full + NT;          // [NT]: the tile's 128 rows have read S
   uint64_t* p_full = s_read + NT;          // [NT]: the tile's 128 rows have written P
   uint64_t* pv_done = p_full + NT;         // [NT]: the tile's last issued P.V done
-  uint64_t* o_full = pv_done + NT;         // [NT]: the tile's final P.V done
-  uint64_t* drain = o_full + NT;           // clean-up
+  uint64_t* o_full = pv_done + NT;         // [NT]: the tile's final P.V of an item done
+  uint64_t* q_full = o_full + NT;          // [NT]: the tile's Q rows of an item written
+  uint64_t* drain = q_full + NT;           // clean-up
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PL::tslot);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], NT);  // every tile's MMAs of the step done
+      mbar_init(&kv_empty[i], NT);
     }
     for (int x = 0; x < NT; ++x) {
       mbar_init(&s_full[x], 1);
@@ -269,93 +271,70 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
       mbar_init(&p_full[x], kTcRows);
       mbar_init(&pv_done[x], 1);
       mbar_init(&o_full[x], 1);
+      mbar_init(&q_full[x], kTcRows);
     }
     mbar_init(drain, NT);
     *abort_f = 0;
     fence_barrier_init();
   }
   if (warp == 0) tc_alloc(tslot, PL::cols);
-
-  // ---- softmax threads: their own Q row into the tile (K-major, swizzled)
-  float csc = p.sm_scale_log2;
-  if (is_sm) {
-    const __half* src = row_ok ? p.q + orow * D : nullptr;
-    char* qx = sm + PL::q + X * PL::QB;
-    if constexpr (!CH) {
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = src ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = v;
-      }
-    } else {
-      // fold the K channel scale into the row, scale it by 2^eq so that its
-      // largest magnitude lies in [2^13, 2^14), split into fp16 hi + lo
-      const float* ksc = pool.chan_scales + (int64_t)h * D;
-      char* ql = sm + PL::q + (NT + X) * PL::QB;
-      float amax = 0.f;
-      if (src)
-        for (int d = 0; d < D; ++d) amax = fmaxf(amax, fabsf(__half2float(src[d]) * ksc[d]));
-      const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
-      const float up = ldexpf(1.f, eq);
-      csc = ldexpf(csc, -eq);
-      for (int c = 0; c < D / 8; ++c) {
-        uint4 hv4 = make_uint4(0, 0, 0, 0), lv4 = make_uint4(0, 0, 0, 0);
-        if (src) {
-          uint32_t* ho = reinterpret_cast<uint32_t*>(&hv4);
-          uint32_t* lo = reinterpret_cast<uint32_t*>(&lv4);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int d = 8 * c + 2 * e;
-            split_h2(__half2float(src[d]) * ksc[d] * up, __half2float(src[d + 1]) * ksc[d + 1] * up,
-                     ho[e], lo[e]);
-          }
-        }
-        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = hv4;
-        *reinterpret_cast<uint4*>(ql + sw128_offset(r, 8 * c, kTcRows)) = lv4;
-      }
-    }
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  auto stage_of = [&](int j) { return sm + PL::stage + (j % NS) * R::bytes; };
+  auto stage_of = [&](int g) { return sm + PL::stage + (g % NS) * R::bytes; };
+  const bool is_sm = tid < NT * kTcRows;
 
   if (!is_sm) {
-    // ======================= control: tile C's MMAs (tile 0's: the copies too) =======================
+    // ============ control: tile C's MMAs (tile 0's thread: the record copies too) ============
     const int C = warp - 4 * NT;
     if (lane == 0) {
-      const char* recs = p.ws + ((int64_t)seq * p.max_steps * pool.Hkv + h) * R::bytes;
-      int copied = 0;
-      auto copy_rec = [&](int j) {
-        mbar_arrive_expect_tx(&kv_full[j % NS], R::copy);
-        bulk_g2s(stage_of(j), recs + (int64_t)j * pool.Hkv * R::bytes, R::copy, &kv_full[j % NS]);
-        copied = j + 1;
+      // the copy cursor walks (item, step) ahead of the MMAs, over the global
+      // step sequence of this CTA
+      int c_item = blockIdx.x, c_j = 0, copied = 0;
+      WsItem c_it = c_item < n_items ? ws_item<NT>(p, c_item) : WsItem{};
+      auto c_advance_item = [&]() {  // to the cursor's next item with steps
+        while (c_item < n_items && c_j >= c_it.nsteps) {
+          c_item += gridDim.x;
+          c_j = 0;
+          if (c_item < n_items) c_it = ws_item<NT>(p, c_item);
+        }
       };
+      c_advance_item();
+      auto copy_next = [&]() {  // the record of the cursor's step into stage `copied`
+        const char* rec = p.ws + (((int64_t)c_it.seq * p.max_steps + c_j) * pool.Hkv + c_it.h) * R::bytes;
+        mbar_arrive_expect_tx(&kv_full[copied % NS], R::copy);
+        bulk_g2s(stage_of(copied), rec, R::copy, &kv_full[copied % NS]);
+        ++copied;
+        ++c_j;
+        c_advance_item();
+      };
+      auto has_next = [&]() { return c_item < n_items; };
       // issue every copy whose stage is free (non-blocking; tile 0's thread)
       auto pump = [&]() {
-        while (C == 0 && copied < nsteps &&
+        while (C == 0 && has_next() &&
                (copied < NS || mbar_test_wait(&kv_empty[copied % NS], ((copied / NS) - 1) & 1)))
-          copy_rec(copied);
+          copy_next();
       };
-      // make sure record j's copy is issued, waiting for its stage if needed
-      // (tile 0's thread; the others only wait for the record to land)
-      auto ensure = [&](int j) -> bool {
-        while (C == 0 && copied <= j) {
+      // make sure the record of global step g is being copied, waiting for
+      // its stage if needed (tile 0's thread; the others wait for it to land)
+      auto ensure = [&](int g) -> bool {
+        while (C == 0 && copied <= g && has_next()) {
           if (copied >= NS && !tc_wait(&kv_empty[copied % NS], ((copied / NS) - 1) & 1, abort_f))
             return false;
-          copy_rec(copied);
+          copy_next();
         }
         return true;
       };
       constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
       constexpr uint32_t id_o = tc_idesc_f16(128, D);
-      auto issue_s = [&](int x, int j) {  // S_x = Q_x K^T of step j
-        const uint32_t qa = smem_u32(sm + PL::q + x * PL::QB);
-        const uint32_t qla = smem_u32(sm + PL::q + (NT + x) * PL::QB);
-        const uint32_t kha = smem_u32(stage_of(j) + R::kh);
-        const uint32_t ts = tmem + PL::s_col(x);
+      const uint32_t qa = smem_u32(sm + PL::q + C * PL::QB);
+      const uint32_t qla = smem_u32(sm + PL::q + (NT + C) * PL::QB);
+      const uint32_t ts = tmem + PL::s_col(C);
+      const uint32_t tp = ts + 64;
+      const uint32_t to = tmem + C * 128;
+      auto issue_s = [&](int g) {  // S = Q K^T of global step g
+        const uint32_t kha = smem_u32(stage_of(g) + R::kh);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * (kTcStep * 128) + (kk & 3) * 32;
@@ -363,194 +342,292 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
           tc_mma_f16(ts, sw128_desc(qa + qo), sw128_desc(kha + ko), id_s, kk > 0);
           if constexpr (CH) tc_mma_f16(ts, sw128_desc(qla + qo), sw128_desc(kha + ko), id_s, 1);
         }
-        tc_commit(&s_full[x]);
+        tc_commit(&s_full[C]);
       };
-      auto issue_pv = [&](int x, int j) {  // O_x += P_x V of step j (P in TMEM)
-        const uint32_t vta = smem_u32(stage_of(j) + R::vt);
-        const uint32_t tp = tmem + PL::s_col(x) + 64;
-        const uint32_t to = tmem + x * 128;
+      auto issue_pv = [&](int g, bool first) {  // O += P V of global step g (P in TMEM)
+        const uint32_t vta = smem_u32(stage_of(g) + R::vt);
 #pragma unroll
         for (int kk = 0; kk < kTcStep / 16; ++kk)
-          tc_mma_f16_ts(to, tp + 8 * kk, sw128_desc(vta + kk * 32), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(to, tp + 8 * kk, sw128_desc(vta + kk * 32), id_o, (!first || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kTcStep / 16; ++kk)
           tc_mma_f16_ts(to, tp + 32 + 8 * kk, sw128_desc(vta + kk * 32), id_o, 1u);
-        tc_commit(&pv_done[x]);
+        tc_commit(&pv_done[C]);
       };
       pump();
-      for (int j = 0; j <= nsteps && !*abort_f; ++j) {
-        if (j < nsteps) {
-          // S of step j, once its record has landed and the tile has read its
-          // previous S
-          if (!ensure(j) || !tc_wait(&kv_full[j % NS], (j / NS) & 1, abort_f)) break;
-          if (j > 0 && !tc_wait(&s_read[C], (j - 1) & 1, abort_f)) break;
-          tc_fence_after();
-          issue_s(C, j);
+      int gbase = 0, n_done = 0;  // global steps before the item, items with steps done
+      for (int item = blockIdx.x; item < n_items && !*abort_f; item += gridDim.x) {
+        const WsItem it = ws_item<NT>(p, item);
+        if (it.nsteps <= 0) continue;
+        // this item's Q rows are in shared memory
+        if (!tc_wait(&q_full[C], n_done & 1, abort_f)) break;
+        bool ok = true;
+        for (int j = 0; j <= it.nsteps && ok; ++j) {
+          const int g = gbase + j;
+          if (j < it.nsteps) {
+            // S of step j, once its record has landed and the tile has read
+            // its previous S
+            ok = ensure(g) && tc_wait(&kv_full[g % NS], (g / NS) & 1, abort_f) &&
+                 (g == 0 || tc_wait(&s_read[C], (g - 1) & 1, abort_f));
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(g);
+          }
+          if (j > 0) {
+            // P.V of step j-1, once the tile's weights are written
+            ok = tc_wait(&p_full[C], (g - 1) & 1, abort_f);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(g - 1, j == 1);
+            if (j == it.nsteps) tc_commit(&o_full[C]);
+            tc_commit(&kv_empty[(g - 1) % NS]);  // this tile's MMAs reading that stage are issued
+          }
+          pump();
         }
-        if (j > 0) {
-          // P.V of step j-1, once the tile's weights are written
-          if (!tc_wait(&p_full[C], (j - 1) & 1, abort_f)) break;
-          tc_fence_after();
-          issue_pv(C, j - 1);
-          if (j == nsteps) tc_commit(&o_full[C]);
-          tc_commit(&kv_empty[(j - 1) % NS]);  // this tile's MMAs reading that stage are issued
-        }
-        pump();
+        if (!ok) break;
+        gbase += it.nsteps;
+        ++n_done;
       }
       // every MMA has completed and every copy has landed before the CTA exits
       tc_commit(drain);
       bool ok = false;
       for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(drain, 0);
-      for (int j = copied > NS ? copied - NS : 0; j < copied; ++j) {
+      for (int g = copied > NS ? copied - NS : 0; g < copied; ++g) {
         ok = false;
         for (int tries = 0; tries < kWaitTries && !ok; ++tries)
-          ok = mbar_try_wait(&kv_full[j % NS], (j / NS) & 1);
+          ok = mbar_try_wait(&kv_full[g % NS], (g / NS) & 1);
       }
     }
   } else {
-    // ======================= softmax rows, tile X =======================
+    // ======================= softmax rows of tile X =======================
+    const int X = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t tO = tmem + X * 128;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + PL::s_col(X) + lane_base;
     const uint32_t tP = tS + 64;
+    char* qx = sm + PL::q + X * PL::QB;
+    char* ql = sm + PL::q + (NT + X) * PL::QB;
     bool failed = false;
-    float m = kNegInf, l = 0.f;
-    int E = T::row_scales ? 100 : 14 - kTcSlack;
-    for (int j = 0; j < nsteps; ++j) {
-      const char* st = stage_of(j);
-      // S of this step (its record's scales and mask landed before it)
-      if (!warp_wait(&s_full[X], j & 1, abort_f) ||
-          !warp_wait(&kv_full[j % NS], (j / NS) & 1, abort_f)) {
-        failed = true;
-        break;
+    int gbase = 0, n_done = 0;
+    // The next item with key steps, from `from` on; items without any write
+    // zeros for their rows here.
+    auto next_item = [&](int from, WsItem& it) -> int {
+      for (int i = from; i < n_items; i += gridDim.x) {
+        it = ws_item<NT>(p, i);
+        if (it.nsteps < 0) continue;  // no rows in this item
+        if (it.bad_ctx && it.row0 == 0 && it.h == 0 && tid == 0) set_error(pool.err, ERR_RANGE);
+        if (it.nsteps > 0) return i;
+        const int rr = it.row0 + X * kTcRows + r;
+        if (rr < it.rows_total) {
+          float* o = p.out + ((int64_t)(it.qbase + rr / p.G) * p.Hq + it.h * p.G + rr % p.G) * D;
+          for (int d = 0; d < D; ++d) o[d] = 0.f;
+        }
       }
-      tc_fence_after();
-      const int t0 = j * kTcStep;
-      float z[kTcStep];
-      {
-        float a[32];
-        tc_ld32(tS, a);
+      return n_items;
+    };
+    // This row of an item's Q into the tile (K-major, swizzled), then the
+    // tile's q_full arrival; returns the row's score scale (per-channel pools
+    // fold the K channel scale into the row and scale it by a power of two).
+    auto load_q = [&](const WsItem& it) -> float {
+      const int rr = it.row0 + X * kTcRows + r;
+      const __half* src =
+          rr < it.rows_total
+              ? p.q + ((int64_t)(it.qbase + rr / p.G) * p.Hq + it.h * p.G + rr % p.G) * D
+              : nullptr;
+      float csc = p.sm_scale_log2;
+      if constexpr (!CH) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = a[i];
-        tc_ld32(tS + 32, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
-      }
-      tc_fence_before();
-      mbar_arrive(&s_read[X]);  // the next S may go into this buffer
-      const float* ksb = reinterpret_cast<const float*>(st + R::ks);
-      const float* vsb = reinterpret_cast<const float*>(st + R::vs);
-      const uint32_t mk0 = reinterpret_cast<const uint32_t*>(st + R::mask)[0];
-      const uint32_t mk1 = reinterpret_cast<const uint32_t*>(st + R::mask)[1];
-      const int lr = lim - t0;  // tokens [0, lr) of this step are attended by this row
-      float mx = kNegInf;
-      if (lr >= kTcStep && (mk0 & mk1) == 0xffffffffu) {
-#pragma unroll
-        for (int t = 0; t < kTcStep; t += 4) {
-          float a0 = z[t], a1 = z[t + 1], a2 = z[t + 2], a3 = z[t + 3];
-          if constexpr (T::row_scales) {
-            const float4 k4 = *reinterpret_cast<const float4*>(ksb + t);
-            f2_unpack(f2_mul(f2_pack(a0, a1), f2_pack(k4.x, k4.y)), a0, a1);
-            f2_unpack(f2_mul(f2_pack(a2, a3), f2_pack(k4.z, k4.w)), a2, a3);
-          }
-          z[t] = a0;
-          z[t + 1] = a1;
-          z[t + 2] = a2;
-          z[t + 3] = a3;
-          mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = src ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = v;
         }
       } else {
+        // largest magnitude of the scaled row into [2^13, 2^14), fp16 hi + lo
+        const float* ksc = pool.chan_scales + (int64_t)it.h * D;
+        float amax = 0.f;
+        if (src)
+          for (int d = 0; d < D; ++d) amax = fmaxf(amax, fabsf(__half2float(src[d]) * ksc[d]));
+        const int eq = amax > 0.f ? 13 - exponent_of(amax) : 0;
+        const float up = ldexpf(1.f, eq);
+        csc = ldexpf(csc, -eq);
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 hv4 = make_uint4(0, 0, 0, 0), lv4 = make_uint4(0, 0, 0, 0);
+          if (src) {
+            uint32_t* ho = reinterpret_cast<uint32_t*>(&hv4);
+            uint32_t* lo = reinterpret_cast<uint32_t*>(&lv4);
 #pragma unroll
-        for (int t = 0; t < kTcStep; ++t) {
-          const bool okt = t < lr && (((t < 32 ? mk0 : mk1) >> (t & 31)) & 1u);
-          z[t] = okt ? (T::row_scales ? z[t] * ksb[t] : z[t]) : kNegInf;
-          mx = fmaxf(mx, z[t]);
+            for (int e = 0; e < 4; ++e) {
+              const int d = 8 * c + 2 * e;
+              split_h2(__half2float(src[d]) * ksc[d] * up, __half2float(src[d + 1]) * ksc[d + 1] * up,
+                       ho[e], lo[e]);
+            }
+          }
+          *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = hv4;
+          *reinterpret_cast<uint4*>(ql + sw128_offset(r, 8 * c, kTcRows)) = lv4;
         }
       }
-      // scores in log2 units are z * csc (csc > 0); the reference maximum m
-      // moves only when the step's maximum passes it by more than kTcSlack
-      const float mxz = mx == kNegInf ? kNegInf : mx * csc;
-      const float mn = (m == kNegInf || mxz > m + kTcSlack) ? mxz : m;
-      const float ms = mn == kNegInf ? 0.f : mn;
-      int dE = 0;
-      if constexpr (T::row_scales) {
-        const float* vm = reinterpret_cast<const float*>(st + R::vmax);
-        const float vmax = fmaxf(vm[0], vm[1]);
-        if (vmax > 0.f) {
-          const int En = min(E, 13 - kTcSlack - exponent_of(vmax));
-          dE = En - E;
-          E = En;
-        }
-      }
-      // p' = 2^(z csc - ms + E), the weight before the V scale
-      const float nbias = static_cast<float>(E) - ms;
-      uint64_t rs2 = f2_pack(0.f, 0.f);
-      {
-        const uint64_t c2 = f2_pack(csc, csc), b2 = f2_pack(nbias, nbias);
-#pragma unroll
-        for (int t = 0; t < kTcStep; t += 2) {
-          float a0, a1;
-          f2_unpack(f2_fma(f2_pack(z[t], z[t + 1]), c2, b2), a0, a1);
-          z[t] = fast_exp2(a0);  // 0 for masked tokens
-          z[t + 1] = fast_exp2(a1);
-          rs2 = f2_add(rs2, f2_pack(z[t], z[t + 1]));
-        }
-      }
-      float rsa, rsb;
-      f2_unpack(rs2, rsa, rsb);
-      const float alpha = fast_exp2(m - ms);
-      l = fmaf(l, alpha, (rsa + rsb) * pow2f(-E));
-      m = mn;
-      if (j > 0) {
-        // the previous step's P.V must be done before O is rescaled and P
-        // is overwritten
-        if (!warp_wait(&pv_done[X], (j - 1) & 1, abort_f)) {
+      fence_proxy_async_smem();
+      mbar_arrive(&q_full[X]);
+      return csc;
+    };
+    WsItem it;
+    int item = next_item(blockIdx.x, it);
+    float csc = item < n_items ? load_q(it) : 0.f;
+    for (; item < n_items && !failed;) {
+      const int rr = it.row0 + X * kTcRows + r;
+      const bool row_ok = rr < it.rows_total;
+      const int lim = row_ok ? max(0, it.ctx - it.nq + rr / p.G + 1) : 0;
+      const int64_t orow =
+          row_ok ? (int64_t)(it.qbase + rr / p.G) * p.Hq + it.h * p.G + rr % p.G : -1;
+      float m = kNegInf, l = 0.f;
+      int E = T::row_scales ? 100 : 14 - kTcSlack;
+      for (int j = 0; j < it.nsteps; ++j) {
+        const int g = gbase + j;
+        const char* st = stage_of(g);
+        // S of this step (its record's scales and mask landed before it)
+        if (!warp_wait(&s_full[X], g & 1, abort_f) ||
+            !warp_wait(&kv_full[g % NS], (g / NS) & 1, abort_f)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        const float f = alpha * pow2f(dE);
-        if (__any_sync(0xffffffffu, f != 1.f)) {
+        const int t0 = j * kTcStep;
+        float z[kTcStep];
+        {
+          float a[32];
+          tc_ld32(tS, a);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tc_ld32(tO + lane_base + 32 * c, o);
+          for (int i = 0; i < 32; ++i) z[i] = a[i];
+          tc_ld32(tS + 32, a);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= f;
-            tc_st32(tO + lane_base + 32 * c, o);
+          for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
+        }
+        tc_fence_before();
+        mbar_arrive(&s_read[X]);  // the next S may go into this buffer
+        const float* ksb = reinterpret_cast<const float*>(st + R::ks);
+        const float* vsb = reinterpret_cast<const float*>(st + R::vs);
+        const uint32_t mk0 = reinterpret_cast<const uint32_t*>(st + R::mask)[0];
+        const uint32_t mk1 = reinterpret_cast<const uint32_t*>(st + R::mask)[1];
+        const int lr = lim - t0;  // tokens [0, lr) of this step are attended by this row
+        float mx = kNegInf;
+        if (lr >= kTcStep && (mk0 & mk1) == 0xffffffffu) {
+#pragma unroll
+          for (int t = 0; t < kTcStep; t += 4) {
+            float a0 = z[t], a1 = z[t + 1], a2 = z[t + 2], a3 = z[t + 3];
+            if constexpr (T::row_scales) {
+              const float4 k4 = *reinterpret_cast<const float4*>(ksb + t);
+              f2_unpack(f2_mul(f2_pack(a0, a1), f2_pack(k4.x, k4.y)), a0, a1);
+              f2_unpack(f2_mul(f2_pack(a2, a3), f2_pack(k4.z, k4.w)), a2, a3);
+            }
+            z[t] = a0;
+            z[t + 1] = a1;
+            z[t + 2] = a2;
+            z[t + 3] = a3;
+            mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < kTcStep; ++t) {
+            const bool okt = t < lr && (((t < 32 ? mk0 : mk1) >> (t & 31)) & 1u);
+            z[t] = okt ? (T::row_scales ? z[t] * ksb[t] : z[t]) : kNegInf;
+            mx = fmaxf(mx, z[t]);
           }
         }
-      }
-      // the weights w = p' * s_V as fp16 hi + lo pairs into P (two halves of
-      // 32 tokens: 16 columns of the high part, 16 of the low part each)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t hv[16], lv[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int t = 32 * hf + 2 * c;
-          float w0 = z[t], w1 = z[t + 1];
-          // masked tokens (absent, past the end, or causally later) have p' = 0;
-          // an absent token's V scale is 0 too
-          if constexpr (T::row_scales) {
-            const float2 v2 = *reinterpret_cast<const float2*>(vsb + t);
-            f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(v2.x, v2.y)), w0, w1);
+        // scores in log2 units are z * csc (csc > 0); the reference maximum m
+        // moves only when the step's maximum passes it by more than kTcSlack
+        const float mxz = mx == kNegInf ? kNegInf : mx * csc;
+        const float mn = (m == kNegInf || mxz > m + kTcSlack) ? mxz : m;
+        const float ms = mn == kNegInf ? 0.f : mn;
+        int dE = 0;
+        if constexpr (T::row_scales) {
+          const float* vm = reinterpret_cast<const float*>(st + R::vmax);
+          const float vmax = fmaxf(vm[0], vm[1]);
+          if (vmax > 0.f) {
+            const int En = min(E, 13 - kTcSlack - exponent_of(vmax));
+            dE = En - E;
+            E = En;
           }
-          tc_split2(w0, w1, hv[c], lv[c]);
         }
-        tc_st16(tP + 16 * hf, hv);
-        tc_st16(tP + 32 + 16 * hf, lv);
+        // p' = 2^(z csc - ms + E), the weight before the V scale
+        const float nbias = static_cast<float>(E) - ms;
+        uint64_t rs2 = f2_pack(0.f, 0.f);
+        {
+          const uint64_t c2 = f2_pack(csc, csc), b2 = f2_pack(nbias, nbias);
+#pragma unroll
+          for (int t = 0; t < kTcStep; t += 2) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(z[t], z[t + 1]), c2, b2), a0, a1);
+            z[t] = fast_exp2(a0);  // 0 for masked tokens
+            z[t + 1] = fast_exp2(a1);
+            rs2 = f2_add(rs2, f2_pack(z[t], z[t + 1]));
+          }
+        }
+        float rsa, rsb;
+        f2_unpack(rs2, rsa, rsb);
+        const float alpha = fast_exp2(m - ms);
+        l = fmaf(l, alpha, (rsa + rsb) * pow2f(-E));
+        m = mn;
+        if (g > 0) {
+          // the previous P.V must be done before P is overwritten (and, within
+          // an item, before O is rescaled)
+          if (!warp_wait(&pv_done[X], (g - 1) & 1, abort_f)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const float f = alpha * pow2f(dE);
+          if (j > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tc_ld32(tO + lane_base + 32 * c, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= f;
+              tc_st32(tO + lane_base + 32 * c, o);
+            }
+          }
+        }
+        // the weights w = p' * s_V as fp16 hi + lo pairs into P (two halves of
+        // 32 tokens: 16 columns of the high part, 16 of the low part each)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t hv[16], lv[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int t = 32 * hf + 2 * c;
+            float w0 = z[t], w1 = z[t + 1];
+            // masked tokens (absent, past the end, or causally later) have
+            // p' = 0; an absent token's V scale is 0 too
+            if constexpr (T::row_scales) {
+              const float2 v2 = *reinterpret_cast<const float2*>(vsb + t);
+              f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(v2.x, v2.y)), w0, w1);
+            }
+            tc_split2(w0, w1, hv[c], lv[c]);
+          }
+          tc_st16(tP + 16 * hf, hv);
+          tc_st16(tP + 32 + 16 * hf, lv);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[X]);
       }
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[X]);
-    }
-    if (!failed) {
-      // ---- normalised output rows once the tile's last P.V is done
-      if (warp_wait(&o_full[X], 0, abort_f)) {
-        tc_fence_after();
+      if (failed) break;
+      // ---- the next item's Q now (the S products of this item, the last
+      // readers of the tile, are done: this thread has read their results),
+      // so that its first S overlaps this item's epilogue
+      WsItem nit;
+      const int nitem = next_item(item + gridDim.x, nit);
+      const float ncsc = nitem < n_items ? load_q(nit) : 0.f;
+      // ---- normalised output rows once the item's last P.V is done
+      if (!warp_wait(&o_full[X], n_done & 1, abort_f)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      {
         const float f = l > 0.f ? pow2f(-E) / l : 0.f;
-        const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
+        const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + it.h) * D : nullptr;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -573,6 +650,14 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
           }
         }
       }
+      // the next item's first P.V overwrites O: it is issued only after this
+      // tile's next p_full, which comes after these reads
+      tc_fence_before();
+      gbase += it.nsteps;
+      ++n_done;
+      item = nitem;
+      it = nit;
+      csc = ncsc;
     }
   }
   tc_fence_before();
