@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
             z[t + 1] = a1;
             z[t + 2] = a2;
             z[t + 3] = a3;
-            mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+            mx = fmax3(fmax3(mx, a0, a1), a2, a3);
           }
         } else {
 #pragma unroll
@@ -594,16 +594,18 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t hv[16], lv[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < 16; c += 2) {
             const int t = 32 * hf + 2 * c;
-            float w0 = z[t], w1 = z[t + 1];
+            float w0 = z[t], w1 = z[t + 1], w2 = z[t + 2], w3 = z[t + 3];
             // masked tokens (absent, past the end, or causally later) have
             // p' = 0; an absent token's V scale is 0 too
             if constexpr (T::row_scales) {
-              const float2 v2 = *reinterpret_cast<const float2*>(vsb + t);
-              f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(v2.x, v2.y)), w0, w1);
+              const float4 v4 = *reinterpret_cast<const float4*>(vsb + t);
+              f2_unpack(f2_mul(f2_pack(w0, w1), f2_pack(v4.x, v4.y)), w0, w1);
+              f2_unpack(f2_mul(f2_pack(w2, w3), f2_pack(v4.z, v4.w)), w2, w3);
             }
             tc_split2(w0, w1, hv[c], lv[c]);
+            tc_split2(w2, w3, hv[c + 1], lv[c + 1]);
           }
           tc_st16(tP + 16 * hf, hv);
           tc_st16(tP + 32 + 16 * hf, lv);

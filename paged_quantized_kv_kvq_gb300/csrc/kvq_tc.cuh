@@ -145,6 +145,13 @@ __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Packed fp32 pairs (one instruction for two lanes of arithmetic).
 __device__ __forceinline__ uint64_t f2_pack(float a, float b) {
   uint64_t r;

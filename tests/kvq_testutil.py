@@ -11,6 +11,11 @@ import paged_quantized_kv_kvq_gb300 as kvq
 from paged_quantized_kv_kvq_gb300 import synth
 
 TOL = 1e-3  # max abs error of attention outputs vs the float64 oracle
+# Prefill outputs whose softmax weights reach P.V with fp32-level precision
+# (an fp16 high plus an fp16 low part) stay well inside this on the prefill
+# precision case; fp16 weights alone miss it by several times (the CPU check
+# of the case shows both).
+PREC_TOL = 2e-4
 
 
 def layer_tokens(w: synth.Workload, layer: int, seqs=None):

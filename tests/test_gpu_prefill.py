@@ -9,7 +9,7 @@ import torch
 
 import paged_quantized_kv_kvq_gb300 as kvq
 from paged_quantized_kv_kvq_gb300 import synth
-from kvq_testutil import TOL, gpu_pool, layer_tokens, oracle_layer
+from kvq_testutil import PREC_TOL, TOL, gpu_pool, layer_tokens, oracle_layer
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -83,6 +83,23 @@ def test_prefill_parity(fmt, group, api):
     pool, got, exp, _ = _case(fmt, group, api=api)
     assert pool.error() == kvq.KVQ_OK
     np.testing.assert_allclose(got, exp, rtol=0, atol=TOL)
+    pool.close()
+
+
+@pytest.mark.parametrize("api", APIS)
+@pytest.mark.parametrize("fmt,group", [(kvq.KVQ_INT8_PER_GROUP, 128), (kvq.KVQ_FP16, 0),
+                                       (kvq.KVQ_INT8_PER_CHANNEL, 0), (kvq.KVQ_INT4_PER_GROUP, 32)])
+def test_prefill_weights_keep_fp32_precision(fmt, group, api):
+    """The softmax weights enter P.V as an fp16 high part plus an fp16 low
+    part (the two-pass kernel stores the low part negated and negates the
+    operand back in the MMA).  Both parts must arrive with the right sign:
+    with the high part alone, or the low part subtracted, the weights carry
+    an fp16 rounding error and the outputs miss the float64 oracle by
+    several times PREC_TOL (shown on the CPU for this very case)."""
+    pool, got, exp, _ = _case(fmt, group, S=2, L=600, nq=(600, 200), api=api)
+    err = float(np.abs(got - exp).max())
+    print("max abs error vs oracle: %.3g" % err)
+    assert err <= PREC_TOL
     pool.close()
 
 
