@@ -170,6 +170,18 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
+// The same bound without the spinning phase, for a thread off the critical
+// path (its polls would take issue slots from the warps sharing its
+// scheduler): suspending tries only.
+__device__ __forceinline__ bool tc_wait_suspend(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (int tries = 0; tries < kWaitTries; ++tries) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
 // Named barrier ID over `count` threads with an OR of `pred` (the id is an
 // immediate: a barrier id held in a register makes the compiler reserve all
 // sixteen barriers and lowers the register budget of the kernel).

@@ -24,9 +24,10 @@
 // The attention pass: a CTA takes one (sequence, kv head) and two tiles of
 // 128 Q rows (one tile for per-channel pools, whose Q has a low part too).
 // Its eight softmax warps own the rows (one row per thread, one TMEM lane
-// each); one control thread bulk-copies the step records into four shared
-// memory stages and issues every tcgen05.mma.  Per tile, tensor memory holds
-// the output accumulator O, the step's scores S and the step's weights P:
+// each); a copier thread bulk-copies the step records into four shared
+// memory stages the moment each is free, and one control thread per tile
+// issues that tile's tcgen05.mma.  Per tile, tensor memory holds the output
+// accumulator O, the step's scores S and the step's weights P:
 //   * the control thread issues S = Q.K^T (M 128, N 64, K D, A and B from
 //     shared memory) for every tile once the step's record has landed and the
 //     tile has read its previous S;
@@ -193,9 +194,9 @@ struct WsPlan {
   static constexpr int OSCR_WARP = 32 * 16 * 4;
   static constexpr int request = oscr + 4 * NT * OSCR_WARP + 1024;  // + alignment slack
   static_assert(tslot + 16 <= oscr, "mbarriers overlap the output blocks");
-  // the softmax warps plus one control warp per tile (its lane 0 issues that
-  // tile's MMAs; tile 0's also issues the record copies)
-  static constexpr int threads = kTcRows * NT + 32 * NT;
+  // the softmax warps, one control warp per tile (its lane 0 issues that
+  // tile's MMAs) and a copier warp (its lane 0 issues the record copies)
+  static constexpr int threads = kTcRows * NT + 32 * NT + 32;
   // TMEM: per tile x, O at 128x (D columns), S at 256 + 128x (64), P at S + 64
   // (32 columns of fp16 pairs for the high part, 32 for the low part); one
   // tile: O 0, S 128, P 192
@@ -290,47 +291,38 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
   auto stage_of = [&](int g) { return sm + PL::stage + (g % NS) * R::bytes; };
   const bool is_sm = tid < NT * kTcRows;
 
-  if (!is_sm) {
-    // ============ control: tile C's MMAs (tile 0's thread: the record copies too) ============
+  if (!is_sm && warp == 5 * NT) {
+    // ============ copier: the step records into the stages, as soon as each
+    // stage is free, over the global step sequence of this CTA ============
+    if (lane == 0) {
+      int copied = 0;
+      for (int item = blockIdx.x; item < n_items && !*abort_f; item += gridDim.x) {
+        const WsItem it = ws_item<NT>(p, item);
+        bool ok = true;
+        for (int j = 0; j < it.nsteps; ++j) {
+          if (copied >= NS &&
+              !tc_wait_suspend(&kv_empty[copied % NS], ((copied / NS) - 1) & 1, abort_f)) {
+            ok = false;
+            break;
+          }
+          const char* rec = p.ws + (((int64_t)it.seq * p.max_steps + j) * pool.Hkv + it.h) * R::bytes;
+          mbar_arrive_expect_tx(&kv_full[copied % NS], R::copy);
+          bulk_g2s(stage_of(copied), rec, R::copy, &kv_full[copied % NS]);
+          ++copied;
+        }
+        if (!ok) break;
+      }
+      // every copy has landed before the CTA exits
+      for (int g = copied > NS ? copied - NS : 0; g < copied; ++g) {
+        bool ok = false;
+        for (int tries = 0; tries < kWaitTries && !ok; ++tries)
+          ok = mbar_try_wait(&kv_full[g % NS], (g / NS) & 1);
+      }
+    }
+  } else if (!is_sm) {
+    // ============ control: tile C's MMAs ============
     const int C = warp - 4 * NT;
     if (lane == 0) {
-      // the copy cursor walks (item, step) ahead of the MMAs, over the global
-      // step sequence of this CTA
-      int c_item = blockIdx.x, c_j = 0, copied = 0;
-      WsItem c_it = c_item < n_items ? ws_item<NT>(p, c_item) : WsItem{};
-      auto c_advance_item = [&]() {  // to the cursor's next item with steps
-        while (c_item < n_items && c_j >= c_it.nsteps) {
-          c_item += gridDim.x;
-          c_j = 0;
-          if (c_item < n_items) c_it = ws_item<NT>(p, c_item);
-        }
-      };
-      c_advance_item();
-      auto copy_next = [&]() {  // the record of the cursor's step into stage `copied`
-        const char* rec = p.ws + (((int64_t)c_it.seq * p.max_steps + c_j) * pool.Hkv + c_it.h) * R::bytes;
-        mbar_arrive_expect_tx(&kv_full[copied % NS], R::copy);
-        bulk_g2s(stage_of(copied), rec, R::copy, &kv_full[copied % NS]);
-        ++copied;
-        ++c_j;
-        c_advance_item();
-      };
-      auto has_next = [&]() { return c_item < n_items; };
-      // issue every copy whose stage is free (non-blocking; tile 0's thread)
-      auto pump = [&]() {
-        while (C == 0 && has_next() &&
-               (copied < NS || mbar_test_wait(&kv_empty[copied % NS], ((copied / NS) - 1) & 1)))
-          copy_next();
-      };
-      // make sure the record of global step g is being copied, waiting for
-      // its stage if needed (tile 0's thread; the others wait for it to land)
-      auto ensure = [&](int g) -> bool {
-        while (C == 0 && copied <= g && has_next()) {
-          if (copied >= NS && !tc_wait(&kv_empty[copied % NS], ((copied / NS) - 1) & 1, abort_f))
-            return false;
-          copy_next();
-        }
-        return true;
-      };
       constexpr uint32_t id_s = tc_idesc_f16(128, kTcStep);
       constexpr uint32_t id_o = tc_idesc_f16(128, D);
       const uint32_t qa = smem_u32(sm + PL::q + C * PL::QB);
@@ -359,7 +351,6 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
           tc_mma_f16_ts(to, tp + 32 + 8 * kk, sw128_desc(vta + kk * 32), id_o, 1u);
         tc_commit(&pv_done[C]);
       };
-      pump();
       int gbase = 0, n_done = 0;  // global steps before the item, items with steps done
       for (int item = blockIdx.x; item < n_items && !*abort_f; item += gridDim.x) {
         const WsItem it = ws_item<NT>(p, item);
@@ -372,7 +363,7 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
           if (j < it.nsteps) {
             // S of step j, once its record has landed and the tile has read
             // its previous S
-            ok = ensure(g) && tc_wait(&kv_full[g % NS], (g / NS) & 1, abort_f) &&
+            ok = tc_wait(&kv_full[g % NS], (g / NS) & 1, abort_f) &&
                  (g == 0 || tc_wait(&s_read[C], (g - 1) & 1, abort_f));
             if (!ok) break;
             tc_fence_after();
@@ -387,21 +378,15 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
             if (j == it.nsteps) tc_commit(&o_full[C]);
             tc_commit(&kv_empty[(g - 1) % NS]);  // this tile's MMAs reading that stage are issued
           }
-          pump();
         }
         if (!ok) break;
         gbase += it.nsteps;
         ++n_done;
       }
-      // every MMA has completed and every copy has landed before the CTA exits
+      // every MMA has completed before the CTA exits
       tc_commit(drain);
       bool ok = false;
       for (int tries = 0; tries < kWaitTries && !ok; ++tries) ok = mbar_try_wait(drain, 0);
-      for (int g = copied > NS ? copied - NS : 0; g < copied; ++g) {
-        ok = false;
-        for (int tries = 0; tries < kWaitTries && !ok; ++tries)
-          ok = mbar_try_wait(&kv_full[g % NS], (g / NS) & 1);
-      }
     }
   } else {
     // ======================= softmax rows of tile X =======================
