@@ -174,6 +174,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+// One arrival for the whole warp, after every lane's prior work (a warp-wide
+// arrive would be 32 atomic updates of the same word).  The lanes' shared
+// memory writes, tensor memory accesses (each lane fenced with
+// tcgen05.fence::before_thread_sync) and proxy fences are ordered before the
+// arrival by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Shared-memory plan of the attention pass (offsets from a 1024-byte aligned
 // base): Q tiles (and low parts), kWsStages record stages, misc.
 template <int D, int NT, bool CH>
@@ -259,8 +269,8 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
   uint64_t* kv_full = bars;                // [NS]: the step's record landed
   uint64_t* kv_empty = bars + NS;          // [NS]: every tile's MMAs of the step in that stage done
   uint64_t* s_full = bars + 2 * NS;        // [NT]: S of the tile's current step
-  uint64_t* s_read = s_full + NT;          // [NT]: the tile's 128 rows have read S
-  uint64_t* p_full = s_read + NT;          // [NT]: the tile's 128 rows have written P
+  uint64_t* s_read = s_full + NT;          // [NT]: the tile's 4 warps have read S
+  uint64_t* p_full = s_read + NT;          // [NT]: the tile's 4 warps have written P
   uint64_t* pv_done = p_full + NT;         // [NT]: the tile's last issued P.V done
   uint64_t* o_full = pv_done + NT;         // [NT]: the tile's final P.V of an item done
   uint64_t* q_full = o_full + NT;          // [NT]: the tile's Q rows of an item written
@@ -273,11 +283,11 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
     }
     for (int x = 0; x < NT; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&s_read[x], kTcRows);
-      mbar_init(&p_full[x], kTcRows);
+      mbar_init(&s_read[x], kTcRows / 32);  // one arrival per warp
+      mbar_init(&p_full[x], kTcRows / 32);  // one arrival per warp
       mbar_init(&pv_done[x], 1);
       mbar_init(&o_full[x], 1);
-      mbar_init(&q_full[x], kTcRows);
+      mbar_init(&q_full[x], kTcRows / 32);  // one arrival per warp
     }
     mbar_init(drain, NT);
     *abort_f = 0;
@@ -473,7 +483,7 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&q_full[X]);
+      warp_arrive(&q_full[X]);
       return csc;
     };
     WsItem it;
@@ -509,7 +519,7 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
           for (int i = 0; i < 32; ++i) z[32 + i] = a[i];
         }
         tc_fence_before();
-        mbar_arrive(&s_read[X]);  // the next S may go into this buffer
+        warp_arrive(&s_read[X]);  // the next S may go into this buffer
         const float* ksb = reinterpret_cast<const float*>(st + R::ks);
         const float* vsb = reinterpret_cast<const float*>(st + R::vs);
         const uint32_t mk0 = reinterpret_cast<const uint32_t*>(st + R::mask)[0];
@@ -617,7 +627,7 @@ __global__ void __launch_bounds__(WsPlan<D, WsShape<FMT>::NT, FmtTraits<FMT>::ch
         }
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[X]);
+        warp_arrive(&p_full[X]);
       }
       if (failed) break;
       // ---- the next item's Q now (the S products of this item, the last
