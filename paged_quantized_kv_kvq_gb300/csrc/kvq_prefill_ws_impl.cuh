@@ -164,13 +164,14 @@ struct WsShape {
 };
 
 // Wait on an mbarrier phase with one lane of the warp spinning (bounded, see
-// tc_wait); the other lanes then observe the completed phase with one
-// non-blocking test each.  Warp-uniform result.
+// tc_wait); the warp barrier then orders the other lanes' later accesses
+// after that lane's acquire (one test per lane instead would be 32 atomic
+// reads of the same word).  Warp-uniform result.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort);
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) mbar_test_wait(bar, parity);
+  __syncwarp();
   return ok;
 }
 
