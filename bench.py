@@ -185,52 +185,46 @@ def gpu_index(local_rank):
 
 
 # ----------------------------------------------------------------- kernel breakdown
-def kernel_breakdown(run, reps, layers, ms_step):
-    """Device time of each of this library's kernels over `reps` calls of
-    run() (one decode step each), from a CUPTI trace taken by torch.profiler
-    (read back from its Chrome-trace export); launches of a layer overlap
-    through programmatic dependent launch, so the per-layer sum may exceed the
-    step time per layer."""
-    import re
-    import tempfile
+LAUNCH_RECORDS = {"decode": os.path.join(ROOT, "profiles", "decode_launches.json"),
+                  "prefill": os.path.join(ROOT, "profiles", "prefill_launches.json")}
 
-    import torch
 
+def library_sha():
+    """Hash of every library source (kernels, launchers, the C ABI)."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "paged_quantized_kv_kvq_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(d, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "kvq.h"), "rb").read())
+    return h.hexdigest()
+
+
+def kernel_breakdown(kind, workload, layers, ms_step):
+    """Per-kernel device times of one layer's launches, from the committed ncu
+    launch list of this very library build (profiles/<kind>_launches.json,
+    `gpu__time_duration.sum`, launches serialised and cold), with each
+    kernel's share of the layer apportioned to this run's live step time
+    (live, a layer's launches overlap through programmatic dependent launch,
+    so the serialised sum exceeds the live time per layer).  Unavailable when
+    the record was taken on other sources or another workload."""
     try:
-        from torch.profiler import ProfilerActivity, profile
-    except Exception as e:  # noqa: BLE001 -- reported in the JSON line
-        return {"unavailable": str(e)[:120]}
-    torch.cuda.synchronize()
-    try:
-        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-            for _ in range(reps):
-                run()
-            torch.cuda.synchronize()
-        with tempfile.TemporaryDirectory() as d:
-            path = os.path.join(d, "trace.json")
-            prof.export_chrome_trace(path)
-            trace = json.load(open(path))
-    except Exception as e:  # noqa: BLE001
-        return {"unavailable": str(e)[:120]}
-    evs = trace.get("traceEvents", trace) if isinstance(trace, dict) else trace
-    acc = {}
-    for ev in evs:
-        if not isinstance(ev, dict) or ev.get("cat") != "kernel":
-            continue
-        m = re.search(r"(kvq_[a-z0-9_]+_kernel)", str(ev.get("name", "")))
-        if m is None:
-            continue
-        d = acc.setdefault(m.group(1), [0, 0.0])
-        d[0] += 1
-        d[1] += float(ev.get("dur", 0.0))
-    if not acc:
-        cats = sorted({str(e.get("cat")) for e in evs if isinstance(e, dict)})[:8]
-        return {"unavailable": "no kernel records in the trace (categories: %s)" % ", ".join(cats)}
-    out = {k: {"launches": n, "avg_us": round(t / n, 3),
-               "per_layer_us": round(t / (reps * layers), 3)} for k, (n, t) in sorted(acc.items())}
-    return {"kernels": out, "steps_traced": reps,
-            "sum_per_layer_us": round(sum(t for _, t in acc.values()) / (reps * layers), 3),
-            "step_per_layer_us": round(1e3 * ms_step / layers, 3)}
+        rec = json.load(open(LAUNCH_RECORDS[kind]))
+    except (OSError, ValueError) as e:
+        return {"unavailable": "no launch record: %s" % str(e)[:80]}
+    if rec.get("library_sha256") != library_sha() or rec.get("workload") != workload:
+        return {"unavailable": "the launch record was taken on other library sources or another "
+                               "workload (%s)" % rec.get("workload")}
+    ks = rec["kernels"]
+    tot = sum(k["avg_us"] * k["per_layer"] for k in ks.values())
+    live = 1e3 * ms_step / layers
+    out = {name: {"ncu_avg_us": k["avg_us"], "launches_per_layer": k["per_layer"],
+                  "share": round(k["avg_us"] * k["per_layer"] / tot, 4),
+                  "apportioned_live_us_per_layer": round(live * k["avg_us"] * k["per_layer"] / tot, 3)}
+           for name, k in ks.items()}
+    return {"kernels": out, "ncu_sum_per_layer_us": round(tot, 3),
+            "live_step_per_layer_us": round(live, 3), "source": rec.get("source", "")}
 
 
 # ----------------------------------------------------------------- oracle leg
@@ -610,7 +604,7 @@ def run_ours(args, rank, world, local_rank):
 
     # -- per-kernel device times of a few steps (a CUPTI trace, outside the
     # timed regions): explains the step time by its kernels
-    kernel_times = kernel_breakdown(timed_step, min(5, K), L, ms)
+    kernel_times = kernel_breakdown("decode", w.name if w.bs == 16 else "%s bs%d" % (w.name, w.bs), L, ms)
 
     b = step_bytes(w)
     step_total = b["decode"] + b["append"]
@@ -822,6 +816,8 @@ def run_prefill(args, rank, world, local_rank):
                                "one by one after the step region" % (KR * L),
                      "flop_per_launch": flop_layer, "avg_launch_ms": round(att_ms, 4),
                      "peak_source": "%s bf16_tflops_sustained (f16 has the bf16 rate)" % peak_kind},
+        "kernel_times": (kernel_breakdown("prefill", "%s prefill" % w.name, L, att_ms * L)
+                         if ex else {"unavailable": "launch record taken for kvq_prefill_ex"}),
         "gpu_launches": K * L * (3 if ex else 2),  # append, (staging,) attention
         "clocks": clocks,
     }
