@@ -23,11 +23,17 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
   // Pages in flight per SM = CTAs per SM x W x stages; 3 CTAs x 4 warps x 4
   // stages keeps ~200 KB of copies in flight, above what HBM latency needs.
   // Block size 8 consumes up to four pages per update, so keeps four stages.
+  // The stages are cut to what lets kDecodeCtasPerSm CTAs share an SM (228 KB,
+  // 1 KB of it reserved per CTA): a fourth stage of 4 KB pages that left room
+  // for only two CTAs (8 warps) cost more in latency hiding than it gave.
   const int min_stage = pool.bs == 8 ? 4 : 2;
+  auto smem_of = [&](int ns) {
+    return round_up(W * ns * stage_bytes + W * ns * (8 + 4) + W * 4 + (S + 1) * 4, 128);
+  };
+  const int budget = std::min(80 * 1024, 228 * 1024 / kDecodeCtasPerSm - 1024);
   int nstage = kDecodeStages;
-  while (nstage > min_stage && W * nstage * stage_bytes > 80 * 1024) --nstage;
-  const int smem = round_up(W * nstage * stage_bytes + W * nstage * (8 + 4) + W * 4 + (S + 1) * 4,
-                            128);
+  while (nstage > min_stage && smem_of(nstage) > budget) --nstage;
+  const int smem = smem_of(nstage);
   if (smem > 227 * 1024) return false;
   const int G = Hq / pool.Hkv;
   const int n_ht = (G + 7) / 8;
