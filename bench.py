@@ -301,6 +301,47 @@ def cpu_baseline(w, budget_s=12.0):
             "seconds": dt, "bytes": nbytes}
 
 
+def cpu_baseline_prefill(w, budget_s=12.0):
+    """Time the oracle (as it stands) on host cores on a bounded sample of the
+    prefill workload: layer 0, sequence 0's whole prompt appended, then the
+    causal attention of its last n query tokens (every Q head), n sized to
+    ~budget_s of work; TFLOP/s on the same algorithmic count as the GPU leg."""
+    import oracle
+    from paged_quantized_kv_kvq_gb300 import synth
+
+    oracle.build()
+    fmt, group = w.layer_formats[0]
+    Ls = int(w.context_lens[0])
+    nb = (Ls + w.bs - 1) // w.bs
+    cache = oracle.OracleCache(fmt, nb, w.bs, w.Hkv, w.D, group)
+    idx = np.stack([np.zeros(Ls, np.int64), np.arange(Ls, dtype=np.int64)], axis=1)
+    k, v = synth.kv_tokens(w, 0, idx)
+    if fmt == oracle.INT8_PER_CHANNEL:
+        cache.calibrate(k, v)
+    cache.append(k, v, np.arange(Ls, dtype=np.int64))
+    row = np.arange(nb, dtype=np.int32)
+    q_all = np.random.default_rng(11).standard_normal((Ls, w.Hq, w.D)).astype(np.float16)
+
+    def run(n):
+        lens = np.arange(Ls - n + 1, Ls + 1, dtype=np.int32)
+        cache.decode(q_all[Ls - n:], np.repeat(row[None], n, axis=0), lens)
+        return 4 * w.Hq * w.D * int(lens.astype(np.int64).sum())
+
+    t0 = time.perf_counter()
+    run(1)
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(Ls, round(budget_s / max(t1, 1e-4)))))
+    t0 = time.perf_counter()
+    flop = run(n)
+    dt = time.perf_counter() - t0
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": min(oracle.num_threads(), n * w.Hq),
+            "kind": "oracle",
+            "sample": "layer 0 of %d, sequence 0 (%d-token prompt appended), causal float64 attention "
+                      "of its last %d query tokens x %d heads: %.2f s of CPU work, %d algorithmic FLOP"
+                      % (w.layers, Ls, n, w.Hq, dt, flop),
+            "seconds": dt, "flop": flop}
+
+
 def workload_config(w):
     return {"workload": w.name, "layers": w.layers, "seqs": w.S,
             "context_lens": "%d..%d (mean %.0f)" % (w.context_lens.min(), w.context_lens.max(),
@@ -784,7 +825,65 @@ def run_prefill(args, rank, world, local_rank):
             attend(l)
             evs[i * L + l][1].record(stream)
     torch.cuda.synchronize()
+    # -- end to end: every step copies each layer's prompt K/V and Q in from
+    # pinned host memory and each layer's output back, on two copy streams
+    # that overlap the layers (layer l+1's inputs arrive while layer l runs;
+    # outputs alternate between two device buffers); one host copy of a
+    # layer's inputs stands for every layer's (the same bytes move)
+    k_h = kin[0].cpu().pin_memory()
+    v_h = vin[0].cpu().pin_memory()
+    q_h = qin[0].cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    outs = [out, torch.empty_like(out)]
+    cp_in, cp_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d = (k_h.numel() * k_h.element_size() + v_h.numel() * v_h.element_size() +
+           q_h.numel() * q_h.element_size()) * L
+    d2h = out_h.numel() * out_h.element_size() * L
+
+    def e2e_step():
+        in_ev, out_ev = [], []
+        cp_in.wait_stream(stream)
+        for l in range(L):
+            with torch.cuda.stream(cp_in):
+                kin[l].copy_(k_h, non_blocking=True)
+                vin[l].copy_(v_h, non_blocking=True)
+                qin[l].copy_(q_h, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cp_in)
+                in_ev.append(ev)
+        for l in range(L):
+            stream.wait_event(in_ev[l])
+            if l >= 2:
+                stream.wait_event(out_ev[l - 2])  # its output buffer has been read back
+            kvq.kvq_append(pools[l].handle, kin[l], vin[l], slots, stream)
+            o = outs[l % 2]
+            if ex:
+                kvq.kvq_prefill_ex(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, o,
+                                   ws, stream)
+            else:
+                kvq.kvq_prefill(pools[l].handle, qin[l], qs, mq, table, ln, mq, sm_scale, o,
+                                stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            cp_out.wait_event(ev)
+            with torch.cuda.stream(cp_out):
+                out_h.copy_(o, non_blocking=True)
+                ev2 = torch.cuda.Event()
+                ev2.record(cp_out)
+                out_ev.append(ev2)
+        stream.wait_stream(cp_out)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    K2 = max(1, min(K, 5))
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
     clocks = sampler.stop()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / K2, dist, dev)
     ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
     att_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
     pairs = int((lens * (lens + 1) // 2).sum())
@@ -816,6 +915,11 @@ def run_prefill(args, rank, world, local_rank):
                                "one by one after the step region" % (KR * L),
                      "flop_per_launch": flop_layer, "avg_launch_ms": round(att_ms, 4),
                      "peak_source": "%s bf16_tflops_sustained (f16 has the bf16 rate)" % peak_kind},
+        "e2e": {"value": round(world * flop_layer * L / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K2,
+                "overlap": "each layer's inputs on one copy stream ahead of the layers, each "
+                           "layer's output read back on another as it completes"},
         "kernel_times": (kernel_breakdown("prefill", "%s prefill" % w.name, L, att_ms * L)
                          if ex else {"unavailable": "launch record taken for kvq_prefill_ex"}),
         "gpu_launches": K * L * (3 if ex else 2),  # append, (staging,) attention
@@ -933,6 +1037,11 @@ def main():
     if args.op == "prefill":
         res = run_prefill(args, rank, world, local_rank)
         if rank == 0:
+            if world == 1 and not args.no_cpu_baseline:
+                from paged_quantized_kv_kvq_gb300 import synth
+
+                res["cpu_baseline"] = cpu_baseline_prefill(
+                    synth.workload(args.workload, S=args.prefill_seqs, layers=args.layers))
             print(json.dumps(res), flush=True)
         if world > 1:
             dist.destroy_process_group()
