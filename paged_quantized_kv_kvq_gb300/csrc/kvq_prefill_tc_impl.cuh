@@ -307,10 +307,25 @@ __global__ void __launch_bounds__(TcPlan<D, NT, FmtTraits<FMT>::channel>::thread
     const __half* src = row_ok ? p.q + orow * D : nullptr;
     char* qx = sm + PL::q + X * PL::QB;
     if constexpr (!CH) {
+      // the warp loads its 32 rows together: one instruction covers 256 / D
+      // whole rows (each row's source address comes from its owner lane); a
+      // batch of loads is issued before any of its shared-memory stores,
+      // which the compiler may not move loads past
+      constexpr int CPR = D / 8, RPI = 32 / CPR, NI = 32 / RPI, QBATCH = 8;
+      const int cj = lane % CPR, rj = lane / CPR;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = src ? *reinterpret_cast<const uint4*>(src + 8 * c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qx + sw128_offset(r, 8 * c, kTcRows)) = v;
+      for (int k0 = 0; k0 < NI; k0 += QBATCH) {
+        uint4 v[QBATCH];
+#pragma unroll
+        for (int b = 0; b < QBATCH; ++b) {
+          const __half* sj = reinterpret_cast<const __half*>(__shfl_sync(
+              0xffffffffu, reinterpret_cast<unsigned long long>(src), (k0 + b) * RPI + rj));
+          v[b] = sj ? *reinterpret_cast<const uint4*>(sj + 8 * cj) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < QBATCH; ++b)
+          *reinterpret_cast<uint4*>(qx + sw128_offset(r - lane + (k0 + b) * RPI + rj, 8 * cj,
+                                                      kTcRows)) = v[b];
       }
     } else {
       // fold the K channel scale into the row, scale it by 2^eq so that its
@@ -642,25 +657,43 @@ __global__ void __launch_bounds__(TcPlan<D, NT, FmtTraits<FMT>::channel>::thread
         tc_fence_after();
         const float f = l > 0.f ? pow2f(-E) / l : 0.f;
         const float* vch = CH ? pool.chan_scales + ((int64_t)pool.Hkv + h) * D : nullptr;
+        // Each warp passes 16-column blocks of its 32 rows through shared
+        // memory (the tile's weight buffer, free once its last P.V is done),
+        // so that a store instruction covers 8 rows x 64 contiguous bytes
+        // instead of 32 rows x 16 bytes.  Writer: lane = row, chunk q4 at
+        // position q4 ^ ((row / 2) % 4); reader: row 8k + lane / 4, chunk
+        // lane % 4 (both conflict-free).
+        float* scr = reinterpret_cast<float*>(sm + PL::pw + X * 2 * PL::PB) + (warp & 3) * (32 * 16);
+        const int rb = lane >> 2, cb = lane & 3;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           tc_ld32(tO + lane_base + 32 * c, o);
-          if (row_ok) {
-            float4* dst = reinterpret_cast<float4*>(p.out + orow * D + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 v = make_float4(o[4 * i] * f, o[4 * i + 1] * f, o[4 * i + 2] * f,
-                                     o[4 * i + 3] * f);
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float* oo = o + 16 * hh + 4 * q4;
+              float4 v = make_float4(oo[0] * f, oo[1] * f, oo[2] * f, oo[3] * f);
               if constexpr (CH) {
-                const float* cs = vch + 32 * c + 4 * i;
+                const float* cs = vch + 32 * c + 16 * hh + 4 * q4;
                 v.x *= cs[0];
                 v.y *= cs[1];
                 v.z *= cs[2];
                 v.w *= cs[3];
               }
-              dst[i] = v;
+              *reinterpret_cast<float4*>(scr + lane * 16 + 4 * (q4 ^ ((lane >> 1) & 3))) = v;
             }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int rw = 8 * k + rb;
+              const long long orow_k = __shfl_sync(0xffffffffu, static_cast<long long>(orow), rw);
+              const float4 v = *reinterpret_cast<const float4*>(scr + rw * 16 + 4 * (cb ^ ((rw >> 1) & 3)));
+              if (orow_k >= 0)
+                *reinterpret_cast<float4*>(p.out + orow_k * D + 32 * c + 16 * hh + 4 * cb) = v;
+            }
+            __syncwarp();
           }
         }
       }
