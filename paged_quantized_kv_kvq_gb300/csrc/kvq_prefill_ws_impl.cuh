@@ -21,13 +21,15 @@
 // one-pass kernel, so the arithmetic is the same; only where the fp16 copy
 // of the codes is made differs.
 //
-// The attention pass: a CTA takes one (sequence, kv head) and two tiles of
-// 128 Q rows (one tile for per-channel pools, whose Q has a low part too).
-// Its eight softmax warps own the rows (one row per thread, one TMEM lane
-// each); a copier thread bulk-copies the step records into four shared
-// memory stages the moment each is free, and one control thread per tile
-// issues that tile's tcgen05.mma.  Per tile, tensor memory holds the output
-// accumulator O, the step's scores S and the step's weights P:
+// The attention pass: a work item is one (sequence, kv head) and two tiles
+// of 128 Q rows (one tile for per-channel pools, whose Q has a low part too);
+// the grid is persistent, one CTA per SM taking every grid-th item, longest
+// items first.  The CTA's eight softmax warps own the rows (one row per
+// thread, one TMEM lane each); a copier thread bulk-copies the step records
+// into four shared-memory stages the moment each is free, running ahead
+// across items, and one control thread per tile issues that tile's
+// tcgen05.mma.  Per tile, tensor memory holds the output accumulator O, the
+// step's scores S and the step's weights P:
 //   * the control thread issues S = Q.K^T (M 128, N 64, K D, A and B from
 //     shared memory) for every tile once the step's record has landed and the
 //     tile has read its previous S;
@@ -40,7 +42,9 @@
 //   * the control thread then issues O += P_hi.V + P_lo.V (M 128, N D, K 64,
 //     A from tensor memory, V^T from shared memory).
 // So the next step's S is computed while the softmax of the current one runs,
-// and the two tiles' softmax and tensor work interleave.  The threads meet
+// and the two tiles' softmax and tensor work interleave.  The next item's Q
+// rows are loaded before the current item's epilogue, whose output rows go
+// out through a per-warp shared-memory transpose.  The threads meet
 // only at mbarriers; every wait is bounded and gives up early once another
 // role has given up; the CTA then flags a timeout, waits (bounded) for its
 // copies and MMAs in flight, and frees TMEM.
@@ -186,7 +190,8 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
 }
 
 // Shared-memory plan of the attention pass (offsets from a 1024-byte aligned
-// base): Q tiles (and low parts), kWsStages record stages, misc.
+// base): Q tiles (and low parts), kWsStages record stages, misc (flags and
+// mbarriers), the softmax warps' output transpose blocks.
 template <int D, int NT, bool CH>
 struct WsPlan {
   using R = StepRec<D>;
