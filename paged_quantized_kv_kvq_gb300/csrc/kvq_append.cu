@@ -89,6 +89,13 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
   // lengths, the block table and every page this append does not write (all
   // but each sequence's last page) before its own griddepcontrol.wait.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The row's first 16-byte chunk of each thread is loaded alongside the slot
+  // lookup (every token has its row, padding included), so the two round
+  // trips overlap.
+  const __half* x = (kv == 0 ? p.k : p.v) + t * p.x_stride;
+  const int per = pool.Hkv * pool.D;
+  const uint4 raw0 = threadIdx.x * 8 < per ? *reinterpret_cast<const uint4*>(x + threadIdx.x * 8)
+                                           : make_uint4(0, 0, 0, 0);
   int64_t slot;
   if (p.slots != nullptr) {
     slot = p.slots[t];
@@ -108,15 +115,13 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
   const int off = static_cast<int>(slot % pool.bs);
   const int sub = off >> 4, tt = off & 15;
   const int D = pool.D, Hkv = pool.Hkv;
-  const int per = Hkv * D;
-  const __half* x = (kv == 0 ? p.k : p.v) + t * p.x_stride;
 
   __shared__ float red[kAppendThreads / 32];
   float tok_scale = 0.f;
   if constexpr (FMT == FMT_INT8_TOKEN || FMT == FMT_FP8_TOKEN) {
     float a = 0.f;
     for (int c = threadIdx.x * 8; c < per; c += kAppendThreads * 8) {
-      uint4 raw = *reinterpret_cast<const uint4*>(x + c);
+      uint4 raw = c < kAppendThreads * 8 ? raw0 : *reinterpret_cast<const uint4*>(x + c);
       a = fmaxf(a, absmax8(*reinterpret_cast<__half2(*)[4]>(&raw)));
     }
 #pragma unroll
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kAppendThreads) kvq_append_kernel(const Append
     const int h = act ? c / D : 0, d0 = act ? c - h * D : 0;
     char* page = pool.pages + (blk * Hkv + h) * pool.page_bytes;
     char* tile = page + (kv == 0 ? 0 : pool.code_bytes) + sub * pool.sub_bytes;
-    uint4 raw = act ? *reinterpret_cast<const uint4*>(x + c) : make_uint4(0, 0, 0, 0);
+    uint4 raw = base == 0 ? raw0 : act ? *reinterpret_cast<const uint4*>(x + c) : make_uint4(0, 0, 0, 0);
     const __half2(&xv)[4] = *reinterpret_cast<const __half2(*)[4]>(&raw);
     float f[8];
 #pragma unroll
