@@ -19,16 +19,20 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
                  DecodePlan* plan) {
   constexpr int W = kDecodeWarps;
   const bool tok = pool.fmt == FMT_INT8_TOKEN || pool.fmt == FMT_FP8_TOKEN;
-  const int stage_bytes = round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
+  // Block size 8: a stage holds a pair of pages (two page slots) completing
+  // on one barrier.
+  const int sps = pool.bs == 8 ? 2 : 1;
+  const int stage_bytes = sps * round_up(pool.page_bytes + (tok ? 2 * pool.bs * 4 : 0), 128);
   // Pages in flight per SM = CTAs per SM x W x stages; 3 CTAs x 4 warps x 4
   // stages keeps ~200 KB of copies in flight, above what HBM latency needs.
-  // Block size 8 consumes up to four pages per update, so keeps four stages.
-  // The stages are cut to what lets kDecodeCtasPerSm CTAs share an SM (228 KB,
-  // 1 KB of it reserved per CTA): a fourth stage of 4 KB pages that left room
-  // for only two CTAs (8 warps) cost more in latency hiding than it gave.
-  const int min_stage = pool.bs == 8 ? 4 : 2;
+  // Block size 8 consumes up to four pages (three pairs) per update, so keeps
+  // at least three stages.  The stages are cut to what lets kDecodeCtasPerSm
+  // CTAs share an SM (228 KB, 1 KB of it reserved per CTA): a fourth stage of
+  // 4 KB pages that left room for only two CTAs (8 warps) cost more in
+  // latency hiding than it gave.
+  const int min_stage = pool.bs == 8 ? 3 : 2;
   auto smem_of = [&](int ns) {
-    return round_up(W * ns * stage_bytes + W * ns * (8 + 4) + W * 4 + (S + 1) * 4, 128);
+    return round_up(W * ns * stage_bytes + W * ns * (8 + 4 * sps) + W * 4 + (S + 1) * 4, 128);
   };
   const int budget = std::min(80 * 1024, 228 * 1024 / kDecodeCtasPerSm - 1024);
   int nstage = kDecodeStages;

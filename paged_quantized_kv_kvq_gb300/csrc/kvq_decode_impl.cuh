@@ -626,9 +626,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   char* stages = smem + warp * nstage * p.stage_bytes;
   uint64_t* bars_base = reinterpret_cast<uint64_t*>(smem + kDecodeWarps * nstage * p.stage_bytes);
   uint64_t* bars = bars_base + warp * nstage;
+  // block size 8: a stage holds two consecutive pages of the range (slots 0
+  // and 1, stage_bytes / 2 apart) completing on one barrier
+  constexpr int SPS = BS8 ? 2 : 1;  // pages per stage
   int* phys_base = reinterpret_cast<int*>(bars_base + kDecodeWarps * nstage);
-  int* stage_phys = phys_base + warp * nstage;
-  int* wtot = phys_base + kDecodeWarps * nstage;  // [kDecodeWarps]
+  int* stage_phys = phys_base + warp * nstage * SPS;
+  int* wtot = phys_base + kDecodeWarps * nstage * SPS;  // [kDecodeWarps]
   int* PS = wtot + kDecodeWarps;                  // [S + 1] page prefix over sequences
 
   // ---- pages per sequence and their prefix (every CTA computes the same)
@@ -784,6 +787,57 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     ++n_issued;
     if (++pst == nstage) pst = 0;
   };
+  // Block size 8: issue pages n_issued and n_issued + 1 (when in the range)
+  // into the next stage, their copies completing on its one barrier.  All
+  // lanes call this; lane 0 issues.  n_issued is even here, so both table
+  // entries sit in tcur.
+  const int slot_bytes = p.stage_bytes / 2;
+  auto issue_pair = [&]() {
+    if (n_issued - tbase == 32) {
+      tcur = tnext;
+      tbase += 32;
+      tnext = table_entry(tbase + 32 + lane);
+    }
+    const bool two = n_issued + 1 < n_w;
+    const int ph0 = __shfl_sync(0xffffffffu, tcur, n_issued - tbase);
+    const int ph1 = __shfl_sync(0xffffffffu, tcur, (n_issued + 1 - tbase) & 31);
+    if (lane == 0) {
+      const int st = pst;
+      int phys[2] = {ph0, ph1}, hh[2] = {0, 0};
+      bool ok[2] = {false, false};
+      uint32_t tx = 0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (k == 1 && !two) {
+          stage_phys[2 * st + 1] = -1;
+          continue;
+        }
+        ok[k] = phys[k] >= 0 && (int64_t)phys[k] < pool.num_blocks;
+        stage_phys[2 * st + k] = ok[k] ? phys[k] : -1;
+        hh[k] = p.n_ht == 1 ? ic.lu : ic.lu / p.n_ht;
+        if (ok[k]) tx += page_tx; else set_error(pool.err, ERR_RANGE);
+        advance(ic);
+      }
+      if (tx == 0) {
+        mbar_arrive(&bars[st]);
+      } else {
+        mbar_arrive_expect_tx(&bars[st], tx);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (!ok[k]) continue;
+          if (p.fault_issue >= 0 && gw == 0 && n_issued + k == p.fault_issue) continue;  // never comes
+          char* dst = stages + st * p.stage_bytes + k * slot_bytes;
+          bulk_g2s(dst, pool.pages + ((int64_t)phys[k] * pool.Hkv + hh[k]) * pool.page_bytes,
+                   pool.page_bytes, &bars[st]);
+          if constexpr (T::token_scales)
+            bulk_g2s(dst + pool.page_bytes, pool.tok_scales + (int64_t)phys[k] * 2 * bs, 2 * bs * 4,
+                     &bars[st]);
+        }
+      }
+    }
+    n_issued += two ? 2 : 1;
+    if (++pst == nstage) pst = 0;
+  };
   // Everything above reads only inputs (lengths, block table).  When the
   // decode is a programmatic dependent of the decode-step append (directly or
   // through the prefix kernel), that append launched this grid only after
@@ -792,7 +846,19 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
   // the first stages are filled before griddepcontrol.wait up to the first
   // last page, and the rest after it; without a dependency the wait returns
   // at once.
-  {
+  if constexpr (BS8) {
+    int k = 0;
+    for (; k < nstage && n_issued < n_w; ++k) {
+      Cursor c2 = ic;
+      advance(c2);
+      const bool last = __shfl_sync(
+          0xffffffffu, ic.pi + 1 == ic.Ps || (n_issued + 1 < n_w && c2.pi + 1 == c2.Ps), 0);
+      if (last) break;
+      issue_pair();
+    }
+    after_wait();
+    for (; k < nstage && n_issued < n_w; ++k) issue_pair();
+  } else {
     const int npre = min(n_w, nstage);
     int k = 0;
     for (; k < npre; ++k) {
@@ -934,7 +1000,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     else
       npg = (bs == 16 && i + 1 < n_w && cc.pi + 1 < cc.Ps) ? 2 : 1;
     auto issue_after = [&]() {
-      for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
+      if constexpr (BS8) {
+        // a pair's stage is free once both its pages are consumed
+        while (n_issued < n_w && i + npg >= n_issued + 2 - 2 * nstage) issue_pair();
+      } else {
+        for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
+      }
     };
     if constexpr (BS8) {
       bool ok = true;
@@ -945,11 +1016,15 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
         pg[k] = nullptr;
         rp[k] = 0;
         if (k < npg && ok) {
-          const bool wrap = cst + k >= nstage;  // nstage >= 4 for block size 8
-          const int st = wrap ? cst + k - nstage : cst + k;
-          ok = wait_stage(st, wrap ? cph ^ 1u : cph);
-          pg[k] = stages + st * p.stage_bytes;
-          rp[k] = stage_phys[st] >= 0 ? max(0, min(8, L - (cc.pi + k) * 8)) : 0;
+          // page q = i + k is slot q % 2 of pair q / 2; cst is the stage of
+          // pair i / 2 (nstage >= 3 pairs for block size 8); a slot-1 page's
+          // pair was waited with its slot 0, in this update or the one before
+          const int q = i + k, po = (q >> 1) - (i >> 1);
+          const bool wrap = cst + po >= nstage;
+          const int st = wrap ? cst + po - nstage : cst + po;
+          if ((q & 1) == 0) ok = wait_stage(st, wrap ? cph ^ 1u : cph);
+          pg[k] = stages + st * p.stage_bytes + (q & 1) * slot_bytes;
+          rp[k] = stage_phys[2 * st + (q & 1)] >= 0 ? max(0, min(8, L - (cc.pi + k) * 8)) : 0;
         }
       }
       if (!ok) {
@@ -1008,12 +1083,15 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     __syncwarp();
     issue_after();
     // advance the consumer; close the unit at its last page or at the range end
+    {
+      const int nst = BS8 ? ((i + npg) >> 1) - (i >> 1) : npg;  // stages passed
+      for (int k = 0; k < nst; ++k)
+        if (++cst == nstage) {
+          cst = 0;
+          cph ^= 1u;
+        }
+    }
     i += npg;
-    for (int k = 0; k < npg; ++k)
-      if (++cst == nstage) {
-        cst = 0;
-        cph ^= 1u;
-      }
     const Cursor done = cc;
     const int end_pi = cc.pi + npg;
     for (int k = 0; k < npg; ++k) advance(cc);
@@ -1035,7 +1113,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
     }
     int st = cst;
     uint32_t ph = cph;
-    for (int k = i; k < n_issued; ++k) {
+    // stages issued and not yet consumed (block size 8: pairs, from the one
+    // holding page i)
+    const int nst = BS8 ? ((n_issued + 1) >> 1) - (i >> 1) : n_issued - i;
+    for (int k = 0; k < nst; ++k) {
       wait_stage(st, ph);
       if (++st == nstage) {
         st = 0;
