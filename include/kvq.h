@@ -411,6 +411,27 @@ kvq_status kvq_get_error(kvq_pool* pool, cudaStream_t stream);
 /* Static description of a status code (never NULL). */
 const char* kvq_status_string(kvq_status status);
 
+/* Per-kernel timing (a measurement aid; no result depends on it).  A library
+ * call may run several kernels (kvq_paged_decode: the decode kernel, then the
+ * split merge; kvq_decode_step: the append, the decode, the merge;
+ * kvq_prefill_ex: the staging kernel, then the attention kernel).  This call
+ * hands the calling host thread's next n kernel launches one event each:
+ * right after the library launches its k-th kernel from now (k = 0 .. n-1,
+ * counted across calls, on this thread only), it records events[k] on that
+ * kernel's stream.  With an event of the caller's own recorded just before
+ * the call, the differences time each kernel on the device.  A launch that
+ * would follow a recorded event as a programmatic dependent just waits for it
+ * instead (no overlap), so timed kernels run one after another.  After n
+ * launches nothing more is recorded; a new call replaces what is left, and
+ * n = 0 (events may then be NULL) clears it.
+ *   events : host array of n CUDA events (cudaEvent_t), created and owned by
+ *            the caller; copied, so the array may be reused after the call
+ *   n      : 0 .. KVQ_MAX_PHASE_EVENTS
+ * Returns KVQ_ERR_INVALID_ARG for n outside that range or NULL events with
+ * n > 0; a failed record makes the launching call return KVQ_ERR_CUDA. */
+#define KVQ_MAX_PHASE_EVENTS 8
+kvq_status kvq_set_phase_events(const cudaEvent_t* events, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -110,6 +110,7 @@ def _declare(L):
         "kvq_read_slots": (i32, [P, P, i64, P, P, P]),
         "kvq_get_error": (i32, [P, P]),
         "kvq_status_string": (ctypes.c_char_p, [i32]),
+        "kvq_set_phase_events": (i32, [P, i32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -410,6 +411,19 @@ def kvq_read_slots(pool, slots, codes_out, scales_out=None, stream=None) -> None
 def kvq_get_error(pool, stream=None) -> int:
     """Synchronises the stream; returns (and clears) the pool's device error status."""
     return int(lib().kvq_get_error(pool, _stream(stream)))
+
+
+def kvq_set_phase_events(events) -> None:
+    """Measurement aid: the calling thread's next len(events) kernel launches
+    by the library each record one of these torch.cuda.Event objects on their
+    stream right after the launch (an empty list clears them; see kvq.h)."""
+    handles = []
+    for ev in events:
+        if not ev.cuda_event:  # torch creates the CUDA event at its first record
+            ev.record()
+        handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * len(handles))(*handles) if handles else None
+    _check(lib().kvq_set_phase_events(arr, len(handles)), "kvq_set_phase_events")
 
 
 # ------------------------------------------------------------------ convenience

@@ -6,9 +6,28 @@
 
 #include "kvq.h"
 #include "kvq_common.cuh"
+#include "kvq_context.h"
 #include "kvq_internal.h"
 
 using kvq::PoolView;
+
+namespace {
+
+// Events handed to this host thread's next kernel launches
+// (kvq_set_phase_events).
+struct PhaseEvents {
+  cudaEvent_t ev[KVQ_MAX_PHASE_EVENTS] = {};
+  int n = 0;     // registered
+  int next = 0;  // the next launch records ev[next] while next < n
+};
+thread_local PhaseEvents t_phase;
+
+}  // namespace
+
+cudaError_t kvq::phase_mark(cudaStream_t st, cudaError_t launched) {
+  if (launched != cudaSuccess || t_phase.next >= t_phase.n) return launched;
+  return cudaEventRecord(t_phase.ev[t_phase.next++], st);
+}
 
 struct kvq_pool {
   PoolView view;
@@ -557,6 +576,14 @@ kvq_status kvq_get_error(kvq_pool* pool, cudaStream_t stream) {
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   if (host & kvq::ERR_RANGE) return KVQ_ERR_OUT_OF_RANGE;
   if (host & kvq::ERR_TIMEOUT) return KVQ_ERR_TIMEOUT;
+  return KVQ_OK;
+}
+
+kvq_status kvq_set_phase_events(const cudaEvent_t* events, int n) {
+  if (n < 0 || n > KVQ_MAX_PHASE_EVENTS || (n > 0 && events == nullptr)) return KVQ_ERR_INVALID_ARG;
+  for (int k = 0; k < n; ++k) t_phase.ev[k] = events[k];
+  t_phase.n = n;
+  t_phase.next = 0;
   return KVQ_OK;
 }
 

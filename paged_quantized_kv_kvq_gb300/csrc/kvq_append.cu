@@ -16,6 +16,7 @@
 #include <cuda_fp8.h>
 
 #include "kvq_common.cuh"
+#include "kvq_context.h"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -342,7 +343,7 @@ cudaError_t launch_copy_blocks(const PoolView& pool, const int* src, const int* 
                                cudaStream_t st) {
   if (n == 0) return cudaSuccess;
   kvq_copy_blocks_kernel<<<dim3(static_cast<unsigned>(n), pool.Hkv), 128, 0, st>>>(pool, src, dst, n);
-  return cudaGetLastError();
+  return phase_mark(st, cudaGetLastError());
 }
 
 cudaError_t launch_append(const PoolView& pool, const __half* k, const __half* v,
@@ -364,7 +365,7 @@ cudaError_t launch_append_fmt(const AppendParams& p, dim3 grid, cudaStream_t st,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kvq_append_kernel<FMT>, p);
+  return phase_mark(st, cudaLaunchKernelEx(&cfg, kvq_append_kernel<FMT>, p));
 }
 
 }  // namespace
@@ -399,8 +400,10 @@ cudaError_t launch_calibrate(const PoolView& pool, const __half* k, const __half
   dim3 grid((C + 255) / 256, 2, static_cast<unsigned>(nz < 65535 ? nz : 65535));
   const int64_t ch = (T + grid.z - 1) / grid.z;
   kvq_calib_absmax_kernel<<<grid, 256, 0, st>>>(pool, k, v, T, ch);
+  e = phase_mark(st, cudaGetLastError());
+  if (e != cudaSuccess) return e;
   kvq_calib_finish_kernel<<<(2 * C + 255) / 256, 256, 0, st>>>(pool);
-  return cudaGetLastError();
+  return phase_mark(st, cudaGetLastError());
 }
 
 cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_t n,
@@ -408,7 +411,7 @@ cudaError_t launch_read_slots(const PoolView& pool, const int64_t* slots, int64_
   if (n == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(n), 2);
   kvq_read_slots_kernel<<<grid, 256, 0, st>>>(pool, slots, n, codes_out, scales_out);
-  return cudaGetLastError();
+  return phase_mark(st, cudaGetLastError());
 }
 
 }  // namespace kvq

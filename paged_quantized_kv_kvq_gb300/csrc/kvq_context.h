@@ -1,4 +1,5 @@
-// kvq_context.h -- host-side bookkeeping of per-CUDA-context set-up.
+// kvq_context.h -- host-side bookkeeping of per-CUDA-context set-up, and the
+// per-thread hook that records timing events after kernel launches.
 //
 // Some set-up is done once and then remembered: a kernel's opt-in to more
 // than 48 KB of dynamic shared memory (cudaFuncSetAttribute), and the device
@@ -86,6 +87,13 @@ class PerContext {
   V vals_[kSlots] = {};
   int next_ = 0;
 };
+
+// Per-kernel timing events (kvq_set_phase_events): every kernel launch of the
+// library passes its launch status through this, right after the launch, on
+// the kernel's stream.  On success it records the calling thread's next
+// registered event, if one is left; the launch's error otherwise.  Defined in
+// kvq_api.cu.
+cudaError_t phase_mark(cudaStream_t st, cudaError_t launched);
 
 // Opt a kernel in to up to 227 KB of dynamic shared memory, once per
 // context (one cache per kernel: the kernel is a template argument).

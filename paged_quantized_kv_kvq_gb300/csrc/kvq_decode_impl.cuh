@@ -1244,7 +1244,7 @@ cudaError_t run_decode(const DecodeLaunch& l) {
     da[0].val.programmaticStreamSerializationAllowed = 1;
     dc.attrs = da;
     dc.numAttrs = l.dependent ? 1 : 0;
-    e = cudaLaunchKernelEx(&dc, kvq_decode_kernel<FMT, D, NG, BS8>, l.p);
+    e = phase_mark(l.st, cudaLaunchKernelEx(&dc, kvq_decode_kernel<FMT, D, NG, BS8>, l.p));
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1257,7 +1257,7 @@ cudaError_t run_decode(const DecodeLaunch& l) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D>, l.p);
+  return phase_mark(l.st, cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D>, l.p));
 }
 
 template <int FMT, bool BS8 = false>

@@ -469,7 +469,7 @@ cudaError_t run_prefill(const PrefillLaunch& l) {
   cudaError_t e = allow_big_smem<kvq_prefill_kernel<FMT, D, NG>>();
   if (e != cudaSuccess) return e;
   kvq_prefill_kernel<FMT, D, NG><<<l.grid, kPfThreads, l.smem, l.st>>>(l.p);
-  return cudaGetLastError();
+  return phase_mark(l.st, cudaGetLastError());
 }
 
 }  // namespace kvq

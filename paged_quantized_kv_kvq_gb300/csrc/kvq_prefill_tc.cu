@@ -85,7 +85,7 @@ cudaError_t run_ws(const StageParams& sp, const PrefillWsParams& ap, int64_t nti
   const int64_t sgrid = (int64_t)sp.S * sp.max_steps * sp.pool.Hkv;
   if (sgrid > 0x7fffffffLL) return cudaErrorInvalidValue;
   kvq_prefill_stage_kernel<FMT, D><<<static_cast<unsigned>(sgrid), 128, 0, st>>>(sp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = phase_mark(st, cudaGetLastError());
   if (e != cudaSuccess) return e;
   PrefillWsParams a = ap;
   const int64_t ngroups = (ntiles + NT - 1) / NT;
@@ -102,7 +102,7 @@ cudaError_t run_ws(const StageParams& sp, const PrefillWsParams& ap, int64_t nti
   e = allow_big_smem<kvq_prefill_ws_kernel<FMT, D>>();
   if (e != cudaSuccess) return e;
   kvq_prefill_ws_kernel<FMT, D><<<static_cast<unsigned>(grid), PL::threads, PL::request, st>>>(a);
-  return cudaGetLastError();
+  return phase_mark(st, cudaGetLastError());
 }
 
 template <int FMT>

@@ -724,7 +724,7 @@ cudaError_t run_prefill_tc(const PrefillTcLaunch& l) {
   cudaError_t e = allow_big_smem<kvq_prefill_tc_kernel<FMT, D, NT>>();
   if (e != cudaSuccess) return e;
   kvq_prefill_tc_kernel<FMT, D, NT><<<l.grid, PL::threads, PL::request, l.st>>>(l.p);
-  return cudaGetLastError();
+  return phase_mark(l.st, cudaGetLastError());
 }
 
 }  // namespace kvq

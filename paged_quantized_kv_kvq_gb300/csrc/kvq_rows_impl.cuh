@@ -502,7 +502,7 @@ cudaError_t run_rows(const RowsLaunch& l) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = l.dependent ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kvq_rows_kernel<FMT, D, NG>, l.p);
+  return phase_mark(l.st, cudaLaunchKernelEx(&cfg, kvq_rows_kernel<FMT, D, NG>, l.p));
 }
 
 }  // namespace kvq

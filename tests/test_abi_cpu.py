@@ -25,6 +25,24 @@ def test_exports_every_declared_symbol(L):
         assert isinstance(getattr(L, n), ctypes._CFuncPtr)
 
 
+def test_phase_event_argument_checks(L):
+    """kvq_set_phase_events only stores handles (no CUDA call): its range and
+    NULL checks run without a GPU, and n = 0 clears whatever was set."""
+    arr = (ctypes.c_void_p * 9)()
+    assert L.kvq_set_phase_events(None, 0) == kvq.KVQ_OK
+    assert L.kvq_set_phase_events(None, 1) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_set_phase_events(arr, -1) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_set_phase_events(arr, 9) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_set_phase_events(arr, 8) == kvq.KVQ_OK
+    assert L.kvq_set_phase_events(None, 0) == kvq.KVQ_OK
+    class Ev:  # stands in for a torch.cuda.Event whose CUDA event exists
+        cuda_event = 1
+
+    with pytest.raises(kvq.KVQError):
+        kvq.kvq_set_phase_events([Ev()] * 9)
+    kvq.kvq_set_phase_events([])
+
+
 def test_status_strings(L):
     for st in range(7):
         assert kvq.kvq_status_string(st)
