@@ -428,7 +428,9 @@ const char* kvq_status_string(kvq_status status);
  *            the caller; copied, so the array may be reused after the call
  *   n      : 0 .. KVQ_MAX_PHASE_EVENTS
  * Returns KVQ_ERR_INVALID_ARG for n outside that range or NULL events with
- * n > 0; a failed record makes the launching call return KVQ_ERR_CUDA. */
+ * n > 0.  A record that fails (an event of another device, say) makes the
+ * launching call return KVQ_ERR_CUDA without launching that call's later
+ * kernels, so its results are then undefined. */
 #define KVQ_MAX_PHASE_EVENTS 8
 kvq_status kvq_set_phase_events(const cudaEvent_t* events, int n);
 

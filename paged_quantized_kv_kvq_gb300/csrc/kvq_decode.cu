@@ -63,8 +63,9 @@ bool plan_decode(const PoolView& pool, int S, int Hq, int max_ctx, int split_blo
   plan->stage_bytes = stage_bytes;
   plan->smem_bytes = smem;
   plan->ps_bytes = round_up_sz((size_t)(S + 1) * sizeof(int), 256);
-  // one warp per (unit, head row); enough CTAs to cover every task once
-  const int64_t merge_tasks = units * kPartRows;
+  // one warp per (unit, head row that a Q head fills); enough CTAs to cover
+  // every task once
+  const int64_t merge_tasks = units * std::min(kPartRows, G);
   plan->merge_grid = static_cast<int>(std::max<int64_t>(
       1, std::min<int64_t>((merge_tasks + kMergeThreads / 32 - 1) / (kMergeThreads / 32),
                            16LL * std::max(sms, 1))));

@@ -52,7 +52,7 @@ constexpr int kDecodeStages = 8;     // shared-memory stages per warp (at most; 
 constexpr int kDecodeCtasPerSm = 3;  // resident CTAs per SM the grid is sized for
 constexpr int kDecodeThreads = kDecodeWarps * 32;
 constexpr int kPartRows = 8;       // partial rows per (warp, slot): one per Q head of a tile
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
 
 struct DecodeParams {
   PoolView pool;
@@ -1149,12 +1149,15 @@ __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodePa
   const int nwarps = p.grid * kDecodeWarps;
   const int ppw = p.ppw_fixed > 0 ? p.ppw_fixed : (Ttot + nwarps - 1) / nwarps;
   if (ppw <= 0) return;
-  // one task per (unit, Q-head row of its tile); one warp per task
-  const int64_t ntasks = (int64_t)p.S * U * kPartRows;
+  // one task per (unit, Q-head row of its tile) that a Q head fills: rows
+  // 0 .. min(8, G) - 1 of each tile (fewer in a ragged last tile); one warp
+  // per task
+  const int rpu = min(kPartRows, p.G);
+  const int64_t ntasks = (int64_t)p.S * U * rpu;
   for (int64_t task = (int64_t)blockIdx.x * NW + (threadIdx.x >> 5); task < ntasks;
        task += (int64_t)gridDim.x * NW) {
-    const int64_t u = task / kPartRows;
-    const int rr = (int)(task % kPartRows);
+    const int64_t u = task / rpu;
+    const int rr = (int)(task % rpu);
     const int s = (int)(u / U), lu = (int)(u % U);
     const int ht = lu % p.n_ht;
     if (rr >= min(8, p.G - 8 * ht)) continue;
