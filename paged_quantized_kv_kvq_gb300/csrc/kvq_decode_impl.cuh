@@ -1130,8 +1130,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
 // unit u's pieces are the partials of warps wf..wl (slot 1 of wf when its range
 // started before the unit, slot 0 otherwise).  Launched as a programmatic
 // dependent of the decode kernel: griddepcontrol.wait returns once the decode
-// grid has completed and its writes are visible.
-template <int D>
+// grid has completed and its writes are visible.  CH: pieces loaded together
+// (one round trip), 8 or 16 as the plan chooses.
+template <int D, int CH>
 __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodeParams p) {
   // A kernel launched after this one as a programmatic dependent (the next
   // decode-step append) may launch now; it waits for this grid's completion
@@ -1141,7 +1142,6 @@ __global__ void __launch_bounds__(kMergeThreads) kvq_merge_kernel(const DecodePa
   const float kNegInf = __int_as_float(0xff800000u);
   constexpr int NW = kMergeThreads / 32;
   constexpr int NE = D / 32;   // output elements per lane
-  constexpr int CH = 8;        // pieces loaded together (one round trip)
   const int lane = threadIdx.x & 31;
   const int U = p.pool.Hkv * p.n_ht;
   const int* PS = p.ps;
@@ -1227,6 +1227,7 @@ struct DecodeLaunch {
   DecodeParams p;
   dim3 grid;
   unsigned merge_grid;
+  int merge_chunk;  // kvq_merge_kernel's CH
   int smem;
   cudaStream_t st;
   bool dependent;  // launch as a programmatic dependent of the previous kernel
@@ -1260,7 +1261,9 @@ cudaError_t run_decode(const DecodeLaunch& l) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return phase_mark(l.st, cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D>, l.p));
+  return phase_mark(l.st, l.merge_chunk == 16
+                              ? cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D, 16>, l.p)
+                              : cudaLaunchKernelEx(&cfg, kvq_merge_kernel<D, 8>, l.p));
 }
 
 template <int FMT, bool BS8 = false>

@@ -37,6 +37,7 @@ struct DecodePlan {
   int stage_bytes = 0;  // bytes of one stage
   int smem_bytes = 0;   // dynamic shared memory per CTA
   int merge_grid = 0;   // CTAs of the merge kernel
+  int merge_chunk = 8;  // pieces the merge loads per round trip
   size_t ps_bytes = 0;  // page prefix at the start of the workspace
   size_t ws_bytes = 0;  // page prefix + split partials
 };
