@@ -1007,7 +1007,34 @@ __global__ void __launch_bounds__(kDecodeThreads, kDecodeCtasPerSm)
         for (int k = 0; k < npg && n_issued < n_w; ++k) issue_next();
       }
     };
+    // Block size 8, the common case: four whole pages, i.e. two whole pairs
+    // (16 tokens each) in consecutive stages, taken without the per-page
+    // bookkeeping of the general path below (which handles a pair split by
+    // the range, short or absent pages and unit ends).
+    bool pairs_whole = false;
     if constexpr (BS8) {
+      if (npg == 4 && (i & 1) == 0 && (cc.pi + 4) * 8 <= L) {
+        const bool wrap1 = cst + 1 == nstage;
+        const int st1 = wrap1 ? 0 : cst + 1;
+        const int2 ph0 = *reinterpret_cast<const int2*>(stage_phys + 2 * cst);
+        const int2 ph1 = *reinterpret_cast<const int2*>(stage_phys + 2 * st1);
+        if ((ph0.x | ph0.y | ph1.x | ph1.y) >= 0) {  // all four pages in the pool
+          pairs_whole = true;
+          if (!wait_stage(cst, cph) || !wait_stage(st1, wrap1 ? cph ^ 1u : cph)) {
+            failed = true;
+            break;
+          }
+          const char* s0 = stages + cst * p.stage_bytes;
+          const char* s1 = stages + st1 * p.stage_bytes;
+          load_tile8<FMT, D, NG>(R, 0, s0, s0 + slot_bytes, 16, pool, lane);
+          load_tile8<FMT, D, NG>(R, 1, s1, s1 + slot_bytes, 16, pool, lane);
+          compute_pair<FMT, D, NG, true>(R, lane, qb, ql, csc, m, l, E, o);
+        }
+      }
+    }
+    if (pairs_whole) {
+      // done above
+    } else if constexpr (BS8) {
       bool ok = true;
       const char* pg[4];
       int rp[4];
