@@ -181,6 +181,25 @@ def test_split_k_invariance(bs):
     pool.close()
 
 
+@pytest.mark.parametrize("bs", [16, 32])
+def test_split_merge_chunks(bs):
+    """Warp ranges of 1024 tokens or more make the merge load 16 pieces per
+    round trip: 21 pieces per unit (a whole chunk and a partial one) and 12
+    (one partial chunk), and one-page pieces (1500 or 750 per unit, many
+    chunks of 8), each against the oracle.  The bound is tighter than the
+    path's 1e-3: with ranges of at most 2048 tokens the tensor cores' fp32
+    accumulation of P.V stays within ~4e-5 here (a single 24000-token range
+    drifts to ~5e-4; the error grows with the tokens one accumulator sums)."""
+    w = synth.workload("long_8x32k", S=1, L=24000, bs=bs, layers=1)
+    pool, ref, table, _ = _layer_case(w, 0, *w.layer_formats[0])
+    q = synth.queries(w, 0)
+    exp = ref.decode(q, table, w.context_lens)
+    for sb in (1152 // bs, 2048 // bs, 1):
+        np.testing.assert_allclose(run_gpu_decode(pool, w, q, DEV, split_blocks=sb), exp,
+                                   rtol=0, atol=1e-4, err_msg="split_blocks=%d" % sb)
+    pool.close()
+
+
 def test_gqa_ratios_and_head_tiles():
     # MQA (32 Q heads over 1 KV head: four head tiles) and GQA 12:1 (a ragged tile)
     for hq, hkv in ((32, 1), (24, 2), (4, 4)):
