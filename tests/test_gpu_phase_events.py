@@ -119,3 +119,31 @@ def test_phase_events_cleared():
     torch.cuda.synchronize()
     assert ev[0].elapsed_time(ev[1]) == stamp
     pool.close()
+
+
+def test_phase_events_split_the_cascade_and_carry_over():
+    """The cascade's three kernels (shared-prefix rows, decode, merge) each
+    take an event; events beyond one call's launches go to the next call's
+    (the count runs across calls): five events over a cascade call (three
+    launches) and a plain decode call (two)."""
+    w = synth.workload("mixed_256", S=4, L=100, layers=1)
+    fmt, group = w.layer_formats[0]
+    k, v, slots = layer_tokens(w, 0)
+    pool = gpu_pool(w, fmt, group, DEV, k, v, slots)
+    q, table, lens = _t(synth.queries(w, 0)), _t(w.block_table), _t(w.context_lens)
+    L = int(w.context_lens.max())
+    P = w.shared_prefix_tokens // w.bs
+    plain = pool.cascade_decode(q, table, lens, L, P)
+    torch.cuda.synchronize()
+    ev = _events(6)
+    kvq.kvq_set_phase_events(ev[1:])
+    ev[0].record()
+    timed = pool.cascade_decode(q, table, lens, L, P)   # rows, decode, merge: ev[1..3]
+    dec = pool.decode(q, table, lens, L)                # decode, merge: ev[4..5]
+    torch.cuda.synchronize()
+    assert pool.error() == kvq.KVQ_OK
+    assert torch.equal(plain, timed)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t >= 0 for t in times) and times[1] > 0 and times[3] > 0
+    np.testing.assert_allclose(dec.cpu().numpy(), timed.cpu().numpy(), rtol=0, atol=3e-5)
+    pool.close()
